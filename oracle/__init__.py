@@ -1,0 +1,153 @@
+"""fp64 CPU oracle for Subsampling Global Attention (SGA).
+
+TEST INFRASTRUCTURE ONLY: the test-suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg are the only callers.  The product package never imports this module and
+shares no code with it.  The arithmetic lives in ``sga_oracle.c`` (plain C, fp64, OpenMP over
+query rows); this file compiles it with gcc and marshals numpy arrays through ctypes.
+
+Pages followed (by title and section): "AVGGT: Rethinking Global Attention for Accelerating
+VGGT" Key designs 1-3; "RegimeVGGT: Layer-Wise Spatially Preserving Redundancy Removal for
+Visual Geometry Grounded Transformer" Core mechanism and Key designs 2-3.  The readings taken
+where the pages are silent are listed at the top of ``sga_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sga_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``sga_oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", _LIB_PATH, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        p = ctypes.c_void_p
+        i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.oracle_plan.restype = i64
+        lib.oracle_plan.argtypes = [i32] * 8 + [p, p, p]
+        lib.oracle_dropped_sums.restype = i64
+        lib.oracle_dropped_sums.argtypes = [i64, i32, p, p, p, p, p]
+        lib.oracle_sga_rows.restype = None
+        lib.oracle_sga_rows.argtypes = [i64, i32, p, p, i64, p, p, i64, p, p, p, p, i64,
+                                        i32, i32, i32, f64, p, p]
+        lib.oracle_attention_rows.restype = None
+        lib.oracle_attention_rows.argtypes = [i64, i32, i64, p, p, p, p, i64, f64, p, p]
+        lib.oracle_num_threads.restype = i32
+        lib.oracle_num_threads.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+@dataclass
+class Plan:
+    """The kept key/value set S of one layer (same for every batch element and head)."""
+    T: int
+    L: int
+    kept: np.ndarray        # uint8 [T]
+    kv_index: np.ndarray    # int32 [|S|], ascending token indices
+    frame_off: np.ndarray   # int32 [N+1]
+
+    @property
+    def S(self) -> int:
+        return int(self.kv_index.shape[0])
+
+    @property
+    def dropped(self) -> int:
+        return self.T - self.S
+
+
+def plan(N: int, grid_h: int, grid_w: int, n_special: int, s_h: int, s_w: int,
+         phase_shift: bool, ref_frame_dense: bool) -> Plan:
+    L = n_special + grid_h * grid_w
+    T = N * L
+    kept = np.zeros(T, dtype=np.uint8)
+    kv = np.zeros(T, dtype=np.int32)
+    off = np.zeros(N + 1, dtype=np.int32)
+    n = _load().oracle_plan(N, grid_h, grid_w, n_special, s_h, s_w, int(phase_shift),
+                            int(ref_frame_dense), _ptr(kept), _ptr(kv), _ptr(off))
+    if n < 0:
+        raise ValueError("oracle_plan: bad argument")
+    return Plan(T=T, L=L, kept=kept, kv_index=kv[:n].copy(), frame_off=off)
+
+
+def _f32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def dropped_sums(p: Plan, K: np.ndarray, V: np.ndarray):
+    """fp64 sums of K and V over the dropped set of one (batch, head); returns (k_sum, v_sum, c)."""
+    K, V = _f32(K), _f32(V)
+    d = K.shape[1]
+    ks = np.zeros(d, dtype=np.float64)
+    vs = np.zeros(d, dtype=np.float64)
+    c = _load().oracle_dropped_sums(p.T, d, _ptr(p.kept), _ptr(K), _ptr(V), _ptr(ks), _ptr(vs))
+    return ks, vs, int(c)
+
+
+def sga_rows(p: Plan, Qrows, K, V, rows, *, diag=True, mean=True, mean_mode=0,
+             scale=0.125, sums=None):
+    """SGA outputs (fp64) of the query rows ``rows`` of one (batch, head).
+
+    ``Qrows`` holds those rows' query vectors; ``K`` and ``V`` hold all T rows of the head.
+    Returns (out [n, d], lse [n]).
+    """
+    Qrows, K, V = _f32(Qrows), _f32(K), _f32(V)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n, d = Qrows.shape
+    if sums is None:
+        sums = dropped_sums(p, K, V)
+    ks, vs, c = sums
+    ks = np.ascontiguousarray(ks, dtype=np.float64)
+    vs = np.ascontiguousarray(vs, dtype=np.float64)
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    kv = np.ascontiguousarray(p.kv_index, dtype=np.int32)
+    _load().oracle_sga_rows(p.T, d, _ptr(p.kept), _ptr(kv), p.S, _ptr(ks), _ptr(vs), c,
+                            _ptr(Qrows), _ptr(K), _ptr(V), _ptr(rows), n,
+                            int(diag), int(mean), int(mean_mode), float(scale),
+                            _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def attention_rows(Qrows, K, V, rows, *, frame_len=0, scale=0.125):
+    """Dense (frame_len == 0) or frame-local attention outputs (fp64) of the rows ``rows``."""
+    Qrows, K, V = _f32(Qrows), _f32(K), _f32(V)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n, d = Qrows.shape
+    T = K.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    _load().oracle_attention_rows(T, d, int(frame_len), _ptr(Qrows), _ptr(K), _ptr(V),
+                                  _ptr(rows), n, float(scale), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def sga_full(p: Plan, Q, K, V, **kw):
+    """SGA over every row of one (batch, head): Q, K, V are [T, d]."""
+    rows = np.arange(p.T, dtype=np.int64)
+    return sga_rows(p, Q, K, V, rows, **kw)

@@ -1,0 +1,281 @@
+/*
+ * sga_oracle.c -- slow, plain, fp64 CPU oracle for Subsampling Global Attention (SGA).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes or calls
+ * this file; only the test-suite, the smoke check and the benchmark's CPU-baseline leg
+ * load it (through ctypes).  It shares no code, header, table or constant with the CUDA
+ * path.  It is written for a reader to check against the pages by eye: no blocking, no
+ * fusion, no reordering beyond what the method's definition states.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [AVGGT]   "AVGGT: Rethinking Global Attention for Accelerating VGGT" (CVPR 2026 notes),
+ *             Key design 1 (Global-to-Frame), Key design 2 (SGA, with the standard attention
+ *             equation), Key design 3 (diagonal retention + mean fill, shared softmax).
+ *   [AVGGT-de] the German technical summary of the same paper, section 2.B.
+ *   [Regime]  "RegimeVGGT: Layer-Wise Spatially Preserving Redundancy Removal for Visual
+ *             Geometry Grounded Transformer" (NeurIPS 2026 notes), "Core mechanism"
+ *             (L = T + 5 tokens per frame), Key design 2 (size-aware attention
+ *             softmax(QK^T/sqrt(d) + log g^T) V), Key design 3 (phase-shifted grid,
+ *             frame-0 anchor, camera/register tokens at full density).
+ *
+ * Readings taken where the pages are silent (each is a parameter or a documented rule):
+ *   R1  the n_special camera/register tokens occupy the first slots p = 0..n_special-1 of a
+ *       frame; patches follow in row-major order, p = n_special + r*grid_w + c.
+ *   R2  "first token of each s_h x s_w window": windows tile the grid from (0,0); a partial
+ *       edge window keeps its top-left token.  Equivalently r % s_h == 0 && c % s_w == 0.
+ *   R3  phase shift for a (s_h, s_w) grid: row offset (f div s_w) mod s_h, column offset
+ *       f mod s_w (the RegimeVGGT formula with tile t, generalised per axis); a kept patch
+ *       satisfies r == phi_r (mod s_h) and c == phi_c (mod s_w).  f is the global frame index.
+ *   R4  the diagonal term exists only for a query whose own token was dropped (a kept
+ *       query already sees itself through S; the three components are disjoint).
+ *   R5  mean term, leave-one-out (default): for a dropped query i the mean runs over
+ *       D \ {i} with count c-1; for a kept query over D with count c.  mean_mode = 1 selects
+ *       the plain global mean over D with count c for every query.
+ *   R6  the size-aware bias is + ln(count) added after the 1/sqrt(d) scaling; no mean term
+ *       when its count is 0.
+ *   R7  the mean is per (batch, head) over every dropped token of every frame.
+ *
+ * Parity pins (in tests/): closed-form kept counts; the page's sigma map and phase formula;
+ * sigma = 1 equals textbook attention and torch SDPA in fp64; the frame variant equals
+ * per-frame attention; with all dropped keys/values equal the SGA output equals dense
+ * attention exactly; Q = 0 gives the mean of all values; an explicit per-query brute force
+ * agrees.  The semantic readings R1, R3 (non-square), R4 and R5 themselves cannot be
+ * pinned by the pages: parity unpinned for those choices beyond the invariants above.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------------------------------
+ * Plan: the kept key/value set S.  [AVGGT] Key design 2; [Regime] Key design 3.
+ * Direct double loop over frames f and in-frame slots p.  Writes
+ *   kept[t]      1 if token t = f*L + p is a key/value of S, else 0   (T entries)
+ *   kv_index[s]  the tokens of S in ascending order                    (capacity T)
+ *   frame_off[f] index into kv_index of frame f's first kept token     (N+1 entries)
+ * Returns |S|, or -1 on a bad argument.
+ * ------------------------------------------------------------------------------------ */
+int64_t oracle_plan(int N, int grid_h, int grid_w, int n_special, int s_h, int s_w,
+                    int phase_shift, int ref_frame_dense,
+                    uint8_t* kept, int32_t* kv_index, int32_t* frame_off)
+{
+    if (N <= 0 || grid_h <= 0 || grid_w <= 0 || n_special < 0 || s_h <= 0 || s_w <= 0)
+        return -1;
+    const int64_t L = (int64_t)n_special + (int64_t)grid_h * grid_w;
+    int64_t n_kept = 0;
+    for (int f = 0; f < N; ++f) {
+        frame_off[f] = (int32_t)n_kept;
+        int phi_r = 0, phi_c = 0;
+        if (phase_shift) {
+            phi_r = (f / s_w) % s_h;
+            phi_c = f % s_w;
+        }
+        for (int64_t p = 0; p < L; ++p) {
+            const int64_t t = (int64_t)f * L + p;
+            int keep = 0;
+            if (f == 0 && ref_frame_dense) {
+                keep = 1;                       /* reference frame uncompressed */
+            } else if (p < n_special) {
+                keep = 1;                       /* camera / register tokens at full density */
+            } else {
+                const int64_t r = (p - n_special) / grid_w;
+                const int64_t c = (p - n_special) % grid_w;
+                if (r % s_h == phi_r && c % s_w == phi_c)
+                    keep = 1;                   /* first token of its (shifted) window */
+            }
+            kept[t] = (uint8_t)keep;
+            if (keep)
+                kv_index[n_kept++] = (int32_t)t;
+        }
+    }
+    frame_off[N] = (int32_t)n_kept;
+    return n_kept;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Sums of K and V over the dropped set D (one batch element, one head).
+ * [AVGGT] Key design 3: one mean key/value stands in for every dropped patch.
+ * K, V: [T, d] row-major.  k_sum, v_sum: [d].  Returns the count c = |D|.
+ * ------------------------------------------------------------------------------------ */
+int64_t oracle_dropped_sums(int64_t T, int d, const uint8_t* kept,
+                            const float* K, const float* V, double* k_sum, double* v_sum)
+{
+    int64_t c = 0;
+    for (int j = 0; j < d; ++j) { k_sum[j] = 0.0; v_sum[j] = 0.0; }
+    for (int64_t t = 0; t < T; ++t) {
+        if (kept[t]) continue;
+        ++c;
+        for (int j = 0; j < d; ++j) {
+            k_sum[j] += (double)K[t * d + j];
+            v_sum[j] += (double)V[t * d + j];
+        }
+    }
+    return c;
+}
+
+static double dot_fd(const float* a, const float* b, int d)
+{
+    double s = 0.0;
+    for (int j = 0; j < d; ++j) s += (double)a[j] * (double)b[j];
+    return s;
+}
+
+static double dot_fdd(const float* a, const double* b, int d)
+{
+    double s = 0.0;
+    for (int j = 0; j < d; ++j) s += (double)a[j] * b[j];
+    return s;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * SGA output for selected query rows of one (batch, head).
+ * [AVGGT] Key design 2 (attention over S, all queries kept) and Key design 3 (three
+ * disjoint components -- S, the diagonal self term, the mean of the dropped set -- under
+ * one softmax); [Regime] Key design 2 (the + log(group size) logit bias on a key that
+ * stands for several tokens).
+ *
+ *   Qrows [n_rows, d]  the query vectors of the selected rows
+ *   rows  [n_rows]     their token indices in [0, T)
+ *   K, V  [T, d]       all keys and values of this head (dropped rows are needed for the
+ *                      diagonal term and the leave-one-out mean)
+ *   kv_index [S]       the kept set from oracle_plan; kept[T] its indicator
+ *   k_sum, v_sum [d], c  from oracle_dropped_sums
+ *   diag, mean         switch the two extra components on (1) or off (0)
+ *   mean_mode          0 = leave-one-out (reading R5), 1 = global mean over D
+ *   out [n_rows, d], lse [n_rows] (nullable)
+ * The logits of one row are collected into a buffer, the maximum is subtracted, and the
+ * weights are normalised by their sum: a textbook softmax, in fp64.
+ * ------------------------------------------------------------------------------------ */
+void oracle_sga_rows(int64_t T, int d, const uint8_t* kept, const int32_t* kv_index, int64_t S,
+                     const double* k_sum, const double* v_sum, int64_t c,
+                     const float* Qrows, const float* K, const float* V,
+                     const int64_t* rows, int64_t n_rows,
+                     int diag, int mean, int mean_mode, double scale,
+                     double* out, double* lse)
+{
+    #pragma omp parallel
+    {
+        double* logit = (double*)malloc(sizeof(double) * (size_t)(S + 2));
+        double* kbar = (double*)malloc(sizeof(double) * (size_t)d);
+        double* vbar = (double*)malloc(sizeof(double) * (size_t)d);
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t n = 0; n < n_rows; ++n) {
+            const int64_t i = rows[n];
+            const float* q = Qrows + n * d;
+            double* o = out + n * d;
+
+            /* component (i): every kept key */
+            for (int64_t s = 0; s < S; ++s)
+                logit[s] = scale * dot_fd(q, K + (int64_t)kv_index[s] * d, d);
+
+            /* component (ii): the query's own key, when the query's token was dropped */
+            const int has_diag = diag && !kept[i];
+            if (has_diag)
+                logit[S] = scale * dot_fd(q, K + i * d, d);
+
+            /* component (iii): one mean key/value over the dropped set, logit + ln(count) */
+            int64_t ci = c;
+            if (mean_mode == 0 && !kept[i]) ci = c - 1;           /* leave i out */
+            const int has_mean = mean && ci > 0;
+            if (has_mean) {
+                for (int j = 0; j < d; ++j) {
+                    double ks = k_sum[j], vs = v_sum[j];
+                    if (mean_mode == 0 && !kept[i]) {
+                        ks -= (double)K[i * d + j];
+                        vs -= (double)V[i * d + j];
+                    }
+                    kbar[j] = ks / (double)ci;
+                    vbar[j] = vs / (double)ci;
+                }
+                logit[S + 1] = scale * dot_fdd(q, kbar, d) + log((double)ci);
+            }
+
+            /* one shared softmax over the three components */
+            double m = -INFINITY;
+            for (int64_t s = 0; s < S; ++s) if (logit[s] > m) m = logit[s];
+            if (has_diag && logit[S] > m) m = logit[S];
+            if (has_mean && logit[S + 1] > m) m = logit[S + 1];
+
+            double l = 0.0;
+            for (int j = 0; j < d; ++j) o[j] = 0.0;
+            for (int64_t s = 0; s < S; ++s) {
+                const double w = exp(logit[s] - m);
+                const float* v = V + (int64_t)kv_index[s] * d;
+                l += w;
+                for (int j = 0; j < d; ++j) o[j] += w * (double)v[j];
+            }
+            if (has_diag) {
+                const double w = exp(logit[S] - m);
+                l += w;
+                for (int j = 0; j < d; ++j) o[j] += w * (double)V[i * d + j];
+            }
+            if (has_mean) {
+                const double w = exp(logit[S + 1] - m);
+                l += w;
+                for (int j = 0; j < d; ++j) o[j] += w * vbar[j];
+            }
+            for (int j = 0; j < d; ++j) o[j] /= l;
+            if (lse) lse[n] = m + log(l);
+        }
+        free(logit); free(kbar); free(vbar);
+    }
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Textbook attention softmax(q K^T * scale) V for selected rows over the key range
+ * [key_lo(i), key_hi(i)).  [AVGGT] Key design 2, the standard attention equation.
+ *   frame_len == 0: dense global attention, keys [0, T)
+ *   frame_len  > 0: frame-local attention ([AVGGT] Key design 1, Global-to-Frame):
+ *                   keys of the query's own frame, [f*frame_len, (f+1)*frame_len)
+ * ------------------------------------------------------------------------------------ */
+void oracle_attention_rows(int64_t T, int d, int64_t frame_len,
+                           const float* Qrows, const float* K, const float* V,
+                           const int64_t* rows, int64_t n_rows, double scale,
+                           double* out, double* lse)
+{
+    #pragma omp parallel
+    {
+        const int64_t cap = frame_len > 0 ? frame_len : T;
+        double* logit = (double*)malloc(sizeof(double) * (size_t)cap);
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t n = 0; n < n_rows; ++n) {
+            const int64_t i = rows[n];
+            const float* q = Qrows + n * d;
+            double* o = out + n * d;
+            int64_t lo = 0, hi = T;
+            if (frame_len > 0) {
+                lo = (i / frame_len) * frame_len;
+                hi = lo + frame_len;
+            }
+            double m = -INFINITY;
+            for (int64_t t = lo; t < hi; ++t) {
+                logit[t - lo] = scale * dot_fd(q, K + t * d, d);
+                if (logit[t - lo] > m) m = logit[t - lo];
+            }
+            double l = 0.0;
+            for (int j = 0; j < d; ++j) o[j] = 0.0;
+            for (int64_t t = lo; t < hi; ++t) {
+                const double w = exp(logit[t - lo] - m);
+                l += w;
+                for (int j = 0; j < d; ++j) o[j] += w * (double)V[t * d + j];
+            }
+            for (int j = 0; j < d; ++j) o[j] /= l;
+            if (lse) lse[n] = m + log(l);
+        }
+        free(logit);
+    }
+}
+
+/* Threads the OpenMP runtime will use (reported beside CPU timings). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

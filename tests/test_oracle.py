@@ -1,0 +1,318 @@
+"""Pins for the fp64 CPU oracle: each test checks the oracle against something other than
+itself -- the pages' printed rules (golden fixtures), closed forms, textbook/library attention,
+exact identities and a brute-force re-derivation on tiny inputs.  CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from subsampled_global_attention_sga_b300.inputs import correlated_qkv
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+SCALE = 0.125  # 1/sqrt(64)
+
+
+def _rows(path):
+    out = []
+    for line in open(os.path.join(GOLDEN, path)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            out.append([int(x) for x in line.split()])
+    return out
+
+
+def _sdpa(q, k, v, scale=SCALE):
+    q = torch.as_tensor(q, dtype=torch.float64)[None, None]
+    k = torch.as_tensor(k, dtype=torch.float64)[None, None]
+    v = torch.as_tensor(v, dtype=torch.float64)[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale)[0, 0].numpy()
+
+
+def _textbook(q, k, v, scale=SCALE):
+    s = (q.astype(np.float64) @ k.astype(np.float64).T) * scale
+    s -= s.max(axis=1, keepdims=True)
+    w = np.exp(s)
+    w /= w.sum(axis=1, keepdims=True)
+    return w @ v.astype(np.float64)
+
+
+def _qkv(N, L, H=1, seed=0, q_scale=1.0):
+    q, k, v = correlated_qkv(1, H, N, L, 64, seed=seed, dtype=torch.float32, q_scale=q_scale)
+    return q[0].numpy(), k[0].numpy(), v[0].numpy()
+
+
+# ------------------------------------------------------------------------------ plan pins
+def test_plan_counts_closed_form_golden():
+    for N, gh, gw, nsp, sh, sw, ph, rd, T, S, c in _rows("plan_counts.txt"):
+        p = oracle.plan(N, gh, gw, nsp, sh, sw, bool(ph), bool(rd))
+        assert (p.T, p.S, p.dropped) == (T, S, c)
+
+
+@pytest.mark.parametrize("gh,gw", [(8, 8), (7, 5), (37, 28), (1, 1), (2, 9)])
+@pytest.mark.parametrize("sigma", [1, 2, 4, 6, 9])
+@pytest.mark.parametrize("phase", [False, True])
+@pytest.mark.parametrize("ref", [False, True])
+def test_plan_per_frame_counts(gh, gw, sigma, phase, ref):
+    smap = {s: (a, b) for s, a, b in _rows("sigma_map.txt")}
+    sh, sw = smap[sigma]
+    N, nsp = 11, 5
+    p = oracle.plan(N, gh, gw, nsp, sh, sw, phase, ref)
+    L = nsp + gh * gw
+    for f in range(N):
+        got = p.frame_off[f + 1] - p.frame_off[f]
+        if f == 0 and ref:
+            want = L
+        else:
+            pr, pc = ((f // sw) % sh, f % sw) if phase else (0, 0)
+            want = nsp + math.ceil(max(0, gh - pr) / sh) * math.ceil(max(0, gw - pc) / sw)
+        assert got == want, (f, got, want)
+    assert np.all(np.diff(p.kv_index) > 0)
+    assert p.kept.sum() == p.S
+    assert np.array_equal(np.nonzero(p.kept)[0], p.kv_index)
+
+
+def test_sigma_map_golden_windows():
+    # the first patch of every s_h x s_w window is kept and nothing else (fixed grid)
+    for sigma, sh, sw in _rows("sigma_map.txt"):
+        assert sh * sw == sigma
+        gh, gw, nsp = 7, 8, 5
+        p = oracle.plan(2, gh, gw, nsp, sh, sw, False, True)
+        L = nsp + gh * gw
+        frame1 = p.kept[L:2 * L]
+        assert frame1[:nsp].all()
+        kept_rc = {divmod(int(x) - nsp, gw) for x in np.nonzero(frame1[nsp:])[0] + nsp}
+        windows = {(wr * sh, wc * sw) for wr in range(math.ceil(gh / sh)) for wc in range(math.ceil(gw / sw))}
+        assert kept_rc == windows
+        assert p.kept[:L].all()  # frame 0 dense
+
+
+def test_phase_offsets_golden():
+    for t, f, ro, co in _rows("phase_offsets.txt"):
+        gh = gw = 6
+        nsp = 5
+        N = f + 1
+        p = oracle.plan(N, gh, gw, nsp, t, t, True, False)
+        L = nsp + gh * gw
+        fr = p.kept[f * L:(f + 1) * L]
+        kept_rc = sorted(divmod(int(x), gw) for x in np.nonzero(fr[nsp:])[0])
+        assert kept_rc[0] == (ro, co)  # the first kept patch sits at the frame's offset
+        assert all(r % t == ro and c % t == co for r, c in kept_rc)
+
+
+@pytest.mark.parametrize("sh,sw", [(1, 2), (2, 2), (2, 3), (3, 3)])
+def test_phase_coverage(sh, sw):
+    # with the phase shift, any sigma consecutive frames together cover every grid position once
+    gh, gw, nsp = 9, 10, 5
+    sigma = sh * sw
+    N = 2 * sigma + 3
+    p = oracle.plan(N, gh, gw, nsp, sh, sw, True, False)
+    L = nsp + gh * gw
+    for f0 in range(N - sigma + 1):
+        cover = np.zeros(gh * gw, dtype=int)
+        for f in range(f0, f0 + sigma):
+            cover += p.kept[f * L + nsp:(f + 1) * L]
+        assert np.all(cover == 1), f0
+
+
+def test_sigma1_keeps_everything():
+    p = oracle.plan(3, 5, 4, 5, 1, 1, True, False)
+    assert p.S == p.T and p.dropped == 0
+
+
+# ------------------------------------------------------------------------------ attention pins
+def test_dense_equals_textbook_and_sdpa():
+    q, k, v = _qkv(4, 69)
+    rows = np.arange(q.shape[1])
+    out, lse = oracle.attention_rows(q[0], k[0], v[0], rows)
+    np.testing.assert_allclose(out, _sdpa(q[0], k[0], v[0]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out, _textbook(q[0], k[0], v[0]), rtol=0, atol=1e-12)
+    s = (q[0].astype(np.float64) @ k[0].astype(np.float64).T) * SCALE
+    m = s.max(axis=1)
+    np.testing.assert_allclose(lse, m + np.log(np.exp(s - m[:, None]).sum(axis=1)), atol=1e-12)
+
+
+def test_frame_equals_per_frame_sdpa():
+    N, L = 5, 23
+    q, k, v = _qkv(N, L)
+    out, _ = oracle.attention_rows(q[0], k[0], v[0], np.arange(N * L), frame_len=L)
+    for f in range(N):
+        sl = slice(f * L, (f + 1) * L)
+        np.testing.assert_allclose(out[sl], _sdpa(q[0][sl], k[0][sl], v[0][sl]), atol=1e-12)
+
+
+def test_sigma1_sga_equals_dense():
+    N, gh, gw, nsp = 4, 8, 8, 5
+    p = oracle.plan(N, gh, gw, nsp, 1, 1, False, True)
+    q, k, v = _qkv(N, p.L, H=2)
+    for h in range(2):
+        out, lse = oracle.sga_full(p, q[h], k[h], v[h])
+        np.testing.assert_allclose(out, _sdpa(q[h], k[h], v[h]), atol=1e-12)
+
+
+def _equal_dropped(p, k, v, rng):
+    k = k.copy()
+    v = v.copy()
+    kb = rng.standard_normal(64).astype(np.float32)
+    vb = rng.standard_normal(64).astype(np.float32)
+    d = p.kept == 0
+    k[d] = kb
+    v[d] = vb
+    return k, v
+
+
+@pytest.mark.parametrize("sh,sw,phase,ref", [(2, 2, False, True), (2, 3, True, True),
+                                             (3, 3, True, False), (1, 2, False, False)])
+def test_identity_equal_dropped_rows_equals_dense(sh, sw, phase, ref):
+    # every dropped key/value equal: the diagonal plus the log(count)-biased mean reproduce the
+    # dropped keys exactly, so SGA equals dense attention for kept and dropped queries alike
+    N, gh, gw, nsp = 4, 8, 7, 5
+    p = oracle.plan(N, gh, gw, nsp, sh, sw, phase, ref)
+    q, k, v = _qkv(N, p.L, seed=3)
+    rng = np.random.default_rng(7)
+    k2, v2 = _equal_dropped(p, k[0], v[0], rng)
+    out, _ = oracle.sga_full(p, q[0], k2, v2)
+    np.testing.assert_allclose(out, _sdpa(q[0], k2, v2), atol=1e-12)
+
+
+def test_identity_is_sensitive_to_each_term():
+    # planted mistakes (each switches off or alters one part of the oracle): the identity must fail
+    N, gh, gw, nsp = 4, 8, 8, 5
+    p = oracle.plan(N, gh, gw, nsp, 2, 2, False, True)
+    q, k, v = _qkv(N, p.L, seed=5)
+    k2, v2 = _equal_dropped(p, k[0], v[0], np.random.default_rng(1))
+    ref = _sdpa(q[0], k2, v2)
+    drop = p.kept == 0
+    for kw in (dict(diag=False), dict(mean=False), dict(mean_mode=1)):
+        out, _ = oracle.sga_full(p, q[0], k2, v2, **kw)
+        assert np.abs(out[drop] - ref[drop]).max() > 1e-4, kw
+    # a wrong bias (log2 instead of ln, or no bias) is caught as well: emulate it by feeding
+    # sums scaled so that the mean key is unchanged but the count differs
+    ks, vs, c = oracle.dropped_sums(p, k2, v2)
+    out, _ = oracle.sga_full(p, q[0], k2, v2, sums=(ks * 2, vs * 2, c))
+    assert np.abs(out - ref).max() > 1e-4
+
+
+def test_zero_query_gives_mean_of_all_values():
+    N, gh, gw, nsp = 4, 8, 8, 5
+    for (sh, sw, ph) in [(2, 2, False), (3, 3, True), (1, 1, False)]:
+        p = oracle.plan(N, gh, gw, nsp, sh, sw, ph, True)
+        _, k, v = _qkv(N, p.L, seed=11)
+        q0 = np.zeros((p.T, 64), np.float32)
+        out, lse = oracle.sga_full(p, q0, k[0], v[0])
+        want = v[0].astype(np.float64).mean(axis=0)
+        np.testing.assert_allclose(out, np.broadcast_to(want, out.shape), atol=1e-12)
+        np.testing.assert_allclose(lse, np.log(p.T), atol=1e-12)
+        outd, _ = oracle.attention_rows(q0, k[0], v[0], np.arange(p.T))
+        np.testing.assert_allclose(outd, np.broadcast_to(want, out.shape), atol=1e-12)
+
+
+# ------------------------------------------------------------------------------ brute force
+def _bf_kept(N, gh, gw, nsp, sh, sw, phase, ref):
+    """Kept tokens by enumerating windows (a formulation independent of the oracle's)."""
+    L = nsp + gh * gw
+    kept = set()
+    for f in range(N):
+        if f == 0 and ref:
+            kept.update(range(0, L))
+            continue
+        kept.update(f * L + p for p in range(nsp))
+        r0, c0 = ((f // sw) % sh, f % sw) if phase else (0, 0)
+        for wr in range(r0, gh, sh):
+            for wc in range(c0, gw, sw):
+                kept.add(f * L + nsp + wr * gw + wc)  # top-left token of the window
+    return kept
+
+
+def _bf_row(i, q, k, v, kept, T, diag, mean, mean_mode, scale=SCALE):
+    entries = []  # (token ids it stands for, key, value, bias)
+    for t in sorted(kept):
+        entries.append(([t], k[t].astype(np.float64), v[t].astype(np.float64), 0.0))
+    dropped = [t for t in range(T) if t not in kept]
+    if diag and i not in kept:
+        entries.append(([i], k[i].astype(np.float64), v[i].astype(np.float64), 0.0))
+    if mean:
+        src = [t for t in dropped if (t != i or mean_mode == 1)]
+        if src:
+            kb = np.mean([k[t].astype(np.float64) for t in src], axis=0)
+            vb = np.mean([v[t].astype(np.float64) for t in src], axis=0)
+            entries.append((src, kb, vb, math.log(len(src))))
+    logits = [scale * float(np.dot(q.astype(np.float64), e[1])) + e[3] for e in entries]
+    m = max(logits)
+    ws = [math.exp(x - m) for x in logits]
+    z = math.fsum(ws)
+    o = sum(w * e[2] for w, e in zip(ws, entries)) / z
+    srcs = [t for e in entries for t in e[0]]
+    return o, m + math.log(z), [w / z for w in ws], srcs
+
+
+CASES = [
+    # N, gh, gw, nsp, sh, sw, phase, ref, diag, mean, mode
+    (4, 8, 8, 5, 2, 2, False, True, True, True, 0),
+    (4, 8, 8, 5, 2, 2, True, True, True, True, 0),
+    (3, 7, 5, 5, 2, 3, True, False, True, True, 0),
+    (3, 6, 6, 5, 3, 3, False, True, True, False, 0),
+    (3, 6, 6, 5, 3, 3, False, True, False, True, 0),
+    (3, 6, 6, 5, 3, 3, True, True, True, True, 1),
+    (2, 4, 5, 0, 1, 2, False, False, True, True, 0),
+    (2, 3, 3, 2, 3, 3, False, False, True, True, 0),  # one kept patch per frame
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_bruteforce_agrees(case):
+    N, gh, gw, nsp, sh, sw, ph, ref, diag, mean, mode = case
+    p = oracle.plan(N, gh, gw, nsp, sh, sw, ph, ref)
+    kept = _bf_kept(N, gh, gw, nsp, sh, sw, ph, ref)
+    assert kept == set(p.kv_index.tolist())
+    q, k, v = _qkv(N, p.L, seed=2, q_scale=3.0)
+    rows = np.arange(p.T)
+    out, lse = oracle.sga_rows(p, q[0], k[0], v[0], rows, diag=diag, mean=mean, mean_mode=mode)
+    for i in rows:
+        o, l, w, srcs = _bf_row(int(i), q[0][i], k[0], v[0], kept, p.T, diag, mean, mode)
+        np.testing.assert_allclose(out[i], o, atol=1e-12)
+        assert abs(lse[i] - l) < 1e-12
+        assert abs(math.fsum(w) - 1.0) < 1e-12
+        if diag and mean and mode == 0:
+            # the three components partition the keys: S, {i} if dropped, D \ {i}
+            assert sorted(srcs) == list(range(p.T))
+
+
+def test_mean_count_zero_drops_the_term():
+    # one dropped token only: for that query c_i = 0 (no mean term), the others see count 1
+    N, gh, gw, nsp = 2, 1, 2, 0
+    p = oracle.plan(N, gh, gw, nsp, 1, 2, False, True)
+    assert p.dropped == 1
+    q, k, v = _qkv(N, p.L, seed=9)
+    out, _ = oracle.sga_full(p, q[0], k[0], v[0])
+    np.testing.assert_allclose(out, _sdpa(q[0], k[0], v[0]), atol=1e-12)
+
+
+def test_appended_column_identity():
+    # RegimeVGGT's size-aware bias absorbed into an extra column: [q, 1] . [k, sqrt(d) ln g]
+    # scaled by 1/sqrt(d) equals q.k/sqrt(d) + ln g.  Rebuild each row's SGA softmax that way
+    # and run it through torch SDPA (d + 1 = 65 columns, scale kept at 1/sqrt(64)).
+    N, gh, gw, nsp = 4, 8, 8, 5
+    p = oracle.plan(N, gh, gw, nsp, 2, 2, True, True)
+    q, k, v = _qkv(N, p.L, seed=4)
+    out, _ = oracle.sga_full(p, q[0], k[0], v[0])
+    ks, vs, c = oracle.dropped_sums(p, k[0], v[0])
+    for i in [0, 7, 80, 100, 200, p.T - 1]:
+        keys = [np.append(k[0][t].astype(np.float64), 0.0) for t in p.kv_index]
+        vals = [v[0][t].astype(np.float64) for t in p.kv_index]
+        if not p.kept[i]:
+            keys.append(np.append(k[0][i].astype(np.float64), 0.0))
+            vals.append(v[0][i].astype(np.float64))
+            ci = c - 1
+            kb = (ks - k[0][i]) / ci
+            vb = (vs - v[0][i]) / ci
+        else:
+            ci = c
+            kb, vb = ks / ci, vs / ci
+        keys.append(np.append(kb, math.sqrt(64) * math.log(ci)))
+        vals.append(vb)
+        qq = np.append(q[0][i].astype(np.float64), 1.0)[None]
+        got = _sdpa(qq, np.array(keys), np.array(vals), scale=SCALE)[0]
+        np.testing.assert_allclose(out[i], got, atol=1e-12)
