@@ -1,0 +1,163 @@
+/*
+ * sga.h -- C ABI of libsga: Subsampling Global Attention (SGA) for one global cross-frame
+ * attention layer of a VGGT-style multi-view transformer, on one B300 GPU (sm_103a).
+ *
+ * The method (sources are web pages, cited by title and section):
+ *   "AVGGT: Rethinking Global Attention for Accelerating VGGT" (CVPR 2026 notes)
+ *     Key design 1  Global-to-Frame: a global layer may run as attention within each frame.
+ *     Key design 2  SGA: every query is kept; keys/values are cut to a grid subset S -- the
+ *                   first patch token of each s_h x s_w window (sigma = s_h*s_w; 2->(1,2),
+ *                   4->(2,2), 6->(2,3), 9->(3,3)); special tokens and, for VGGT, frame 0
+ *                   stay uncompressed.  Standard attention softmax(QK^T/sqrt(d))V over S.
+ *     Key design 3  two more components disjoint from S under the same softmax: each token's
+ *                   own key (diagonal) and one mean key/value for all dropped patches.
+ *   "RegimeVGGT: Layer-Wise Spatially Preserving Redundancy Removal for Visual Geometry
+ *    Grounded Transformer" (NeurIPS 2026 notes)
+ *     Core mechanism  L = T + 5 tokens per frame (patches + 5 camera/register tokens).
+ *     Key design 2    size-aware attention softmax(QK^T/sqrt(d) + log g^T)V: a key that
+ *                     stands for g tokens gets the logit bias ln g (here: the mean key,
+ *                     g = number of dropped tokens it averages).
+ *     Key design 3    per-frame phase shift of the grid (row (f div t) mod t, column
+ *                     f mod t); frame 0 and camera/register tokens at full density.
+ *
+ * Readings where the pages are silent (identical in the library and its test oracle):
+ *   special tokens are the first n_special slots of each frame, patches follow row-major;
+ *   partial edge windows keep their top-left token; for a (s_h, s_w) grid the phase is
+ *   row (f div s_w) mod s_h, column f mod s_w; the diagonal term exists only for a dropped
+ *   query; the mean is leave-one-out for a dropped query (mean over D \ {i}, count c-1)
+ *   unless SGA_MEAN_GLOBAL is chosen; the bias is + ln(count) after the 1/sqrt(d) scaling;
+ *   the mean runs over every dropped token of all frames of one (batch, head).
+ *
+ * Tensors.  Q, K, V, O are contiguous [B, H, T, 64] with T = N*L tokens (token t = f*L + p),
+ * in the dtype of the call (SGA_BF16: bfloat16; SGA_F32: float32).  All pointers are DEVICE
+ * pointers owned by the caller and must stay valid until the stream reaches the work; each
+ * must be 16-byte aligned.  Calls never allocate, never synchronise the host (except
+ * sga_device_status) and enqueue their kernels on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream) of the device that is current on the calling thread.
+ *
+ * Errors.  Every call validates its arguments first and returns a status; nothing aborts or
+ * traps.  Kernels that wait on hardware barriers give up after a bounded time, record
+ * SGA_ERR_TIMEOUT in a device status word and return; sga_device_status() reads it.
+ */
+#ifndef SGA_H_
+#define SGA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SGA_OK = 0,
+    SGA_ERR_INVALID_ARG = 1,    /* null pointer, non-positive size, inconsistent shape */
+    SGA_ERR_UNSUPPORTED = 2,    /* head_dim != 64, unknown dtype, kernel not built for it */
+    SGA_ERR_ALIGNMENT = 3,      /* a tensor pointer is not 16-byte aligned */
+    SGA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (launch, memcpy, ...) */
+    SGA_ERR_TIMEOUT = 5,        /* a kernel's bounded wait expired (reported by device status) */
+    SGA_ERR_PLAN_MISMATCH = 6   /* plan used with another device or a destroyed plan */
+} sga_status;
+
+typedef enum { SGA_BF16 = 0, SGA_F32 = 1 } sga_dtype;
+
+/* Mean-term reading (see above).  LOO keeps S, {i} and D\{i} disjoint for every query. */
+typedef enum { SGA_MEAN_LOO = 0, SGA_MEAN_GLOBAL = 1 } sga_mean_mode;
+
+/* Which attention kernel runs.  AUTO: tensor-core kernel (tcgen05/TMEM/TMA) for bf16,
+ * CUDA-core fp32 kernel for f32.  SIMT forces the CUDA-core kernel (any dtype). */
+typedef enum { SGA_KERNEL_AUTO = 0, SGA_KERNEL_TC = 1, SGA_KERNEL_SIMT = 2 } sga_kernel;
+
+/* Layer configuration.  L = n_special + grid_h*grid_w tokens per frame, T = N*L. */
+typedef struct {
+    int B, H;                /* batch elements, heads */
+    int N;                   /* frames */
+    int grid_h, grid_w;      /* patch grid of one frame */
+    int n_special;           /* camera/register tokens per frame (VGGT: 5) */
+    int head_dim;            /* must be 64 */
+    int s_h, s_w;            /* subsampling window, sigma = s_h*s_w; (1,1) keeps every key */
+    int phase_shift;         /* 1: per-frame phase-shifted grid */
+    int ref_frame_dense;     /* 1: frame 0 uncompressed (VGGT); 0: all frames alike (pi^3) */
+    int diag;                /* 1: diagonal self term for dropped queries */
+    int mean;                /* 1: log(count)-biased mean key/value of the dropped set */
+    int mean_mode;           /* sga_mean_mode */
+    int dtype;               /* sga_dtype of Q, K, V, O, K_S, V_S */
+    int kernel;              /* sga_kernel */
+} sga_config;
+
+typedef struct sga_plan_s* sga_plan_t;   /* opaque */
+
+/* Host-only plan builder: the same kept set S as sga_plan_create, computed on the host without
+ * touching any device.  kv_index (capacity T = N*L entries) receives the kept tokens in
+ * ascending order, frame_off (N+1 entries) each frame's first index into kv_index, slot
+ * (T entries, nullable) the position of each token in kv_index or -1 if dropped, *S_out |S|.
+ * Source: AVGGT Key design 2; RegimeVGGT Key design 3. */
+sga_status sga_plan_host(const sga_config* cfg, int32_t* kv_index, int32_t* frame_off,
+                         int32_t* slot, int64_t* S_out);
+
+/* Build the kept set S for `cfg` on the host (integer arithmetic, O(T)) and upload it to
+ * `device`: the token->slot map (int32 [T], -1 = dropped), the kept-token list (int32 [|S|],
+ * ascending) and per-frame offsets (int32 [N+1]).  The plan owns these device buffers and a
+ * small reduction scratch buffer; sga_plan_destroy frees them.  This is the only call that
+ * allocates (cudaMalloc) and it synchronises `device` once after the upload.
+ * Source: AVGGT Key design 2; RegimeVGGT Key design 3. */
+sga_status sga_plan_create(const sga_config* cfg, int device, sga_plan_t* out);
+
+/* T = N*L, S = |S| (kept keys), dropped = T - |S|.  Any output pointer may be NULL. */
+sga_status sga_plan_info(sga_plan_t plan, int64_t* T, int64_t* S, int64_t* dropped);
+
+/* Copy the plan's kept-token list (host int32 [|S|]) and frame offsets (host int32 [N+1]).
+ * Either pointer may be NULL.  Synchronous. */
+sga_status sga_plan_copy_indices(sga_plan_t plan, int32_t* kv_index, int32_t* frame_off);
+
+/* Free the plan's device buffers (synchronises the plan's device).  NULL is a no-op. */
+void sga_plan_destroy(sga_plan_t plan);
+
+/* Compaction (AVGGT Key design 2 "replace K, V by the subset S" and Key design 3 "one mean
+ * key/value for all dropped patches"): K_S, V_S [B, H, |S|, 64] receive exact copies of the
+ * kept rows of K, V [B, H, T, 64] in ascending token order; k_sum, v_sum (fp32 [B, H, 64])
+ * receive the sums of the dropped rows (a fixed-order, deterministic reduction).  The mean
+ * is formed from these sums by sga_forward.  Uses the plan's scratch buffer: two calls with
+ * the same plan must not run concurrently on different streams. */
+sga_status sga_compact(sga_plan_t plan, const void* K, const void* V, void* K_S, void* V_S,
+                       float* k_sum, float* v_sum, void* stream);
+
+/* SGA attention (AVGGT Key designs 2-3, RegimeVGGT Key design 2).  For every query row i of
+ * every (b, h):  O_i = softmax over { scale*q_i.k_j : j in S }
+ *                                 U { scale*q_i.k_i           if diag and i dropped }
+ *                                 U { scale*q_i.kbar_i + ln c_i  if mean and c_i > 0 }
+ * applied to the matching values, where kbar_i, vbar_i, c_i are the mean key/value and count
+ * of the dropped set (leave-one-out for a dropped i under SGA_MEAN_LOO), formed from k_sum,
+ * v_sum.  Q, K, V: [B, H, T, 64]; K_S, V_S, k_sum, v_sum from sga_compact with this plan.
+ * O: [B, H, T, 64] (RN-even from fp32).  lse: optional fp32 [B, H, T], natural-log
+ * log-sum-exp of each row's logits (NULL to skip).  scale: the logit scale (1/sqrt(64)). */
+sga_status sga_forward(sga_plan_t plan, const void* Q, const void* K, const void* V,
+                       const void* K_S, const void* V_S, const float* k_sum, const float* v_sum,
+                       void* O, float* lse, float scale, void* stream);
+
+/* Dense global attention, softmax(scale*QK^T)V over all T tokens of each (b, h)
+ * (AVGGT Key design 2, the standard attention equation; SGA with sigma = 1). */
+sga_status sga_dense_forward(int B, int H, int64_t T, int head_dim, int dtype, int kernel,
+                             const void* Q, const void* K, const void* V, void* O, float* lse,
+                             float scale, void* stream);
+
+/* Frame-local attention (AVGGT Key design 1, Global-to-Frame): each query attends to the L
+ * tokens of its own frame only; Q, K, V, O are [B, H, N*L, 64]. */
+sga_status sga_frame_forward(int B, int H, int N, int L, int head_dim, int dtype, int kernel,
+                             const void* Q, const void* K, const void* V, void* O, float* lse,
+                             float scale, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word of the current device
+ * (SGA_OK or SGA_ERR_TIMEOUT from a kernel's bounded wait).  Returns SGA_ERR_CUDA if the
+ * synchronisation itself failed. */
+sga_status sga_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* sga_status_string(sga_status s);
+
+/* Library build identification: compute capability targeted ("sm_103a") and version. */
+const char* sga_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SGA_H_ */

@@ -1,0 +1,81 @@
+"""ctypes binding of libsga.so (the C ABI declared in include/sga.h): symbol table only."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB
+
+SGA_OK = 0
+STATUS_NAMES = {
+    0: "SGA_OK", 1: "SGA_ERR_INVALID_ARG", 2: "SGA_ERR_UNSUPPORTED", 3: "SGA_ERR_ALIGNMENT",
+    4: "SGA_ERR_CUDA", 5: "SGA_ERR_TIMEOUT", 6: "SGA_ERR_PLAN_MISMATCH",
+}
+SGA_BF16, SGA_F32 = 0, 1
+SGA_MEAN_LOO, SGA_MEAN_GLOBAL = 0, 1
+SGA_KERNEL_AUTO, SGA_KERNEL_TC, SGA_KERNEL_SIMT = 0, 1, 2
+
+# every entry point include/sga.h declares (checked by the CPU test-suite)
+EXPORTS = (
+    "sga_plan_host", "sga_plan_create", "sga_plan_info", "sga_plan_copy_indices", "sga_plan_destroy",
+    "sga_compact", "sga_forward", "sga_dense_forward", "sga_frame_forward", "sga_device_status",
+    "sga_status_string", "sga_build_info",
+)
+
+
+class SgaConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "B", "H", "N", "grid_h", "grid_w", "n_special", "head_dim", "s_h", "s_w",
+        "phase_shift", "ref_frame_dense", "diag", "mean", "mean_mode", "dtype", "kernel")]
+
+
+class SgaError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call} failed: {STATUS_NAMES.get(status, status)} ({_describe(status)})")
+
+
+_lib = None
+
+
+def _describe(status: int) -> str:
+    try:
+        return lib().sga_status_string(status).decode()
+    except Exception:  # pragma: no cover - only while the library is unavailable
+        return "?"
+
+
+def lib():
+    """Load libsga.so (built in-tree by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"libsga.so is not built ({LIB}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        cfgp = ctypes.POINTER(SgaConfig)
+        sig = {
+            "sga_plan_host": (i32, [cfgp, vp, vp, vp, ctypes.POINTER(i64)]),
+            "sga_plan_create": (i32, [cfgp, i32, ctypes.POINTER(vp)]),
+            "sga_plan_info": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)]),
+            "sga_plan_copy_indices": (i32, [vp, vp, vp]),
+            "sga_plan_destroy": (None, [vp]),
+            "sga_compact": (i32, [vp, vp, vp, vp, vp, vp, vp, vp]),
+            "sga_forward": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, vp]),
+            "sga_dense_forward": (i32, [i32, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp]),
+            "sga_frame_forward": (i32, [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp]),
+            "sga_device_status": (i32, [vp]),
+            "sga_status_string": (ctypes.c_char_p, [i32]),
+            "sga_build_info": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def check(call: str, status: int) -> None:
+    if status != SGA_OK:
+        raise SgaError(call, status)

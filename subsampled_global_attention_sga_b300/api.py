@@ -1,0 +1,246 @@
+"""Python front end of libsga: argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module turns torch tensors
+into device pointers plus the current CUDA stream and raises on a non-OK status.  Output
+tensors that the caller does not pass are allocated here with torch (device memory is
+PyTorch's job); the C entry points themselves never allocate.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import SgaConfig, check, lib
+
+# sigma -> (s_h, s_w): "AVGGT: Rethinking Global Attention for Accelerating VGGT", Key design 2
+# (sigma = s_h * s_w; 2 -> (1,2), 4 -> (2,2), 6 -> (2,3), 9 -> (3,3)); sigma = 1 keeps every key.
+SIGMA_WINDOWS = {1: (1, 1), 2: (1, 2), 4: (2, 2), 6: (2, 3), 9: (3, 3)}
+
+_DTYPES = {"bf16": (_lib.SGA_BF16, torch.bfloat16), "f32": (_lib.SGA_F32, torch.float32)}
+_KERNELS = {"auto": _lib.SGA_KERNEL_AUTO, "tc": _lib.SGA_KERNEL_TC, "simt": _lib.SGA_KERNEL_SIMT}
+_MEAN_MODES = {"loo": _lib.SGA_MEAN_LOO, "global": _lib.SGA_MEAN_GLOBAL}
+
+
+def sigma_window(sigma: int):
+    """The (s_h, s_w) window of a subsampling factor sigma."""
+    if sigma not in SIGMA_WINDOWS:
+        raise ValueError(f"sigma must be one of {sorted(SIGMA_WINDOWS)}, got {sigma}")
+    return SIGMA_WINDOWS[sigma]
+
+
+@dataclass
+class SGAConfig:
+    """One SGA layer: B x H heads over N frames of n_special + grid_h*grid_w tokens, d = 64."""
+    B: int
+    H: int
+    N: int
+    grid_h: int = 37
+    grid_w: int = 37
+    n_special: int = 5
+    sigma: int = 4
+    window: tuple | None = None        # explicit (s_h, s_w); overrides sigma
+    phase_shift: bool = False
+    ref_frame_dense: bool = True
+    diag: bool = True
+    mean: bool = True
+    mean_mode: str = "loo"
+    dtype: str = "bf16"
+    kernel: str = "auto"
+    head_dim: int = 64
+
+    @property
+    def L(self) -> int:
+        return self.n_special + self.grid_h * self.grid_w
+
+    @property
+    def T(self) -> int:
+        return self.N * self.L
+
+    @property
+    def s_hw(self):
+        return tuple(self.window) if self.window is not None else sigma_window(self.sigma)
+
+    @property
+    def torch_dtype(self):
+        return _DTYPES[self.dtype][1]
+
+    def to_c(self) -> SgaConfig:
+        s_h, s_w = self.s_hw
+        c = SgaConfig()
+        c.B, c.H, c.N = self.B, self.H, self.N
+        c.grid_h, c.grid_w, c.n_special, c.head_dim = self.grid_h, self.grid_w, self.n_special, self.head_dim
+        c.s_h, c.s_w = s_h, s_w
+        c.phase_shift, c.ref_frame_dense = int(self.phase_shift), int(self.ref_frame_dense)
+        c.diag, c.mean = int(self.diag), int(self.mean)
+        c.mean_mode = _MEAN_MODES[self.mean_mode]
+        c.dtype = _DTYPES[self.dtype][0]
+        c.kernel = _KERNELS[self.kernel]
+        return c
+
+
+def plan_host(cfg: SGAConfig):
+    """Kept set S computed by the library's host builder: (kv_index, frame_off, slot)."""
+    c = cfg.to_c()
+    kv = np.zeros(cfg.T, dtype=np.int32)
+    off = np.zeros(cfg.N + 1, dtype=np.int32)
+    slot = np.zeros(cfg.T, dtype=np.int32)
+    n = ctypes.c_int64(0)
+    check("sga_plan_host", lib().sga_plan_host(ctypes.byref(c), kv.ctypes.data, off.ctypes.data,
+                                              slot.ctypes.data, ctypes.byref(n)))
+    return kv[: n.value].copy(), off, slot
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_tensor(name, t, shape, dtype, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+class Plan:
+    """Device-resident kept set of one layer configuration (owns the library's plan)."""
+
+    def __init__(self, cfg: SGAConfig, device=None):
+        if device is None:
+            device = torch.device("cuda", torch.cuda.current_device())
+        self.device = torch.device(device)
+        self.cfg = cfg
+        self._h = ctypes.c_void_p()
+        c = cfg.to_c()
+        with torch.cuda.device(self.device):
+            check("sga_plan_create", lib().sga_plan_create(ctypes.byref(c), self.device.index, ctypes.byref(self._h)))
+        T, S, D = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        check("sga_plan_info", lib().sga_plan_info(self._h, ctypes.byref(T), ctypes.byref(S), ctypes.byref(D)))
+        self.T, self.S, self.dropped = T.value, S.value, D.value
+
+    def indices(self):
+        kv = np.zeros(max(self.S, 1), dtype=np.int32)
+        off = np.zeros(self.cfg.N + 1, dtype=np.int32)
+        check("sga_plan_copy_indices", lib().sga_plan_copy_indices(self._h, kv.ctypes.data, off.ctypes.data))
+        return kv[: self.S], off
+
+    def close(self):
+        if self._h:
+            lib().sga_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------ steps of the layer
+    def compact(self, K, V, K_S=None, V_S=None, k_sum=None, v_sum=None):
+        """K_S, V_S (kept rows) and k_sum, v_sum (sums of the dropped rows, fp32)."""
+        cfg, dev = self.cfg, self.device
+        shp = (cfg.B, cfg.H, self.T, 64)
+        _check_tensor("K", K, shp, cfg.torch_dtype, dev)
+        _check_tensor("V", V, shp, cfg.torch_dtype, dev)
+        ks_shape = (cfg.B, cfg.H, self.S, 64)
+        K_S = torch.empty(ks_shape, dtype=cfg.torch_dtype, device=dev) if K_S is None else K_S
+        V_S = torch.empty(ks_shape, dtype=cfg.torch_dtype, device=dev) if V_S is None else V_S
+        k_sum = torch.empty((cfg.B, cfg.H, 64), dtype=torch.float32, device=dev) if k_sum is None else k_sum
+        v_sum = torch.empty((cfg.B, cfg.H, 64), dtype=torch.float32, device=dev) if v_sum is None else v_sum
+        _check_tensor("K_S", K_S, ks_shape, cfg.torch_dtype, dev)
+        _check_tensor("V_S", V_S, ks_shape, cfg.torch_dtype, dev)
+        _check_tensor("k_sum", k_sum, (cfg.B, cfg.H, 64), torch.float32, dev)
+        _check_tensor("v_sum", v_sum, (cfg.B, cfg.H, 64), torch.float32, dev)
+        with torch.cuda.device(dev):
+            check("sga_compact", lib().sga_compact(self._h, _ptr(K), _ptr(V), _ptr(K_S), _ptr(V_S),
+                                                   _ptr(k_sum), _ptr(v_sum), _stream(dev)))
+        return K_S, V_S, k_sum, v_sum
+
+    def forward(self, Q, K, V, K_S, V_S, k_sum, v_sum, out=None, lse=None, scale=None):
+        """SGA attention output [B, H, T, 64]; ``lse`` (fp32 [B, H, T]) is filled when given."""
+        cfg, dev = self.cfg, self.device
+        shp = (cfg.B, cfg.H, self.T, 64)
+        for n, t in (("Q", Q), ("K", K), ("V", V)):
+            _check_tensor(n, t, shp, cfg.torch_dtype, dev)
+        out = torch.empty(shp, dtype=cfg.torch_dtype, device=dev) if out is None else out
+        _check_tensor("out", out, shp, cfg.torch_dtype, dev)
+        if lse is not None:
+            _check_tensor("lse", lse, shp[:3], torch.float32, dev)
+        scale = 1.0 / math.sqrt(64) if scale is None else float(scale)
+        with torch.cuda.device(dev):
+            check("sga_forward", lib().sga_forward(self._h, _ptr(Q), _ptr(K), _ptr(V), _ptr(K_S), _ptr(V_S),
+                                                   _ptr(k_sum), _ptr(v_sum), _ptr(out), _ptr(lse),
+                                                   ctypes.c_float(scale), _stream(dev)))
+        return out
+
+    def layer(self, Q, K, V, out=None, lse=None, scale=None):
+        """The whole SGA layer: compaction, then attention."""
+        K_S, V_S, k_sum, v_sum = self.compact(K, V)
+        return self.forward(Q, K, V, K_S, V_S, k_sum, v_sum, out=out, lse=lse, scale=scale)
+
+
+def _plain(kind, Q, K, V, N, L, dtype, kernel, out, lse, scale):
+    B, H, T, d = Q.shape
+    tdt = _DTYPES[dtype][1]
+    dev = Q.device
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _check_tensor(n, t, (B, H, T, d), tdt, dev)
+    out = torch.empty_like(Q) if out is None else out
+    _check_tensor("out", out, (B, H, T, d), tdt, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, (B, H, T), torch.float32, dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        if kind == "dense":
+            st = lib().sga_dense_forward(B, H, T, d, _DTYPES[dtype][0], _KERNELS[kernel], _ptr(Q), _ptr(K),
+                                         _ptr(V), _ptr(out), _ptr(lse), ctypes.c_float(scale), _stream(dev))
+        else:
+            if N * L != T:
+                raise ValueError(f"N*L = {N * L} does not match T = {T}")
+            st = lib().sga_frame_forward(B, H, N, L, d, _DTYPES[dtype][0], _KERNELS[kernel], _ptr(Q), _ptr(K),
+                                         _ptr(V), _ptr(out), _ptr(lse), ctypes.c_float(scale), _stream(dev))
+    check(f"sga_{kind}_forward", st)
+    return out
+
+
+def dense_forward(Q, K, V, *, dtype="bf16", kernel="auto", out=None, lse=None, scale=None):
+    """Dense global attention over all N*L tokens ("AVGGT ...", the standard attention, sigma = 1)."""
+    return _plain("dense", Q, K, V, 0, 0, dtype, kernel, out, lse, scale)
+
+
+def frame_forward(Q, K, V, N, L, *, dtype="bf16", kernel="auto", out=None, lse=None, scale=None):
+    """Frame-local attention ("AVGGT ..." Key design 1, Global-to-Frame)."""
+    return _plain("frame", Q, K, V, N, L, dtype, kernel, out, lse, scale)
+
+
+def device_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device's kernel status word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().sga_device_status(_stream(dev)))
+
+
+def layer_from_host(plan: Plan, Q_host, K_host, V_host, out_host=None, scale=None):
+    """End-to-end call from host memory: copy pinned Q, K, V to the device, run the layer, copy
+    the output back (all on the current stream)."""
+    dev = plan.device
+    Q = Q_host.to(dev, non_blocking=True)
+    K = K_host.to(dev, non_blocking=True)
+    V = V_host.to(dev, non_blocking=True)
+    O = plan.layer(Q, K, V, scale=scale)
+    if out_host is None:
+        out_host = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+    out_host.copy_(O, non_blocking=True)
+    return out_host

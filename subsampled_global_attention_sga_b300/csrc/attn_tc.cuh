@@ -1,0 +1,398 @@
+// attn_tc.cuh -- tensor-core attention kernel for sm_103a (bf16 in, fp32 accumulate):
+// TMA-staged tiles, tcgen05.mma with accumulators in Tensor Memory, online softmax on the
+// CUDA cores, persistent CTAs.  One kernel serves SGA (keys = the compacted K_S/V_S, plus the
+// diagonal and mean components folded into each row's running max and sum), dense global
+// attention and frame-local attention (keys = one frame).
+//
+// Sources: "AVGGT: Rethinking Global Attention for Accelerating VGGT", Key design 2 (attention
+// softmax(QK^T/sqrt(d))V over the kept set, all queries kept) and Key design 3 (the diagonal
+// and mean components share the softmax); "RegimeVGGT ...", Key design 2 (ln g logit bias).
+//
+// Work unit: two 128-row query tiles of one segment (a (batch, head) pair, or one frame of it)
+// against all key tiles of that segment.  Roles (384 threads):
+//   warp 0      TMA producer: the two Q tiles, then a STAGES-deep ring of K and V tiles
+//   warp 1      TMEM owner and MMA issuer (one thread):
+//                 S_t = Q_t K_j^T  (M=128, N=128, K=64; A, B from shared memory)
+//                 O_t += P_t V_j   (M=128, N=64,  K=128; P from TMEM, V from shared memory)
+//   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
+//   warps 8-11  softmax + epilogue of query tile 1
+// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384) P_0 [384,448) P_1 [448,512).
+// The two tiles ping-pong: while one tile's rows are exponentiated the tensor core runs the
+// other tile's products.  A running max is only moved (and O rescaled in TMEM) when a row's
+// maximum grows by more than 2^8; the final normalisation uses the same reference, so the
+// result is exact either way.
+#pragma once
+
+#include "extras.cuh"
+
+namespace sga {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int HD = 64;
+constexpr int STAGES = 4;
+constexpr int TILE_BYTES = BM * HD * 2;        // one 128 x 64 bf16 tile = 16 KB
+constexpr int NUM_THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * (uint32_t)t; }         // S_t
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 64u * (uint32_t)t; }   // O_t
+__host__ __device__ constexpr uint32_t col_p(int t) { return 384u + 64u * (uint32_t)t; }   // P_t
+constexpr float kRescaleThreshold = 8.0f;      // base-2: rescale when the max grows by > 2^8
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
+constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+// barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
+//           p_ready[2], o_done[2], o_free[2], drain
+constexpr int NUM_BARS = 2 + 4 * STAGES + 8 + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, true);
+
+struct TcArgs {
+    int n_seg;              // segments
+    int seg_rows;           // query rows per segment
+    int kv_rows;            // keys per segment
+    int n_pairs;            // work units per segment (pairs of 128-row query tiles)
+    int n_kv_tiles;         // ceil(kv_rows / 128)
+    long long n_units;      // n_seg * n_pairs
+    float scale_log2;       // scale * log2(e)
+    const __nv_bfloat16* Q; // [n_seg, seg_rows, 64] (rows read for the extra components)
+    __nv_bfloat16* O;       // [n_seg, seg_rows, 64]
+    float* lse;             // [n_seg, seg_rows] or null
+    ExtraArgs ex;           // ex.on only for SGA (segment = batch*head)
+};
+
+struct Bars {
+    uint32_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+    uint32_t s_full[2], p_ready[2], o_done[2], o_free[2], drain;
+};
+
+__device__ __forceinline__ Bars make_bars(uint32_t base) {
+    Bars b;
+    uint32_t a = base;
+    b.q_full = a; a += 8;
+    b.q_empty = a; a += 8;
+    for (int s = 0; s < STAGES; ++s) { b.k_full[s] = a; a += 8; }
+    for (int s = 0; s < STAGES; ++s) { b.k_empty[s] = a; a += 8; }
+    for (int s = 0; s < STAGES; ++s) { b.v_full[s] = a; a += 8; }
+    for (int s = 0; s < STAGES; ++s) { b.v_empty[s] = a; a += 8; }
+    for (int t = 0; t < 2; ++t) { b.s_full[t] = a; a += 8; }
+    for (int t = 0; t < 2; ++t) { b.p_ready[t] = a; a += 8; }
+    for (int t = 0; t < 2; ++t) { b.o_done[t] = a; a += 8; }
+    for (int t = 0; t < 2; ++t) { b.o_free[t] = a; a += 8; }
+    b.drain = a;
+    return b;
+}
+
+// Bounded wait without the abort check: used only to drain work already in flight.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kTimeoutCycles / 8) {
+            atomicExch(&g_status, (int)SGA_ERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
+// warp-uniform bounded wait (tcgen05.ld/st that follow are warp-collective)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void ld_row128(uint32_t taddr, float (&s)[128]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        tmem_ld32(taddr + 32 * c, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const TcArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(base);
+    const Bars bars = make_bars(sbase + OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bars.k_full[s], 1);
+            mbar_init(bars.k_empty[s], 1);
+            mbar_init(bars.v_full[s], 1);
+            mbar_init(bars.v_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bars.s_full[t], 1);
+            mbar_init(bars.p_ready[t], 128);
+            mbar_init(bars.o_done[t], 1);
+            mbar_init(bars.o_free[t], 128);
+        }
+        mbar_init(bars.drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_kv = p.n_kv_tiles;
+    const int last_valid = p.kv_rows - (n_kv - 1) * BN;     // keys in the last tile (1..128)
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t kv_it = 0, k_issued = 0, v_issued = 0, q_issued = 0, u_local = 0;
+            bool ok = true;
+            for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
+                const int seg = (int)(u / p.n_pairs);
+                const int row0 = (int)(u % p.n_pairs) * 2 * BM;
+                if (!mbar_wait(bars.q_empty, (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(bars.q_full, 2 * TILE_BYTES);
+                tma_load_3d(sbase + OFF_Q, &tmQ, bars.q_full, 0, row0, seg);
+                tma_load_3d(sbase + OFF_Q + TILE_BYTES, &tmQ, bars.q_full, 0, row0 + BM, seg);
+                ++q_issued;
+                for (int j = 0; j < n_kv; ++j, ++kv_it) {
+                    const int st = kv_it % STAGES;
+                    const uint32_t ph = (kv_it / STAGES) & 1;
+                    if (!mbar_wait(bars.k_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bars.k_full[st], TILE_BYTES);
+                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full[st], 0, j * BN, seg);
+                    ++k_issued;
+                    if (!mbar_wait(bars.v_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bars.v_full[st], TILE_BYTES);
+                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.v_full[st], 0, j * BN, seg);
+                    ++v_issued;
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA leaves
+                for (uint32_t i = (k_issued > STAGES ? k_issued - STAGES : 0); i < k_issued; ++i)
+                    drain_wait(bars.k_full[i % STAGES], (i / STAGES) & 1);
+                for (uint32_t i = (v_issued > STAGES ? v_issued - STAGES : 0); i < v_issued; ++i)
+                    drain_wait(bars.v_full[i % STAGES], (i / STAGES) & 1);
+                if (q_issued > 0) drain_wait(bars.q_full, (q_issued - 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t kv_it = 0, g_it = 0, u_local = 0;
+            bool ok = true;
+            const uint32_t tS[2] = {tmem + col_s(0), tmem + col_s(1)};
+            const uint32_t tO[2] = {tmem + col_o(0), tmem + col_o(1)};
+            const uint32_t tP[2] = {tmem + col_p(0), tmem + col_p(1)};
+            auto issue_qk = [&](int t, int st) {
+                const uint32_t qa = sbase + OFF_Q + t * TILE_BYTES;
+                const uint32_t ka = sbase + OFF_K + st * TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    mma_ss(tS[t], smem_desc_sw128(qa + 32 * kk, 16), smem_desc_sw128(ka + 32 * kk, 16),
+                           IDESC_QK, kk > 0 ? 1u : 0u);
+            };
+            auto issue_pv = [&](int t, int st, uint32_t acc) {
+                const uint32_t va = sbase + OFF_V + st * TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tO[t], tP[t] + 8 * kk, smem_desc_sw128(va + 2048 * kk, TILE_BYTES),
+                           IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+            };
+            for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
+                if (!mbar_wait(bars.q_full, u_local & 1, abort_flag)) { ok = false; break; }
+                {
+                    const int st = kv_it % STAGES;
+                    if (!mbar_wait(bars.k_full[st], (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_qk(0, st);
+                    mma_commit(bars.s_full[0]);
+                    issue_qk(1, st);
+                    mma_commit(bars.s_full[1]);
+                }
+                for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_it) {
+                    const int st = kv_it % STAGES;
+                    const uint32_t ph = (kv_it / STAGES) & 1;
+                    const bool has_next = (j + 1 < n_kv);
+                    const int stn = (kv_it + 1) % STAGES;
+                    const uint32_t phn = ((kv_it + 1) / STAGES) & 1;
+                    mma_commit(bars.k_empty[st]);               // both QK_j issued
+                    if (has_next && !mbar_wait(bars.k_full[stn], phn, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(bars.v_full[st], ph, abort_flag)) { ok = false; break; }
+                    for (int t = 0; t < 2; ++t) {
+                        if (!mbar_wait(bars.p_ready[t], g_it & 1, abort_flag)) { ok = false; break; }
+                        if (j == 0 && !mbar_wait(bars.o_free[t], (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(t, st, j > 0 ? 1u : 0u);
+                        if (t == 1) mma_commit(bars.v_empty[st]);
+                        if (has_next) {
+                            issue_qk(t, stn);
+                            mma_commit(bars.s_full[t]);
+                        } else {
+                            mma_commit(bars.o_done[t]);
+                        }
+                    }
+                    if (!ok) break;
+                }
+                if (!ok) break;
+                mma_commit(bars.q_empty);
+            }
+            // every MMA issued so far completes before TMEM is released
+            mma_commit(bars.drain);
+            drain_wait(bars.drain, 0);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------------ softmax + epilogue
+        const int t = (warp - 4) >> 2;                  // query tile of this warpgroup
+        const int sub = warp & 3;                       // TMEM lanes [32*sub, 32*sub+32)
+        const int r_in_tile = sub * 32 + lane;
+        const uint32_t lane_bits = (uint32_t)(sub * 32) << 16;
+        const uint32_t tS = tmem + lane_bits + col_s(t);
+        const uint32_t tO = tmem + lane_bits + col_o(t);
+        const uint32_t tP = tmem + lane_bits + col_p(t);
+        const float sl2 = p.scale_log2;
+        uint32_t g_it = 0, u_local = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
+            const int seg = (int)(u / p.n_pairs);
+            const int row = (int)(u % p.n_pairs) * 2 * BM + t * BM + r_in_tile;
+            const bool valid = row < p.seg_rows;
+
+            float m = -INFINITY, l = 0.f;
+            ExtraRow xr{};
+            if (p.ex.on && valid) {
+                float q[64];
+                load_row64<__nv_bfloat16>(p.Q + ((long long)seg * p.seg_rows + row) * 64, q);
+                xr = extra_logits<__nv_bfloat16>(p.ex, seg, row, q, sl2);
+                m = fmaxf(xr.s_diag, xr.s_mean);
+                if (m != -INFINITY)
+                    l = (xr.s_diag == -INFINITY ? 0.f : exp2f(xr.s_diag - m)) +
+                        (xr.s_mean == -INFINITY ? 0.f : exp2f(xr.s_mean - m));
+            }
+
+            for (int j = 0; j < n_kv; ++j, ++g_it) {
+                if (!warp_wait(bars.s_full[t], g_it & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                float s[128];
+                ld_row128(tS, s);
+                tmem_wait_ld();
+                if (j == n_kv - 1 && last_valid < BN) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= last_valid) s[c] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < 127; c += 2) mx = max3f(mx, s[c], s[c + 1]);
+                mx = fmaxf(mx, s[127]);
+                const float m_cand = mx * sl2;
+                const bool need = m_cand > m + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = fmaxf(m, m_cand);
+                    const float alpha = ex2_approx(m - m_new);   // 0 when m = -inf
+                    l *= alpha;
+                    if (j > 0) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            tmem_ld32(tO + 32 * c, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(tO + 32 * c, r);
+                        }
+                    }
+                    m = m_new;
+                }
+                const float nm = -m;
+                uint32_t pk[64];
+                float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = ex2_approx(fmaf(s[2 * c], sl2, nm));
+                    const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, nm));
+                    lsum0 += p0;
+                    lsum1 += p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                l += lsum0 + lsum1;
+                tmem_st16(tP + 0, pk + 0);
+                tmem_st16(tP + 16, pk + 16);
+                tmem_st16(tP + 32, pk + 32);
+                tmem_st16(tP + 48, pk + 48);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bars.p_ready[t]);
+            }
+            if (!ok) break;
+
+            // epilogue: O from TMEM, extra components, normalisation, store
+            if (!warp_wait(bars.o_done[t], u_local & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            float o[64];
+            {
+                uint32_t r[32];
+                tmem_ld32(tO, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+                tmem_ld32(tO + 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[32 + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(bars.o_free[t]);
+            if (valid) {
+                if (p.ex.on) extra_values<__nv_bfloat16, 64>(p.ex, seg, row, xr, m, 0, o);
+                const float inv_l = 1.0f / l;
+                const long long grow = (long long)seg * p.seg_rows + row;
+                uint4* dst = reinterpret_cast<uint4*>(p.O + grow * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16x2(o[8 * c + 0] * inv_l, o[8 * c + 1] * inv_l);
+                    w.y = pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l);
+                    w.z = pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l);
+                    w.w = pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l);
+                    dst[c] = w;
+                }
+                if (p.lse) p.lse[grow] = (m + log2f(l)) * 0.69314718055994531f;
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace tc
+}  // namespace sga

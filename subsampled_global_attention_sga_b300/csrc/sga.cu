@@ -1,0 +1,500 @@
+// sga.cu -- libsga: the C ABI declared in include/sga.h, the host-side plan builder and the
+// kernel launchers.  Single translation unit: every kernel of the library is included here.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "attn_simt.cuh"
+#include "attn_tc.cuh"
+#include "compact.cuh"
+
+namespace {
+
+constexpr uint32_t kPlanMagic = 0x53474150u;   // "SGAP"
+constexpr int kCompactRowsPerChunk = 2048;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool init = false;
+    int sm_count = 0;
+    bool tc_smem_set = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+}  // namespace
+
+struct sga_plan_s {
+    uint32_t magic;
+    sga_config cfg;
+    int device;
+    long long L, T, S, D;
+    int n_chunks;
+    int32_t* d_slot;        // [T]
+    int32_t* d_kv_index;    // [S]
+    int32_t* d_frame_off;   // [N+1]
+    float* d_partials;      // [B*H, n_chunks, 128]
+    std::vector<int32_t> h_kv_index;
+    std::vector<int32_t> h_frame_off;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sga_status device_info(int dev, DeviceInfo** out) {
+    if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SGA_ERR_CUDA;
+        d.init = true;
+    }
+    *out = &d;
+    return SGA_OK;
+}
+
+sga_status current_device(int* dev) {
+    return cudaGetDevice(dev) == cudaSuccess ? SGA_OK : SGA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a contiguous [n_seg, rows, 64] bf16 tensor, box = 128 rows x 64 columns,
+// 128-byte swizzle (rows are exactly 128 bytes), zero fill outside [0, rows).
+sga_status make_map(CUtensorMap* map, const void* ptr, long long rows, long long n_seg) {
+    auto fn = encode_fn();
+    if (!fn) return SGA_ERR_CUDA;
+    if (rows <= 0 || n_seg <= 0 || rows > 0x7FFFFFFFLL || n_seg > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)n_seg};
+    cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGA_OK : SGA_ERR_CUDA;
+}
+
+sga_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? SGA_OK : SGA_ERR_CUDA;
+}
+
+// Problem description shared by the three attention entry points.
+struct AttnProblem {
+    int dtype;
+    int kernel;
+    int n_seg;
+    long long seg_rows;
+    long long kv_rows;
+    const void* Q;
+    const void* Kt;
+    const void* Vt;
+    void* O;
+    float* lse;
+    float scale;
+    sga::ExtraArgs ex;
+};
+
+sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
+    int dev;
+    if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
+    DeviceInfo* di;
+    sga_status st = device_info(dev, &di);
+    if (st != SGA_OK) return st;
+    const float scale_log2 = pb.scale * 1.4426950408889634f;
+    int kern = pb.kernel;
+    if (kern == SGA_KERNEL_AUTO) kern = (pb.dtype == SGA_BF16) ? SGA_KERNEL_TC : SGA_KERNEL_SIMT;
+    if (kern == SGA_KERNEL_TC) {
+        if (pb.dtype != SGA_BF16) return SGA_ERR_UNSUPPORTED;
+        if (pb.seg_rows > 0x7FFFFFFFLL || pb.kv_rows > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+        namespace T = sga::tc;
+        {
+            std::lock_guard<std::mutex> lk(g_dev_mu);
+            if (!di->tc_smem_set) {
+                if (cudaFuncSetAttribute(T::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::SMEM_BYTES) != cudaSuccess)
+                    return SGA_ERR_CUDA;
+                di->tc_smem_set = true;
+            }
+        }
+        CUtensorMap mq, mk, mv;
+        if ((st = make_map(&mq, pb.Q, pb.seg_rows, pb.n_seg)) != SGA_OK) return st;
+        if ((st = make_map(&mk, pb.Kt, pb.kv_rows, pb.n_seg)) != SGA_OK) return st;
+        if ((st = make_map(&mv, pb.Vt, pb.kv_rows, pb.n_seg)) != SGA_OK) return st;
+        T::TcArgs a;
+        a.n_seg = pb.n_seg;
+        a.seg_rows = (int)pb.seg_rows;
+        a.kv_rows = (int)pb.kv_rows;
+        const long long q_tiles = (pb.seg_rows + T::BM - 1) / T::BM;
+        a.n_pairs = (int)((q_tiles + 1) / 2);
+        a.n_kv_tiles = (int)((pb.kv_rows + T::BN - 1) / T::BN);
+        a.n_units = (long long)a.n_seg * a.n_pairs;
+        a.scale_log2 = scale_log2;
+        a.Q = reinterpret_cast<const __nv_bfloat16*>(pb.Q);
+        a.O = reinterpret_cast<__nv_bfloat16*>(pb.O);
+        a.lse = pb.lse;
+        a.ex = pb.ex;
+        const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
+        T::attn_tc_kernel<<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+        return launch_status();
+    }
+    if (kern != SGA_KERNEL_SIMT) return SGA_ERR_INVALID_ARG;
+    sga::SimtArgs a;
+    a.seg_rows = pb.seg_rows;
+    a.kv_rows = pb.kv_rows;
+    a.Q = pb.Q;
+    a.Kt = pb.Kt;
+    a.Vt = pb.Vt;
+    a.O = pb.O;
+    a.lse = pb.lse;
+    a.scale_log2 = scale_log2;
+    a.ex = pb.ex;
+    const long long gx = (pb.seg_rows + sga::kSimtRows - 1) / sga::kSimtRows;
+    if (gx > 0x7FFFFFFFLL || pb.n_seg > 65535) return SGA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)gx, (unsigned)pb.n_seg);
+    if (pb.dtype == SGA_BF16)
+        sga::attn_simt_kernel<__nv_bfloat16><<<grid, sga::kSimtRows, 0, stream>>>(a);
+    else if (pb.dtype == SGA_F32)
+        sga::attn_simt_kernel<float><<<grid, sga::kSimtRows, 0, stream>>>(a);
+    else
+        return SGA_ERR_UNSUPPORTED;
+    return launch_status();
+}
+
+sga_status check_plan(sga_plan_t plan) {
+    if (!plan || plan->magic != kPlanMagic) return SGA_ERR_PLAN_MISMATCH;
+    int dev;
+    if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
+    return dev == plan->device ? SGA_OK : SGA_ERR_PLAN_MISMATCH;
+}
+
+sga_status check_common(int dtype, int head_dim, int kernel) {
+    if (head_dim != 64) return SGA_ERR_UNSUPPORTED;
+    if (dtype != SGA_BF16 && dtype != SGA_F32) return SGA_ERR_UNSUPPORTED;
+    if (kernel < SGA_KERNEL_AUTO || kernel > SGA_KERNEL_SIMT) return SGA_ERR_INVALID_ARG;
+    if (kernel == SGA_KERNEL_TC && dtype != SGA_BF16) return SGA_ERR_UNSUPPORTED;
+    return SGA_OK;
+}
+
+// Kept set S of a layer.  Membership of a frame's slots depends only on the frame's phase
+// (and on frame 0 being the dense reference), so one mask per phase is built and reused.
+//   kept: frame 0 when it is the dense reference; the n_special camera/register slots of every
+//   frame; a patch (r, c) with r = phi_r (mod s_h) and c = phi_c (mod s_w), the first patch of
+//   its window, where phi = 0 without the phase shift and phi_r = (f div s_w) mod s_h,
+//   phi_c = f mod s_w with it.
+void build_plan(const sga_config& c, std::vector<int32_t>& slot, std::vector<int32_t>& kv,
+                std::vector<int32_t>& off) {
+    const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
+    const long long T = L * c.N;
+    slot.assign((size_t)T, -1);
+    kv.clear();
+    kv.reserve((size_t)T);
+    off.assign((size_t)c.N + 1, 0);
+    std::vector<uint8_t> mask((size_t)L);
+    int cached_pr = -1, cached_pc = -1;
+    for (int f = 0; f < c.N; ++f) {
+        off[f] = (int32_t)kv.size();
+        const bool dense = (f == 0 && c.ref_frame_dense) || (c.s_h == 1 && c.s_w == 1);
+        const int pr = c.phase_shift ? (f / c.s_w) % c.s_h : 0;
+        const int pc = c.phase_shift ? f % c.s_w : 0;
+        if (!dense && (pr != cached_pr || pc != cached_pc)) {
+            for (long long p = 0; p < L; ++p) {
+                if (p < c.n_special) { mask[p] = 1; continue; }
+                const long long r = (p - c.n_special) / c.grid_w, col = (p - c.n_special) % c.grid_w;
+                mask[p] = (r >= pr && (r - pr) % c.s_h == 0 && col >= pc && (col - pc) % c.s_w == 0) ? 1 : 0;
+            }
+            cached_pr = pr;
+            cached_pc = pc;
+        }
+        for (long long p = 0; p < L; ++p) {
+            const long long t = (long long)f * L + p;
+            if (dense || mask[p]) {
+                slot[t] = (int32_t)kv.size();
+                kv.push_back((int32_t)t);
+            }
+        }
+    }
+    off[c.N] = (int32_t)kv.size();
+}
+
+sga_status check_config(const sga_config* cfg) {
+    if (!cfg) return SGA_ERR_INVALID_ARG;
+    const sga_config& c = *cfg;
+    if (c.B <= 0 || c.H <= 0 || c.N <= 0 || c.grid_h <= 0 || c.grid_w <= 0 || c.n_special < 0 ||
+        c.s_h <= 0 || c.s_w <= 0)
+        return SGA_ERR_INVALID_ARG;
+    if (c.mean_mode != SGA_MEAN_LOO && c.mean_mode != SGA_MEAN_GLOBAL) return SGA_ERR_INVALID_ARG;
+    sga_status st = check_common(c.dtype, c.head_dim, c.kernel);
+    if (st != SGA_OK) return st;
+    const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
+    if (L * c.N > 0x7FFFFFFFLL || (long long)c.B * c.H > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    return SGA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sga_status_string(sga_status s) {
+    switch (s) {
+        case SGA_OK: return "ok";
+        case SGA_ERR_INVALID_ARG: return "invalid argument";
+        case SGA_ERR_UNSUPPORTED: return "unsupported (head_dim must be 64; dtype bf16 or f32)";
+        case SGA_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+        case SGA_ERR_CUDA: return "CUDA runtime or driver error";
+        case SGA_ERR_TIMEOUT: return "kernel wait timed out";
+        case SGA_ERR_PLAN_MISMATCH: return "plan invalid or created for another device";
+    }
+    return "unknown status";
+}
+
+const char* sga_build_info(void) { return "libsga sm_103a (tcgen05/TMEM/TMA attention, CUDA-core fp32 path) v1"; }
+
+sga_status sga_plan_create(const sga_config* cfg, int device, sga_plan_t* out) {
+    if (!cfg || !out) return SGA_ERR_INVALID_ARG;
+    *out = nullptr;
+    sga_status st = check_config(cfg);
+    if (st != SGA_OK) return st;
+    const sga_config& c = *cfg;
+    const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
+    const long long T = L * c.N;
+
+    std::vector<int32_t> slot((size_t)T);
+    std::vector<int32_t> kv;
+    std::vector<int32_t> off((size_t)c.N + 1);
+    build_plan(c, slot, kv, off);
+
+    sga_plan_s* plan = new (std::nothrow) sga_plan_s();
+    if (!plan) return SGA_ERR_CUDA;
+    plan->magic = kPlanMagic;
+    plan->cfg = c;
+    plan->device = device;
+    plan->L = L;
+    plan->T = T;
+    plan->S = (long long)kv.size();
+    plan->D = T - plan->S;
+    plan->n_chunks = (int)((T + kCompactRowsPerChunk - 1) / kCompactRowsPerChunk);
+    plan->h_kv_index = kv;
+    plan->h_frame_off = off;
+    plan->d_slot = nullptr;
+    plan->d_kv_index = nullptr;
+    plan->d_frame_off = nullptr;
+    plan->d_partials = nullptr;
+
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        delete plan;
+        return SGA_ERR_CUDA;
+    }
+    bool okc = true;
+    const size_t part_bytes = (size_t)c.B * c.H * plan->n_chunks * 128 * sizeof(float);
+    okc = okc && cudaMalloc(&plan->d_slot, sizeof(int32_t) * (size_t)T) == cudaSuccess;
+    okc = okc && cudaMalloc(&plan->d_kv_index, sizeof(int32_t) * (size_t)(plan->S > 0 ? plan->S : 1)) == cudaSuccess;
+    okc = okc && cudaMalloc(&plan->d_frame_off, sizeof(int32_t) * (size_t)(c.N + 1)) == cudaSuccess;
+    okc = okc && cudaMalloc(&plan->d_partials, part_bytes) == cudaSuccess;
+    okc = okc && cudaMemcpy(plan->d_slot, slot.data(), sizeof(int32_t) * (size_t)T, cudaMemcpyHostToDevice) == cudaSuccess;
+    if (plan->S > 0)
+        okc = okc && cudaMemcpy(plan->d_kv_index, kv.data(), sizeof(int32_t) * (size_t)plan->S,
+                                cudaMemcpyHostToDevice) == cudaSuccess;
+    okc = okc && cudaMemcpy(plan->d_frame_off, off.data(), sizeof(int32_t) * (size_t)(c.N + 1),
+                            cudaMemcpyHostToDevice) == cudaSuccess;
+    okc = okc && cudaDeviceSynchronize() == cudaSuccess;
+    DeviceInfo* di;
+    okc = okc && device_info(device, &di) == SGA_OK;
+    cudaSetDevice(prev);
+    if (!okc) {
+        sga_plan_destroy(plan);
+        return SGA_ERR_CUDA;
+    }
+    *out = plan;
+    return SGA_OK;
+}
+
+sga_status sga_plan_host(const sga_config* cfg, int32_t* kv_index, int32_t* frame_off,
+                         int32_t* slot, int64_t* S_out) {
+    if (!kv_index || !frame_off || !S_out) return SGA_ERR_INVALID_ARG;
+    sga_status st = check_config(cfg);
+    if (st != SGA_OK) return st;
+    std::vector<int32_t> sl, kv, off;
+    build_plan(*cfg, sl, kv, off);
+    std::memcpy(kv_index, kv.data(), sizeof(int32_t) * kv.size());
+    std::memcpy(frame_off, off.data(), sizeof(int32_t) * off.size());
+    if (slot) std::memcpy(slot, sl.data(), sizeof(int32_t) * sl.size());
+    *S_out = (int64_t)kv.size();
+    return SGA_OK;
+}
+
+sga_status sga_plan_info(sga_plan_t plan, int64_t* T, int64_t* S, int64_t* dropped) {
+    if (!plan || plan->magic != kPlanMagic) return SGA_ERR_PLAN_MISMATCH;
+    if (T) *T = plan->T;
+    if (S) *S = plan->S;
+    if (dropped) *dropped = plan->D;
+    return SGA_OK;
+}
+
+sga_status sga_plan_copy_indices(sga_plan_t plan, int32_t* kv_index, int32_t* frame_off) {
+    if (!plan || plan->magic != kPlanMagic) return SGA_ERR_PLAN_MISMATCH;
+    if (kv_index && plan->S > 0) std::memcpy(kv_index, plan->h_kv_index.data(), sizeof(int32_t) * (size_t)plan->S);
+    if (frame_off) std::memcpy(frame_off, plan->h_frame_off.data(), sizeof(int32_t) * (size_t)(plan->cfg.N + 1));
+    return SGA_OK;
+}
+
+void sga_plan_destroy(sga_plan_t plan) {
+    if (!plan || plan->magic != kPlanMagic) return;
+    int prev = -1;
+    const bool switched = cudaGetDevice(&prev) == cudaSuccess && cudaSetDevice(plan->device) == cudaSuccess;
+    if (switched) cudaDeviceSynchronize();
+    cudaFree(plan->d_slot);
+    cudaFree(plan->d_kv_index);
+    cudaFree(plan->d_frame_off);
+    cudaFree(plan->d_partials);
+    if (switched) cudaSetDevice(prev);
+    plan->magic = 0;
+    delete plan;
+}
+
+sga_status sga_compact(sga_plan_t plan, const void* K, const void* V, void* K_S, void* V_S,
+                       float* k_sum, float* v_sum, void* stream) {
+    sga_status st = check_plan(plan);
+    if (st != SGA_OK) return st;
+    if (!K || !V || !K_S || !V_S || !k_sum || !v_sum) return SGA_ERR_INVALID_ARG;
+    if (!aligned16(K) || !aligned16(V) || !aligned16(K_S) || !aligned16(V_S) || !aligned16(k_sum) ||
+        !aligned16(v_sum))
+        return SGA_ERR_ALIGNMENT;
+    const sga_config& c = plan->cfg;
+    const int BH = c.B * c.H;
+    if (BH > 65535) return SGA_ERR_UNSUPPORTED;
+    sga::CompactArgs a;
+    a.T = plan->T;
+    a.S = plan->S;
+    a.rows_per_chunk = kCompactRowsPerChunk;
+    a.n_chunks = plan->n_chunks;
+    a.slot = plan->d_slot;
+    a.K = K;
+    a.V = V;
+    a.KS = K_S;
+    a.VS = V_S;
+    a.partials = plan->d_partials;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    dim3 grid((unsigned)plan->n_chunks, (unsigned)BH);
+    if (c.dtype == SGA_BF16)
+        sga::compact_kernel<__nv_bfloat16><<<grid, sga::kCompactThreads, 0, s>>>(a);
+    else
+        sga::compact_kernel<float><<<grid, sga::kCompactThreads, 0, s>>>(a);
+    if ((st = launch_status()) != SGA_OK) return st;
+    sga::compact_finalize_kernel<<<BH, 128, 0, s>>>(plan->d_partials, plan->n_chunks, k_sum, v_sum);
+    return launch_status();
+}
+
+sga_status sga_forward(sga_plan_t plan, const void* Q, const void* K, const void* V,
+                       const void* K_S, const void* V_S, const float* k_sum, const float* v_sum,
+                       void* O, float* lse, float scale, void* stream) {
+    sga_status st = check_plan(plan);
+    if (st != SGA_OK) return st;
+    if (!Q || !K || !V || !K_S || !V_S || !k_sum || !v_sum || !O) return SGA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(K_S) || !aligned16(V_S) ||
+        !aligned16(k_sum) || !aligned16(v_sum) || !aligned16(O) || (lse && !aligned16(lse)))
+        return SGA_ERR_ALIGNMENT;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return SGA_ERR_INVALID_ARG;
+    const sga_config& c = plan->cfg;
+    AttnProblem pb;
+    pb.dtype = c.dtype;
+    pb.kernel = c.kernel;
+    pb.n_seg = c.B * c.H;
+    pb.seg_rows = plan->T;
+    pb.kv_rows = plan->S;
+    pb.Q = Q;
+    pb.Kt = K_S;
+    pb.Vt = V_S;
+    pb.O = O;
+    pb.lse = lse;
+    pb.scale = scale;
+    pb.ex.on = (c.diag || c.mean) && plan->D > 0;
+    pb.ex.diag = c.diag;
+    pb.ex.mean = c.mean;
+    pb.ex.mean_mode = c.mean_mode;
+    pb.ex.dropped = plan->D;
+    pb.ex.T = plan->T;
+    pb.ex.slot = plan->d_slot;
+    pb.ex.K = K;
+    pb.ex.V = V;
+    pb.ex.k_sum = k_sum;
+    pb.ex.v_sum = v_sum;
+    return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static sga_status plain_attention(int n_seg, long long seg_rows, int dtype, int kernel, const void* Q,
+                                  const void* K, const void* V, void* O, float* lse, float scale,
+                                  void* stream) {
+    if (!Q || !K || !V || !O) return SGA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (lse && !aligned16(lse)))
+        return SGA_ERR_ALIGNMENT;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return SGA_ERR_INVALID_ARG;
+    AttnProblem pb;
+    std::memset(&pb, 0, sizeof(pb));
+    pb.dtype = dtype;
+    pb.kernel = kernel;
+    pb.n_seg = n_seg;
+    pb.seg_rows = seg_rows;
+    pb.kv_rows = seg_rows;
+    pb.Q = Q;
+    pb.Kt = K;
+    pb.Vt = V;
+    pb.O = O;
+    pb.lse = lse;
+    pb.scale = scale;
+    pb.ex.on = 0;
+    return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sga_status sga_dense_forward(int B, int H, int64_t T, int head_dim, int dtype, int kernel,
+                             const void* Q, const void* K, const void* V, void* O, float* lse,
+                             float scale, void* stream) {
+    if (B <= 0 || H <= 0 || T <= 0) return SGA_ERR_INVALID_ARG;
+    sga_status st = check_common(dtype, head_dim, kernel);
+    if (st != SGA_OK) return st;
+    if ((long long)B * H > 0x7FFFFFFFLL || T > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    return plain_attention(B * H, T, dtype, kernel, Q, K, V, O, lse, scale, stream);
+}
+
+sga_status sga_frame_forward(int B, int H, int N, int L, int head_dim, int dtype, int kernel,
+                             const void* Q, const void* K, const void* V, void* O, float* lse,
+                             float scale, void* stream) {
+    if (B <= 0 || H <= 0 || N <= 0 || L <= 0) return SGA_ERR_INVALID_ARG;
+    sga_status st = check_common(dtype, head_dim, kernel);
+    if (st != SGA_OK) return st;
+    if ((long long)B * H * N > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    return plain_attention(B * H * N, L, dtype, kernel, Q, K, V, O, lse, scale, stream);
+}
+
+sga_status sga_device_status(void* stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SGA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, sga::g_status, sizeof(int)) != cudaSuccess) return SGA_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(sga::g_status, &zero, sizeof(int)) != cudaSuccess) return SGA_ERR_CUDA;
+    }
+    return (sga_status)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+"""CPU-side checks of the library: the C ABI loads and exports every declared symbol, the host
+plan builder matches the oracle's kept set bit for bit, and argument validation rejects bad
+configurations before any device work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import subsampled_global_attention_sga_b300 as sga
+from subsampled_global_attention_sga_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "sga.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sga_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = sga.lib()
+    declared = _declared_functions()
+    assert declared, "no declarations parsed"
+    assert set(declared) == set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+    assert b"sm_103a" in L.sga_build_info()
+
+
+def test_status_strings():
+    L = sga.lib()
+    for s in range(7):
+        assert L.sga_status_string(s)
+
+
+def test_sigma_windows_match_golden():
+    rows = [list(map(int, l.split())) for l in open(os.path.join(GOLDEN, "sigma_map.txt"))
+            if l.strip() and not l.startswith("#")]
+    assert {s: (a, b) for s, a, b in rows} == sga.SIGMA_WINDOWS
+    with pytest.raises(ValueError):
+        sga.sigma_window(3)
+
+
+PLAN_CASES = [
+    (4, 8, 8, 5, 4, None, False, True),
+    (32, 37, 37, 5, 4, None, False, True),
+    (32, 37, 37, 5, 4, None, True, True),
+    (200, 37, 37, 5, 9, None, False, True),
+    (200, 37, 37, 5, 9, None, True, True),
+    (17, 37, 28, 5, 6, None, True, True),
+    (9, 7, 5, 5, 2, None, True, False),
+    (9, 7, 5, 0, 9, None, True, False),
+    (3, 1, 1, 5, 4, None, True, True),
+    (5, 6, 6, 2, 1, None, True, False),
+    (6, 9, 10, 5, 0, (3, 2), True, True),
+]
+
+
+@pytest.mark.parametrize("case", PLAN_CASES)
+def test_host_plan_bit_exact_vs_oracle(case):
+    N, gh, gw, nsp, sigma, window, phase, ref = case
+    cfg = sga.SGAConfig(B=1, H=1, N=N, grid_h=gh, grid_w=gw, n_special=nsp,
+                        sigma=sigma if sigma else 4, window=window, phase_shift=phase, ref_frame_dense=ref)
+    s_h, s_w = cfg.s_hw
+    kv, off, slot = sga.plan_host(cfg)
+    op = oracle.plan(N, gh, gw, nsp, s_h, s_w, phase, ref)
+    assert np.array_equal(kv, op.kv_index)
+    assert np.array_equal(off, op.frame_off)
+    want_slot = np.full(op.T, -1, dtype=np.int32)
+    want_slot[op.kv_index] = np.arange(op.S, dtype=np.int32)
+    assert np.array_equal(slot, want_slot)
+
+
+def test_headline_plan_counts():
+    for ph, S in ((False, 293808), (True, 278808)):
+        cfg = sga.SGAConfig(B=1, H=16, N=800, sigma=4, phase_shift=ph)
+        kv, off, _ = sga.plan_host(cfg)
+        assert len(kv) == S and off[-1] == S and cfg.T == 1099200
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=32), dict(N=0), dict(grid_h=0), dict(window=(0, 2)),
+                                 dict(mean_mode="loo", dtype="f32", kernel="tc")])
+def test_invalid_configs_rejected(bad):
+    kw = dict(B=1, H=1, N=2, grid_h=4, grid_w=4)
+    kw.update(bad)
+    cfg = sga.SGAConfig(**kw)
+    with pytest.raises(sga.SgaError):
+        sga.plan_host(cfg)
+
+
+def test_null_arguments_rejected_without_device():
+    L = sga.lib()
+    assert L.sga_plan_host(None, None, None, None, None) == 1
+    assert L.sga_plan_info(None, None, None, None) == 6
+    assert L.sga_compact(None, None, None, None, None, None, None, None) == 6
+    L.sga_plan_destroy(None)
+    # dense/frame validate shapes and pointers before touching the device
+    assert L.sga_dense_forward(1, 1, 128, 32, 0, 0, None, None, None, None, None, ctypes.c_float(0.125), None) == 2
+    assert L.sga_dense_forward(1, 1, 128, 64, 0, 0, None, None, None, None, None, ctypes.c_float(0.125), None) == 1
+    assert L.sga_frame_forward(1, 1, 0, 10, 64, 0, 0, None, None, None, None, None, ctypes.c_float(0.125), None) == 1
+    buf = (ctypes.c_char * 64)()
+    p = ctypes.addressof(buf) + 1  # misaligned
+    assert L.sga_dense_forward(1, 1, 4, 64, 0, 0, p, p, p, p, None, ctypes.c_float(0.125), None) == 3
