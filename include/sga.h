@@ -55,7 +55,8 @@ typedef enum {
     SGA_ERR_ALIGNMENT = 3,      /* a tensor pointer is not 16-byte aligned */
     SGA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (launch, memcpy, ...) */
     SGA_ERR_TIMEOUT = 5,        /* a kernel's bounded wait expired (reported by device status) */
-    SGA_ERR_PLAN_MISMATCH = 6   /* plan used with another device or a destroyed plan */
+    SGA_ERR_PLAN_MISMATCH = 6,  /* plan used with another device or a destroyed plan */
+    SGA_ERR_SCRATCH_LIMIT = 7   /* problem larger than sga_compact_noalloc's fixed scratch */
 } sga_status;
 
 typedef enum { SGA_BF16 = 0, SGA_F32 = 1 } sga_dtype;
@@ -145,6 +146,37 @@ sga_status sga_dense_forward(int B, int H, int64_t T, int head_dim, int dtype, i
 sga_status sga_frame_forward(int B, int H, int N, int L, int head_dim, int dtype, int kernel,
                              const void* Q, const void* K, const void* V, void* O, float* lse,
                              float scale, void* stream);
+
+/* Compaction that allocates nothing, for callers that cannot call cudaMalloc.  The pages have
+ * no counterpart: this entry point exists for integration only.
+ *
+ * Who needs it: code that runs where device allocation is off limits -- for example, inside
+ * an engine whose memory is fully reserved up front by its own allocator, a plug-in that the
+ * host framework forbids to allocate, or a step that must not pay for (or risk failing) an
+ * allocation.  Such a caller cannot create an sga_plan_t (sga_plan_create allocates the plan's
+ * index buffers and scratch).  This call needs no plan: it derives each token's place in K_S
+ * from `cfg` in closed form and keeps its only scratch -- the per-block partial sums of the
+ * dropped rows -- in a fixed array inside the library.
+ *
+ * Results are those of sga_compact with a plan for `cfg`: K_S, V_S [B, H, |S|, 64] get the
+ * kept rows of K, V [B, H, T, 64] in ascending token order (|S| from sga_plan_host or
+ * sga_plan_info), and k_sum, v_sum (fp32 [B, H, 64]) get the sums of the dropped rows.  All
+ * pointers are caller-owned device memory, 16-byte aligned.  No cudaMalloc, cudaFree or other
+ * allocating call is made.
+ *
+ * Limit: B * H * ceil(T / 2048) <= 16384 (the scratch holds 2^21 floats, 8 MiB, which every
+ * GPU that loads the library keeps until the process exits); larger problems return
+ * SGA_ERR_SCRATCH_LIMIT before anything is launched.  A layer of 800 frames of 1374 tokens
+ * with 16 heads (T = 1,099,200) needs 8592.
+ *
+ * The first call on a device looks up the scratch array's device address (once per device,
+ * with that device current); make that first call before any stream capture.  Every call on a
+ * device shares the one scratch array, so calls that may overlap on the GPU (other streams,
+ * other host threads) race and must be serialised by the caller.  The array keeps the last
+ * call's contents; nothing in it needs to start at zero because each call overwrites every
+ * partial it reads. */
+sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, const void* V, void* K_S,
+                               void* V_S, float* k_sum, float* v_sum, void* stream);
 
 /* Synchronise `stream`, then read and clear the device status word of the current device
  * (SGA_OK or SGA_ERR_TIMEOUT from a kernel's bounded wait).  Returns SGA_ERR_CUDA if the

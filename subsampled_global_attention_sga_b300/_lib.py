@@ -9,7 +9,7 @@ from ._build import LIB
 SGA_OK = 0
 STATUS_NAMES = {
     0: "SGA_OK", 1: "SGA_ERR_INVALID_ARG", 2: "SGA_ERR_UNSUPPORTED", 3: "SGA_ERR_ALIGNMENT",
-    4: "SGA_ERR_CUDA", 5: "SGA_ERR_TIMEOUT", 6: "SGA_ERR_PLAN_MISMATCH",
+    4: "SGA_ERR_CUDA", 5: "SGA_ERR_TIMEOUT", 6: "SGA_ERR_PLAN_MISMATCH", 7: "SGA_ERR_SCRATCH_LIMIT",
 }
 SGA_BF16, SGA_F32 = 0, 1
 SGA_MEAN_LOO, SGA_MEAN_GLOBAL = 0, 1
@@ -19,7 +19,7 @@ SGA_KERNEL_AUTO, SGA_KERNEL_TC, SGA_KERNEL_SIMT = 0, 1, 2
 EXPORTS = (
     "sga_plan_host", "sga_plan_create", "sga_plan_info", "sga_plan_copy_indices", "sga_plan_destroy",
     "sga_compact", "sga_forward", "sga_dense_forward", "sga_frame_forward", "sga_device_status",
-    "sga_status_string", "sga_build_info",
+    "sga_status_string", "sga_build_info", "sga_compact_noalloc",
 )
 
 
@@ -64,6 +64,7 @@ def lib():
             "sga_forward": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, vp]),
             "sga_dense_forward": (i32, [i32, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp]),
             "sga_frame_forward": (i32, [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp]),
+            "sga_compact_noalloc": (i32, [cfgp, vp, vp, vp, vp, vp, vp, vp]),
             "sga_device_status": (i32, [vp]),
             "sga_status_string": (ctypes.c_char_p, [i32]),
             "sga_build_info": (ctypes.c_char_p, []),

@@ -191,6 +191,26 @@ class Plan:
         return self.forward(Q, K, V, K_S, V_S, k_sum, v_sum, out=out, lse=lse, scale=scale)
 
 
+def compact_noalloc(cfg: SGAConfig, K, V, K_S, V_S, k_sum, v_sum):
+    """Compaction through ``sga_compact_noalloc``: no plan and no device allocation inside the
+    library (its scratch is a fixed array in the library; see include/sga.h).  Every output is
+    passed in by the caller; K_S/V_S are [B, H, |S|, 64] with |S| from ``plan_host``."""
+    dev = K.device
+    shp = (cfg.B, cfg.H, cfg.T, 64)
+    _check_tensor("K", K, shp, cfg.torch_dtype, dev)
+    _check_tensor("V", V, shp, cfg.torch_dtype, dev)
+    S = K_S.shape[2]
+    for n, t in (("K_S", K_S), ("V_S", V_S)):
+        _check_tensor(n, t, (cfg.B, cfg.H, S, 64), cfg.torch_dtype, dev)
+    for n, t in (("k_sum", k_sum), ("v_sum", v_sum)):
+        _check_tensor(n, t, (cfg.B, cfg.H, 64), torch.float32, dev)
+    c = cfg.to_c()
+    with torch.cuda.device(dev):
+        check("sga_compact_noalloc", lib().sga_compact_noalloc(ctypes.byref(c), _ptr(K), _ptr(V), _ptr(K_S),
+                                                               _ptr(V_S), _ptr(k_sum), _ptr(v_sum), _stream(dev)))
+    return K_S, V_S, k_sum, v_sum
+
+
 def _plain(kind, Q, K, V, N, L, dtype, kernel, out, lse, scale):
     B, H, T, d = Q.shape
     tdt = _DTYPES[dtype][1]

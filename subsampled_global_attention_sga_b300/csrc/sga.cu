@@ -12,6 +12,7 @@
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
 #include "compact.cuh"
+#include "compact_noalloc.cuh"
 
 namespace {
 
@@ -263,6 +264,7 @@ const char* sga_status_string(sga_status s) {
         case SGA_ERR_CUDA: return "CUDA runtime or driver error";
         case SGA_ERR_TIMEOUT: return "kernel wait timed out";
         case SGA_ERR_PLAN_MISMATCH: return "plan invalid or created for another device";
+        case SGA_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch of sga_compact_noalloc";
     }
     return "unknown status";
 }
@@ -498,3 +500,103 @@ sga_status sga_device_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// sga_compact_noalloc: the compaction for callers that cannot allocate device memory.
+//
+// Its only scratch -- the per-block partial sums of the dropped rows -- lives in the fixed
+// array below, which every GPU that loads this library holds until the process exits.  In host
+// code the array's name is a host-side stand-in, not a device address, so the address is looked
+// up once per device (with that device current) and passed to the kernel.
+constexpr long long kNoallocScratchFloats = 2LL * 1024 * 1024;   // 8 MiB: B*H*ceil(T/2048) <= 16384
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchFloats];
+
+namespace {
+
+float* g_noalloc_ptr[kMaxDevices];
+bool g_noalloc_ready[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+sga_status noalloc_scratch(int dev, float** out) {
+    if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ready[dev]) {
+        float* p = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch) != cudaSuccess || !p)
+            return SGA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+        g_noalloc_ready[dev] = true;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SGA_OK;
+}
+
+// |S| of a configuration in closed form (no allocation): per frame, L tokens when the frame is
+// kept whole, else the special tokens plus ceil((G_h - phi_r)/s_h) * ceil((G_w - phi_c)/s_w).
+long long kept_count_closed_form(const sga_config& c) {
+    const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
+    long long total = 0;
+    for (int f = 0; f < c.N; ++f) {
+        if ((f == 0 && c.ref_frame_dense) || (c.s_h == 1 && c.s_w == 1)) {
+            total += L;
+            continue;
+        }
+        const int pr = c.phase_shift ? (f / c.s_w) % c.s_h : 0;
+        const int pc = c.phase_shift ? f % c.s_w : 0;
+        const long long rows = pr < c.grid_h ? (c.grid_h - pr + c.s_h - 1) / c.s_h : 0;
+        const long long cols = pc < c.grid_w ? (c.grid_w - pc + c.s_w - 1) / c.s_w : 0;
+        total += c.n_special + rows * cols;
+    }
+    return total;
+}
+
+}  // namespace
+
+extern "C" sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, const void* V, void* K_S,
+                                          void* V_S, float* k_sum, float* v_sum, void* stream) {
+    sga_status st = check_config(cfg);
+    if (st != SGA_OK) return st;
+    if (!K || !V || !K_S || !V_S || !k_sum || !v_sum) return SGA_ERR_INVALID_ARG;
+    if (!aligned16(K) || !aligned16(V) || !aligned16(K_S) || !aligned16(V_S) || !aligned16(k_sum) ||
+        !aligned16(v_sum))
+        return SGA_ERR_ALIGNMENT;
+    const sga_config& c = *cfg;
+    const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
+    const long long T = L * c.N;
+    const long long BH = (long long)c.B * c.H;
+    const long long n_chunks = (T + kCompactRowsPerChunk - 1) / kCompactRowsPerChunk;
+    if (BH > 65535 || n_chunks > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    if (BH * n_chunks * 128 > kNoallocScratchFloats) return SGA_ERR_SCRATCH_LIMIT;
+    int dev;
+    if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
+    float* scratch = nullptr;
+    if ((st = noalloc_scratch(dev, &scratch)) != SGA_OK) return st;
+
+    sga::NoallocArgs a;
+    a.T = T;
+    a.S = kept_count_closed_form(c);
+    a.L = (int)L;
+    a.n_special = c.n_special;
+    a.grid_h = c.grid_h;
+    a.grid_w = c.grid_w;
+    a.s_h = c.s_h;
+    a.s_w = c.s_w;
+    a.phase_shift = c.phase_shift;
+    a.ref_frame_dense = c.ref_frame_dense;
+    a.rows_per_chunk = kCompactRowsPerChunk;
+    a.n_chunks = (int)n_chunks;
+    a.K = K;
+    a.V = V;
+    a.KS = K_S;
+    a.VS = V_S;
+    a.partials = scratch;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    dim3 grid((unsigned)n_chunks, (unsigned)BH);
+    if (c.dtype == SGA_BF16)
+        sga::compact_noalloc_kernel<__nv_bfloat16><<<grid, sga::kCompactThreads, 0, s>>>(a);
+    else
+        sga::compact_noalloc_kernel<float><<<grid, sga::kCompactThreads, 0, s>>>(a);
+    if ((st = launch_status()) != SGA_OK) return st;
+    sga::compact_finalize_kernel<<<(unsigned)BH, 128, 0, s>>>(scratch, (int)n_chunks, k_sum, v_sum);
+    return launch_status();
+}
