@@ -40,6 +40,16 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 64u * (uint3
 __host__ __device__ constexpr uint32_t col_p(int t) { return 384u + 64u * (uint32_t)t; }   // P_t
 constexpr float kRescaleThreshold = 8.0f;      // base-2: rescale when the max grows by > 2^8
 
+// Register split (setmaxnreg): the kernel is launched with LAUNCH_REGS per thread; warpgroup 0
+// (TMA producer, MMA issuer, two idle warps) gives registers back, the two softmax warpgroups
+// take them.  The split must add up to the launch total, otherwise setmaxnreg.inc cannot be
+// satisfied; the host checks the compiled register count before every launch.
+constexpr uint32_t LAUNCH_REGS = 168;
+constexpr uint32_t REGS_CTRL = 72;
+constexpr uint32_t REGS_SOFTMAX = 216;
+static_assert(REGS_CTRL * 128 + REGS_SOFTMAX * 256 == LAUNCH_REGS * NUM_THREADS, "register split");
+static_assert(LAUNCH_REGS * NUM_THREADS <= 65536, "register file");
+
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
@@ -68,27 +78,22 @@ struct TcArgs {
     ExtraArgs ex;           // ex.on only for SGA (segment = batch*head)
 };
 
+// mbarrier addresses (computed, so that no dynamically indexed array lands in local memory)
 struct Bars {
-    uint32_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-    uint32_t s_full[2], p_ready[2], o_done[2], o_free[2], drain;
+    uint32_t base;
+    __device__ __forceinline__ uint32_t q_full() const { return base; }
+    __device__ __forceinline__ uint32_t q_empty() const { return base + 8; }
+    __device__ __forceinline__ uint32_t k_full(int s) const { return base + 16 + 8 * s; }
+    __device__ __forceinline__ uint32_t k_empty(int s) const { return base + 16 + 8 * (STAGES + s); }
+    __device__ __forceinline__ uint32_t v_full(int s) const { return base + 16 + 8 * (2 * STAGES + s); }
+    __device__ __forceinline__ uint32_t v_empty(int s) const { return base + 16 + 8 * (3 * STAGES + s); }
+    __device__ __forceinline__ uint32_t s_full(int t) const { return base + 16 + 8 * (4 * STAGES + t); }
+    __device__ __forceinline__ uint32_t p_ready(int t) const { return base + 16 + 8 * (4 * STAGES + 2 + t); }
+    __device__ __forceinline__ uint32_t o_done(int t) const { return base + 16 + 8 * (4 * STAGES + 4 + t); }
+    __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (4 * STAGES + 6 + t); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (4 * STAGES + 8); }
 };
-
-__device__ __forceinline__ Bars make_bars(uint32_t base) {
-    Bars b;
-    uint32_t a = base;
-    b.q_full = a; a += 8;
-    b.q_empty = a; a += 8;
-    for (int s = 0; s < STAGES; ++s) { b.k_full[s] = a; a += 8; }
-    for (int s = 0; s < STAGES; ++s) { b.k_empty[s] = a; a += 8; }
-    for (int s = 0; s < STAGES; ++s) { b.v_full[s] = a; a += 8; }
-    for (int s = 0; s < STAGES; ++s) { b.v_empty[s] = a; a += 8; }
-    for (int t = 0; t < 2; ++t) { b.s_full[t] = a; a += 8; }
-    for (int t = 0; t < 2; ++t) { b.p_ready[t] = a; a += 8; }
-    for (int t = 0; t < 2; ++t) { b.o_done[t] = a; a += 8; }
-    for (int t = 0; t < 2; ++t) { b.o_free[t] = a; a += 8; }
-    b.drain = a;
-    return b;
-}
+static_assert(16 + 8 * (4 * STAGES + 9) == NUM_BARS * 8, "barrier block size");
 
 // Bounded wait without the abort check: used only to drain work already in flight.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -123,7 +128,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(base);
-    const Bars bars = make_bars(sbase + OFF_BAR);
+    const Bars bars{sbase + OFF_BAR};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + OFF_MISC + 4);
 
@@ -131,21 +136,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(bars.q_full, 1);
-        mbar_init(bars.q_empty, 1);
+        mbar_init(bars.q_full(), 1);
+        mbar_init(bars.q_empty(), 1);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bars.k_full[s], 1);
-            mbar_init(bars.k_empty[s], 1);
-            mbar_init(bars.v_full[s], 1);
-            mbar_init(bars.v_empty[s], 1);
+            mbar_init(bars.k_full(s), 1);
+            mbar_init(bars.k_empty(s), 1);
+            mbar_init(bars.v_full(s), 1);
+            mbar_init(bars.v_empty(s), 1);
         }
         for (int t = 0; t < 2; ++t) {
-            mbar_init(bars.s_full[t], 1);
-            mbar_init(bars.p_ready[t], 128);
-            mbar_init(bars.o_done[t], 1);
-            mbar_init(bars.o_free[t], 128);
+            mbar_init(bars.s_full(t), 1);
+            mbar_init(bars.p_ready(t), 128);
+            mbar_init(bars.o_done(t), 1);
+            mbar_init(bars.o_free(t), 128);
         }
-        mbar_init(bars.drain, 1);
+        mbar_init(bars.drain(), 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
@@ -164,7 +169,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int n_kv = p.n_kv_tiles;
     const int last_valid = p.kv_rows - (n_kv - 1) * BN;     // keys in the last tile (1..128)
 
-    if (warp == 0) {
+    if (warp < 4) {
+      regs_dec<REGS_CTRL>();                            // warpgroup 0: one instruction for all 4 warps
+      if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t kv_it = 0, k_issued = 0, v_issued = 0, q_issued = 0, u_local = 0;
@@ -172,66 +179,63 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
                 const int seg = (int)(u / p.n_pairs);
                 const int row0 = (int)(u % p.n_pairs) * 2 * BM;
-                if (!mbar_wait(bars.q_empty, (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(bars.q_full, 2 * TILE_BYTES);
-                tma_load_3d(sbase + OFF_Q, &tmQ, bars.q_full, 0, row0, seg);
-                tma_load_3d(sbase + OFF_Q + TILE_BYTES, &tmQ, bars.q_full, 0, row0 + BM, seg);
+                if (!mbar_wait(bars.q_empty(), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(bars.q_full(), 2 * TILE_BYTES);
+                tma_load_3d(sbase + OFF_Q, &tmQ, bars.q_full(), 0, row0, seg);
+                tma_load_3d(sbase + OFF_Q + TILE_BYTES, &tmQ, bars.q_full(), 0, row0 + BM, seg);
                 ++q_issued;
                 for (int j = 0; j < n_kv; ++j, ++kv_it) {
                     const int st = kv_it % STAGES;
                     const uint32_t ph = (kv_it / STAGES) & 1;
-                    if (!mbar_wait(bars.k_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(bars.k_full[st], TILE_BYTES);
-                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full[st], 0, j * BN, seg);
+                    if (!mbar_wait(bars.k_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bars.k_full(st), TILE_BYTES);
+                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, j * BN, seg);
                     ++k_issued;
-                    if (!mbar_wait(bars.v_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(bars.v_full[st], TILE_BYTES);
-                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.v_full[st], 0, j * BN, seg);
+                    if (!mbar_wait(bars.v_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bars.v_full(st), TILE_BYTES);
+                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.v_full(st), 0, j * BN, seg);
                     ++v_issued;
                 }
             }
             if (!ok) {
                 // let the copies already issued land before the CTA leaves
                 for (uint32_t i = (k_issued > STAGES ? k_issued - STAGES : 0); i < k_issued; ++i)
-                    drain_wait(bars.k_full[i % STAGES], (i / STAGES) & 1);
+                    drain_wait(bars.k_full(i % STAGES), (i / STAGES) & 1);
                 for (uint32_t i = (v_issued > STAGES ? v_issued - STAGES : 0); i < v_issued; ++i)
-                    drain_wait(bars.v_full[i % STAGES], (i / STAGES) & 1);
-                if (q_issued > 0) drain_wait(bars.q_full, (q_issued - 1) & 1);
+                    drain_wait(bars.v_full(i % STAGES), (i / STAGES) & 1);
+                if (q_issued > 0) drain_wait(bars.q_full(), (q_issued - 1) & 1);
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t kv_it = 0, g_it = 0, u_local = 0;
             bool ok = true;
-            const uint32_t tS[2] = {tmem + col_s(0), tmem + col_s(1)};
-            const uint32_t tO[2] = {tmem + col_o(0), tmem + col_o(1)};
-            const uint32_t tP[2] = {tmem + col_p(0), tmem + col_p(1)};
             auto issue_qk = [&](int t, int st) {
                 const uint32_t qa = sbase + OFF_Q + t * TILE_BYTES;
                 const uint32_t ka = sbase + OFF_K + st * TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
-                    mma_ss(tS[t], smem_desc_sw128(qa + 32 * kk, 16), smem_desc_sw128(ka + 32 * kk, 16),
+                    mma_ss(tmem + col_s(t), smem_desc_sw128(qa + 32 * kk, 16), smem_desc_sw128(ka + 32 * kk, 16),
                            IDESC_QK, kk > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int st, uint32_t acc) {
                 const uint32_t va = sbase + OFF_V + st * TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tO[t], tP[t] + 8 * kk, smem_desc_sw128(va + 2048 * kk, TILE_BYTES),
+                    mma_ts(tmem + col_o(t), tmem + col_p(t) + 8 * kk, smem_desc_sw128(va + 2048 * kk, TILE_BYTES),
                            IDESC_PV, (acc || kk > 0) ? 1u : 0u);
             };
             for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-                if (!mbar_wait(bars.q_full, u_local & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
                 {
                     const int st = kv_it % STAGES;
-                    if (!mbar_wait(bars.k_full[st], (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(bars.k_full(st), (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     issue_qk(0, st);
-                    mma_commit(bars.s_full[0]);
+                    mma_commit(bars.s_full(0));
                     issue_qk(1, st);
-                    mma_commit(bars.s_full[1]);
+                    mma_commit(bars.s_full(1));
                 }
                 for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_it) {
                     const int st = kv_it % STAGES;
@@ -239,32 +243,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     const bool has_next = (j + 1 < n_kv);
                     const int stn = (kv_it + 1) % STAGES;
                     const uint32_t phn = ((kv_it + 1) / STAGES) & 1;
-                    mma_commit(bars.k_empty[st]);               // both QK_j issued
-                    if (has_next && !mbar_wait(bars.k_full[stn], phn, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(bars.v_full[st], ph, abort_flag)) { ok = false; break; }
+                    mma_commit(bars.k_empty(st));               // both QK_j issued
+                    if (has_next && !mbar_wait(bars.k_full(stn), phn, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(bars.v_full(st), ph, abort_flag)) { ok = false; break; }
                     for (int t = 0; t < 2; ++t) {
-                        if (!mbar_wait(bars.p_ready[t], g_it & 1, abort_flag)) { ok = false; break; }
-                        if (j == 0 && !mbar_wait(bars.o_free[t], (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(bars.p_ready(t), g_it & 1, abort_flag)) { ok = false; break; }
+                        if (j == 0 && !mbar_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         issue_pv(t, st, j > 0 ? 1u : 0u);
-                        if (t == 1) mma_commit(bars.v_empty[st]);
+                        if (t == 1) mma_commit(bars.v_empty(st));
                         if (has_next) {
                             issue_qk(t, stn);
-                            mma_commit(bars.s_full[t]);
+                            mma_commit(bars.s_full(t));
                         } else {
-                            mma_commit(bars.o_done[t]);
+                            mma_commit(bars.o_done(t));
                         }
                     }
                     if (!ok) break;
                 }
                 if (!ok) break;
-                mma_commit(bars.q_empty);
+                mma_commit(bars.q_empty());
             }
             // every MMA issued so far completes before TMEM is released
-            mma_commit(bars.drain);
-            drain_wait(bars.drain, 0);
+            mma_commit(bars.drain());
+            drain_wait(bars.drain(), 0);
         }
-    } else if (warp >= 4) {
+      }                                                 // warps 2-3: idle
+    } else {
+        regs_inc<REGS_SOFTMAX>();
         // ------------------------------------------------------------------ softmax + epilogue
         const int t = (warp - 4) >> 2;                  // query tile of this warpgroup
         const int sub = warp & 3;                       // TMEM lanes [32*sub, 32*sub+32)
@@ -294,7 +300,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
 
             for (int j = 0; j < n_kv; ++j, ++g_it) {
-                if (!warp_wait(bars.s_full[t], g_it & 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 float s[128];
                 ld_row128(tS, s);
@@ -304,53 +310,72 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     for (int c = 0; c < 128; ++c)
                         if (c >= last_valid) s[c] = -INFINITY;
                 }
-                float mx = s[0];
+                // row maximum: eight independent 16-column chains, then a small tree
+                float mx8[8];
 #pragma unroll
-                for (int c = 1; c < 127; c += 2) mx = max3f(mx, s[c], s[c + 1]);
-                mx = fmaxf(mx, s[127]);
+                for (int g = 0; g < 8; ++g) {
+                    float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
+#pragma unroll
+                    for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
+                    mx8[g] = fmaxf(a, s[16 * g + 15]);
+                }
+                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 const float m_cand = mx * sl2;
                 const bool need = m_cand > m + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
+                const bool rescale = __any_sync(0xffffffffu, need);
+                float alpha = 1.0f;
+                if (rescale) {
                     const float m_new = fmaxf(m, m_cand);
-                    const float alpha = ex2_approx(m - m_new);   // 0 when m = -inf
+                    alpha = ex2_approx(m - m_new);               // 0 when m = -inf
                     l *= alpha;
-                    if (j > 0) {
-                        uint32_t r[32];
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            tmem_ld32(tO + 32 * c, r);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            tmem_st32(tO + 32 * c, r);
-                        }
-                    }
                     m = m_new;
                 }
-                const float nm = -m;
-                uint32_t pk[64];
-                float lsum0 = 0.f, lsum1 = 0.f;
+                // p = 2^(s * scale_log2 - m), two columns per packed FMA; P goes back to TMEM
+                // as bf16 pairs one 32-column chunk at a time
+                const uint64_t sc2 = f2_pack(sl2, sl2);
+                const uint64_t nm2 = f2_pack(-m, -m);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float p0 = ex2_approx(fmaf(s[2 * c], sl2, nm));
-                    const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, nm));
-                    lsum0 += p0;
-                    lsum1 += p1;
-                    pk[c] = pack_bf16x2(p0, p1);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tP + 16 * c, pk);
                 }
-                l += lsum0 + lsum1;
-                tmem_st16(tP + 0, pk + 0);
-                tmem_st16(tP + 16, pk + 16);
-                tmem_st16(tP + 32, pk + 32);
-                tmem_st16(tP + 48, pk + 48);
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                    l += a0 + a1;
+                }
+                // O *= alpha when the reference max moved (the logits are dead by now); the
+                // PV product of this tile waits for p_ready, so it sees both updates
+                if (rescale && j > 0) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld32(tO + 32 * c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tO + 32 * c, r);
+                    }
+                }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bars.p_ready[t]);
+                mbar_arrive(bars.p_ready(t));
             }
             if (!ok) break;
 
             // epilogue: O from TMEM, extra components, normalisation, store
-            if (!warp_wait(bars.o_done[t], u_local & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(bars.o_done(t), u_local & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             float o[64];
             {
@@ -365,7 +390,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 for (int i = 0; i < 32; ++i) o[32 + i] = __uint_as_float(r[i]);
             }
             tc_fence_before();
-            mbar_arrive(bars.o_free[t]);
+            mbar_arrive(bars.o_free(t));
             if (valid) {
                 if (p.ex.on) extra_values<__nv_bfloat16, 64>(p.ex, seg, row, xr, m, 0, o);
                 const float inv_l = 1.0f / l;
@@ -389,6 +414,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }

@@ -131,6 +131,11 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         {
             std::lock_guard<std::mutex> lk(g_dev_mu);
             if (!di->tc_smem_set) {
+                // the kernel's setmaxnreg split assumes exactly LAUNCH_REGS registers per thread
+                // at launch; any other count would leave setmaxnreg.inc unsatisfiable
+                cudaFuncAttributes fa;
+                if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel) != cudaSuccess) return SGA_ERR_CUDA;
+                if (fa.numRegs != (int)T::LAUNCH_REGS) return SGA_ERR_UNSUPPORTED;
                 if (cudaFuncSetAttribute(T::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES) != cudaSuccess)
                     return SGA_ERR_CUDA;
