@@ -173,83 +173,102 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       regs_dec<REGS_CTRL>();                            // warpgroup 0: one instruction for all 4 warps
       if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            uint32_t kv_it = 0, k_issued = 0, v_issued = 0, q_issued = 0, u_local = 0;
-            bool ok = true;
-            for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-                const int seg = (int)(u / p.n_pairs);
-                const int row0 = (int)(u % p.n_pairs) * 2 * BM;
-                if (!mbar_wait(bars.q_empty(), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+        // The whole warp runs the loop (warp-uniform state); one elected lane issues.
+        uint32_t kv_it = 0, k_issued = 0, v_issued = 0, q_issued = 0, u_local = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
+            const int seg = (int)(u / p.n_pairs);
+            const int row0 = (int)(u % p.n_pairs) * 2 * BM;
+            if (!warp_wait(bars.q_empty(), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (elect_one()) {
                 mbar_arrive_expect_tx(bars.q_full(), 2 * TILE_BYTES);
                 tma_load_3d(sbase + OFF_Q, &tmQ, bars.q_full(), 0, row0, seg);
                 tma_load_3d(sbase + OFF_Q + TILE_BYTES, &tmQ, bars.q_full(), 0, row0 + BM, seg);
-                ++q_issued;
-                for (int j = 0; j < n_kv; ++j, ++kv_it) {
-                    const int st = kv_it % STAGES;
-                    const uint32_t ph = (kv_it / STAGES) & 1;
-                    if (!mbar_wait(bars.k_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+            }
+            __syncwarp();
+            ++q_issued;
+            for (int j = 0; j < n_kv; ++j, ++kv_it) {
+                const int st = kv_it % STAGES;
+                const uint32_t ph = (kv_it / STAGES) & 1;
+                if (!warp_wait(bars.k_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+                if (elect_one()) {
                     mbar_arrive_expect_tx(bars.k_full(st), TILE_BYTES);
                     tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, j * BN, seg);
-                    ++k_issued;
-                    if (!mbar_wait(bars.v_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+                }
+                __syncwarp();
+                ++k_issued;
+                if (!warp_wait(bars.v_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+                if (elect_one()) {
                     mbar_arrive_expect_tx(bars.v_full(st), TILE_BYTES);
                     tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.v_full(st), 0, j * BN, seg);
-                    ++v_issued;
                 }
+                __syncwarp();
+                ++v_issued;
             }
-            if (!ok) {
-                // let the copies already issued land before the CTA leaves
-                for (uint32_t i = (k_issued > STAGES ? k_issued - STAGES : 0); i < k_issued; ++i)
-                    drain_wait(bars.k_full(i % STAGES), (i / STAGES) & 1);
-                for (uint32_t i = (v_issued > STAGES ? v_issued - STAGES : 0); i < v_issued; ++i)
-                    drain_wait(bars.v_full(i % STAGES), (i / STAGES) & 1);
-                if (q_issued > 0) drain_wait(bars.q_full(), (q_issued - 1) & 1);
-            }
+        }
+        if (!ok) {
+            // let the copies already issued land before the CTA leaves
+            for (uint32_t i = (k_issued > STAGES ? k_issued - STAGES : 0); i < k_issued; ++i)
+                drain_wait(bars.k_full(i % STAGES), (i / STAGES) & 1);
+            for (uint32_t i = (v_issued > STAGES ? v_issued - STAGES : 0); i < v_issued; ++i)
+                drain_wait(bars.v_full(i % STAGES), (i / STAGES) & 1);
+            if (q_issued > 0) drain_wait(bars.q_full(), (q_issued - 1) & 1);
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t kv_it = 0, g_it = 0, u_local = 0;
-            bool ok = true;
-            auto issue_qk = [&](int t, int st) {
-                const uint32_t qa = sbase + OFF_Q + t * TILE_BYTES;
-                const uint32_t ka = sbase + OFF_K + st * TILE_BYTES;
+        // The whole warp runs the loop so descriptors and TMEM addresses stay warp-uniform;
+        // one elected lane (always the same, the lowest) issues every MMA and commit.
+        // Descriptors advance by adding (byte offset >> 4) to their start-address field.
+        const uint64_t dQ = smem_desc_sw128(sbase + OFF_Q, 16);
+        const uint64_t dK = smem_desc_sw128(sbase + OFF_K, 16);
+        const uint64_t dV = smem_desc_sw128(sbase + OFF_V, TILE_BYTES);
+        constexpr uint64_t kTileStep = TILE_BYTES >> 4;
+        uint32_t kv_it = 0, g_it = 0, u_local = 0;
+        bool ok = true;
+        auto issue_qk = [&](int t, int st) {
+            const uint64_t dq = dQ + (uint64_t)t * kTileStep;
+            const uint64_t dk = dK + (uint64_t)st * kTileStep;
+            const uint32_t ts = tmem + col_s(t);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    mma_ss(tmem + col_s(t), smem_desc_sw128(qa + 32 * kk, 16), smem_desc_sw128(ka + 32 * kk, 16),
-                           IDESC_QK, kk > 0 ? 1u : 0u);
-            };
-            auto issue_pv = [&](int t, int st, uint32_t acc) {
-                const uint32_t va = sbase + OFF_V + st * TILE_BYTES;
+            for (int kk = 0; kk < HD / 16; ++kk)                  // 16 columns = 32 bytes
+                mma_ss(ts, dq + 2 * kk, dk + 2 * kk, IDESC_QK, kk > 0 ? 1u : 0u);
+        };
+        auto issue_pv = [&](int t, int st, uint32_t acc) {
+            const uint64_t dv = dV + (uint64_t)st * kTileStep;
+            const uint32_t to = tmem + col_o(t), tp = tmem + col_p(t);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + col_o(t), tmem + col_p(t) + 8 * kk, smem_desc_sw128(va + 2048 * kk, TILE_BYTES),
-                           IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-            };
-            for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-                if (!mbar_wait(bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
-                {
-                    const int st = kv_it % STAGES;
-                    if (!mbar_wait(bars.k_full(st), (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+            for (int kk = 0; kk < BN / 16; ++kk)                  // 16 rows = 2048 bytes
+                mma_ts(to, tp + 8 * kk, dv + 128 * kk, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        };
+        for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
+            if (!warp_wait(bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
+            {
+                const int st = kv_it % STAGES;
+                if (!warp_wait(bars.k_full(st), (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
                     issue_qk(0, st);
                     mma_commit(bars.s_full(0));
                     issue_qk(1, st);
                     mma_commit(bars.s_full(1));
                 }
-                for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_it) {
-                    const int st = kv_it % STAGES;
-                    const uint32_t ph = (kv_it / STAGES) & 1;
-                    const bool has_next = (j + 1 < n_kv);
-                    const int stn = (kv_it + 1) % STAGES;
-                    const uint32_t phn = ((kv_it + 1) / STAGES) & 1;
-                    mma_commit(bars.k_empty(st));               // both QK_j issued
-                    if (has_next && !mbar_wait(bars.k_full(stn), phn, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(bars.v_full(st), ph, abort_flag)) { ok = false; break; }
-                    for (int t = 0; t < 2; ++t) {
-                        if (!mbar_wait(bars.p_ready(t), g_it & 1, abort_flag)) { ok = false; break; }
-                        if (j == 0 && !mbar_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
+                __syncwarp();
+            }
+            for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_it) {
+                const int st = kv_it % STAGES;
+                const uint32_t ph = (kv_it / STAGES) & 1;
+                const bool has_next = (j + 1 < n_kv);
+                const int stn = (kv_it + 1) % STAGES;
+                const uint32_t phn = ((kv_it + 1) / STAGES) & 1;
+                if (elect_one()) mma_commit(bars.k_empty(st));      // both QK_j issued
+                __syncwarp();
+                if (has_next && !warp_wait(bars.k_full(stn), phn, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.v_full(st), ph, abort_flag)) { ok = false; break; }
+                for (int t = 0; t < 2; ++t) {
+                    if (!warp_wait(bars.p_ready(t), g_it & 1, abort_flag)) { ok = false; break; }
+                    if (j == 0 && !warp_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    if (elect_one()) {
                         issue_pv(t, st, j > 0 ? 1u : 0u);
                         if (t == 1) mma_commit(bars.v_empty(st));
                         if (has_next) {
@@ -259,15 +278,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                             mma_commit(bars.o_done(t));
                         }
                     }
-                    if (!ok) break;
+                    __syncwarp();
                 }
                 if (!ok) break;
-                mma_commit(bars.q_empty());
             }
-            // every MMA issued so far completes before TMEM is released
-            mma_commit(bars.drain());
-            drain_wait(bars.drain(), 0);
+            if (!ok) break;
+            if (elect_one()) mma_commit(bars.q_empty());
+            __syncwarp();
         }
+        // every MMA issued so far completes before TMEM is released
+        if (elect_one()) mma_commit(bars.drain());
+        __syncwarp();
+        drain_wait(bars.drain(), 0);
       }                                                 // warps 2-3: idle
     } else {
         regs_inc<REGS_SOFTMAX>();
