@@ -49,6 +49,8 @@ def _load():
                                         i32, i32, i32, f64, p, p]
         lib.oracle_attention_rows.restype = None
         lib.oracle_attention_rows.argtypes = [i64, i32, i64, p, p, p, p, i64, f64, p, p]
+        lib.oracle_biased_attention_rows.restype = None
+        lib.oracle_biased_attention_rows.argtypes = [i64, i32, p, p, p, p, i64, f64, p, p]
         lib.oracle_num_threads.restype = i32
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -144,6 +146,20 @@ def attention_rows(Qrows, K, V, rows, *, frame_len=0, scale=0.125):
     lse = np.zeros(n, dtype=np.float64)
     _load().oracle_attention_rows(T, d, int(frame_len), _ptr(Qrows), _ptr(K), _ptr(V),
                                   _ptr(rows), n, float(scale), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def biased_attention_rows(Qrows, K, V, bias, *, scale=0.125):
+    """Size-aware attention softmax(scale * q K^T + bias) V (fp64) of the query vectors
+    ``Qrows`` against all Tk keys; ``bias`` is the per-key natural-log bias [Tk]."""
+    Qrows, K, V = _f32(Qrows), _f32(K), _f32(V)
+    bias = np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
+    n, d = Qrows.shape
+    Tk = K.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    _load().oracle_biased_attention_rows(Tk, d, _ptr(Qrows), _ptr(K), _ptr(V), _ptr(bias), n,
+                                         float(scale), _ptr(out), _ptr(lse))
     return out, lse
 
 

@@ -279,3 +279,41 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Size-aware attention, softmax(scale * q K^T + b) V, for selected query rows of one
+ * (batch, head).  [Regime] Key design 2: a key that stands for g source tokens carries the
+ * logit bias log g (natural log), added after the 1/sqrt(d) scaling; b is that per-key bias
+ * (any real value; -INFINITY removes the key).
+ *   Qrows [n_rows, d]; K, V [Tk, d]; bias [Tk] (fp64); out [n_rows, d]; lse [n_rows] (nullable)
+ * Textbook softmax with max subtraction, in fp64.
+ * ------------------------------------------------------------------------------------ */
+void oracle_biased_attention_rows(int64_t Tk, int d, const float* Qrows, const float* K,
+                                  const float* V, const double* bias, int64_t n_rows,
+                                  double scale, double* out, double* lse)
+{
+    #pragma omp parallel
+    {
+        double* logit = (double*)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t n = 0; n < n_rows; ++n) {
+            const float* q = Qrows + n * d;
+            double* o = out + n * d;
+            double m = -INFINITY;
+            for (int64_t t = 0; t < Tk; ++t) {
+                logit[t] = scale * dot_fd(q, K + t * d, d) + bias[t];
+                if (logit[t] > m) m = logit[t];
+            }
+            double l = 0.0;
+            for (int j = 0; j < d; ++j) o[j] = 0.0;
+            for (int64_t t = 0; t < Tk; ++t) {
+                const double w = exp(logit[t] - m);
+                l += w;
+                for (int j = 0; j < d; ++j) o[j] += w * (double)V[t * d + j];
+            }
+            for (int j = 0; j < d; ++j) o[j] /= l;
+            if (lse) lse[n] = m + log(l);
+        }
+        free(logit);
+    }
+}

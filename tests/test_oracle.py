@@ -316,3 +316,61 @@ def test_appended_column_identity():
         qq = np.append(q[0][i].astype(np.float64), 1.0)[None]
         got = _sdpa(qq, np.array(keys), np.array(vals), scale=SCALE)[0]
         np.testing.assert_allclose(out[i], got, atol=1e-12)
+
+
+# ------------------------------------------------------------------------------ size-aware bias
+# "RegimeVGGT ..." Key design 2: softmax(QK^T/sqrt(d) + log g) V, a key standing for g tokens.
+def test_biased_integer_groups_equal_expanded_keys():
+    # a key with bias ln g is exactly g copies of that key: compare with fp64 SDPA over the
+    # key set in which every key is repeated g times
+    rng = np.random.default_rng(21)
+    q, k, v = _qkv(3, 40, seed=13)
+    q, k, v = q[0][:50], k[0][:37], v[0][:37]
+    g = rng.integers(1, 6, size=37)
+    out, lse = oracle.biased_attention_rows(q, k, v, np.log(g))
+    ke, ve = np.repeat(k, g, axis=0), np.repeat(v, g, axis=0)
+    np.testing.assert_allclose(out, _sdpa(q, ke, ve), atol=1e-12)
+    s = (q.astype(np.float64) @ ke.astype(np.float64).T) * SCALE
+    m = s.max(axis=1)
+    np.testing.assert_allclose(lse, m + np.log(np.exp(s - m[:, None]).sum(axis=1)), atol=1e-12)
+    # planted mistake: a base-2 logarithm instead of ln no longer reproduces the copies
+    bad, _ = oracle.biased_attention_rows(q, k, v, np.log2(g))
+    assert np.abs(bad - out).max() > 1e-3
+
+
+def test_biased_constant_and_removed_keys():
+    q, k, v = _qkv(2, 30, seed=14)
+    q, k, v = q[0], k[0], v[0]
+    out, lse = oracle.biased_attention_rows(q, k, v, np.full(len(k), 2.5))
+    dense, dlse = oracle.attention_rows(q, k, v, np.arange(len(q)))
+    np.testing.assert_allclose(out, _sdpa(q, k, v), atol=1e-12)        # shift invariance
+    np.testing.assert_allclose(lse, dlse + 2.5, atol=1e-12)
+    keep = np.arange(len(k)) % 3 != 1
+    bias = np.where(keep, 0.0, -np.inf)
+    out, _ = oracle.biased_attention_rows(q, k, v, bias)
+    np.testing.assert_allclose(out, _sdpa(q, k[keep], v[keep]), atol=1e-12)
+
+
+def test_sga_mean_term_is_a_size_aware_key():
+    # the SGA mean term is one merged key: for every query, SGA equals size-aware attention
+    # over S, the query's own key when it was dropped, and the (leave-one-out) mean key with
+    # bias ln(count)
+    N, gh, gw, nsp = 4, 8, 8, 5
+    p = oracle.plan(N, gh, gw, nsp, 2, 2, True, True)
+    q, k, v = _qkv(N, p.L, seed=15)
+    q, k, v = q[0], k[0], v[0]
+    out, _ = oracle.sga_full(p, q, k, v)
+    ks, vs, c = oracle.dropped_sums(p, k, v)
+    for i in range(p.T):
+        keys = [k[t].astype(np.float64) for t in p.kv_index]
+        vals = [v[t].astype(np.float64) for t in p.kv_index]
+        bias = [0.0] * p.S
+        ci = c
+        kb, vb = ks.copy(), vs.copy()
+        if not p.kept[i]:
+            keys.append(k[i].astype(np.float64)); vals.append(v[i].astype(np.float64)); bias.append(0.0)
+            ci = c - 1
+            kb -= k[i]; vb -= v[i]
+        keys.append(kb / ci); vals.append(vb / ci); bias.append(math.log(ci))
+        got, _ = oracle.biased_attention_rows(q[i:i + 1], np.array(keys), np.array(vals), np.array(bias))
+        np.testing.assert_allclose(got[0], out[i], atol=1e-6)   # keys pass through fp32 here
