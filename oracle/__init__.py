@@ -49,6 +49,8 @@ def _load():
                                         i32, i32, i32, f64, p, p]
         lib.oracle_attention_rows.restype = None
         lib.oracle_attention_rows.argtypes = [i64, i32, i64, p, p, p, p, i64, f64, p, p]
+        lib.oracle_plan_general.restype = i64
+        lib.oracle_plan_general.argtypes = [i32] * 10 + [p, i64, p, p, p]
         lib.oracle_biased_attention_rows.restype = None
         lib.oracle_biased_attention_rows.argtypes = [i64, i32, p, p, p, p, i64, f64, p, p]
         lib.oracle_num_threads.restype = i32
@@ -94,6 +96,24 @@ def plan(N: int, grid_h: int, grid_w: int, n_special: int, s_h: int, s_w: int,
                             int(ref_frame_dense), _ptr(kept), _ptr(kv), _ptr(off))
     if n < 0:
         raise ValueError("oracle_plan: bad argument")
+    return Plan(T=T, L=L, kept=kept, kv_index=kv[:n].copy(), frame_off=off)
+
+
+def plan_general(N: int, grid_h: int, grid_w: int, n_special: int, sigma_h, sigma_w,
+                 phase_shift: bool, ref_frame_dense: bool, protected=()) -> Plan:
+    """Generalised kept set: per-axis rational window sizes ``sigma_h``, ``sigma_w`` given as
+    (num, den) pairs, and a list of protected token indices kept in full."""
+    L = n_special + grid_h * grid_w
+    T = N * L
+    kept = np.zeros(T, dtype=np.uint8)
+    kv = np.zeros(T, dtype=np.int32)
+    off = np.zeros(N + 1, dtype=np.int32)
+    prot = np.ascontiguousarray(np.asarray(list(protected), dtype=np.int32).reshape(-1))
+    n = _load().oracle_plan_general(N, grid_h, grid_w, n_special, int(sigma_h[0]), int(sigma_h[1]),
+                                    int(sigma_w[0]), int(sigma_w[1]), int(phase_shift), int(ref_frame_dense),
+                                    _ptr(prot) if len(prot) else None, len(prot), _ptr(kept), _ptr(kv), _ptr(off))
+    if n < 0:
+        raise ValueError("oracle_plan_general: bad argument")
     return Plan(T=T, L=L, kept=kept, kv_index=kv[:n].copy(), frame_off=off)
 
 

@@ -317,3 +317,74 @@ void oracle_biased_attention_rows(int64_t Tk, int d, const float* Qrows, const f
         free(logit);
     }
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Generalised kept set.  [Regime] Key design 3: per-axis sampling factors that need not be
+ * integers (1.5 / 1.3 / 1.7, keeping about 1/sigma_b^2 of the patches), the phase shift,
+ * frame 0 and the camera/register tokens at full density, and an externally chosen list of
+ * protected (salient) tokens kept in full as well.
+ *
+ * A window size is the rational sigma = num/den >= 1 (exact integer arithmetic).  Along one
+ * axis of length G, window i covers [i*sigma, (i+1)*sigma) and keeps its first position
+ * ceil(i*sigma); with the phase shift the positions move by phi, phi + ceil(i*sigma) < G.
+ * The phase uses the page's formula with the integer tile t = ceil(sigma) per axis:
+ * phi_r = (f div t_w) mod t_h, phi_c = f mod t_w (for integer sigma this is the plain grid).
+ * protected_tokens: n_protected token indices in [0, N*L), any order, repeats allowed.
+ * Outputs as oracle_plan.  Returns |S|, or -1 on a bad argument.
+ * ------------------------------------------------------------------------------------ */
+static int on_axis(int64_t x, int64_t phi, int64_t num, int64_t den)
+{
+    /* is x = phi + ceil(i * num / den) for some integer i >= 0 ? */
+    if (x < phi) return 0;
+    const int64_t y = x - phi;
+    if (y == 0) return 1;
+    /* ceil(i*sigma) >= y  <=>  i*sigma > y - 1: the smallest such i is floor((y-1)/sigma) + 1;
+       y is a window start iff that window starts exactly at y */
+    const int64_t i = ((y - 1) * den) / num + 1;
+    return (i * num + den - 1) / den == y;
+}
+
+int64_t oracle_plan_general(int N, int grid_h, int grid_w, int n_special,
+                            int sh_num, int sh_den, int sw_num, int sw_den,
+                            int phase_shift, int ref_frame_dense,
+                            const int32_t* protected_tokens, int64_t n_protected,
+                            uint8_t* kept, int32_t* kv_index, int32_t* frame_off)
+{
+    if (N <= 0 || grid_h <= 0 || grid_w <= 0 || n_special < 0 || sh_den <= 0 || sw_den <= 0 ||
+        sh_num < sh_den || sw_num < sw_den || n_protected < 0)
+        return -1;
+    const int64_t L = (int64_t)n_special + (int64_t)grid_h * grid_w;
+    const int64_t T = (int64_t)N * L;
+    const int64_t th = (sh_num + sh_den - 1) / sh_den, tw = (sw_num + sw_den - 1) / sw_den;
+    for (int64_t t = 0; t < T; ++t) kept[t] = 0;
+    for (int64_t k = 0; k < n_protected; ++k) {
+        if (protected_tokens[k] < 0 || protected_tokens[k] >= T) return -1;
+        kept[protected_tokens[k]] = 1;                 /* protected salient token */
+    }
+    int64_t n_kept = 0;
+    for (int f = 0; f < N; ++f) {
+        frame_off[f] = (int32_t)n_kept;
+        int64_t phi_r = 0, phi_c = 0;
+        if (phase_shift) {
+            phi_r = (f / tw) % th;
+            phi_c = f % tw;
+        }
+        for (int64_t p = 0; p < L; ++p) {
+            const int64_t t = (int64_t)f * L + p;
+            if (f == 0 && ref_frame_dense) {
+                kept[t] = 1;                           /* reference frame uncompressed */
+            } else if (p < n_special) {
+                kept[t] = 1;                           /* camera / register tokens */
+            } else {
+                const int64_t r = (p - n_special) / grid_w;
+                const int64_t c = (p - n_special) % grid_w;
+                if (on_axis(r, phi_r, sh_num, sh_den) && on_axis(c, phi_c, sw_num, sw_den))
+                    kept[t] = 1;                       /* first position of its window */
+            }
+            if (kept[t])
+                kv_index[n_kept++] = (int32_t)t;
+        }
+    }
+    frame_off[N] = (int32_t)n_kept;
+    return n_kept;
+}

@@ -374,3 +374,68 @@ def test_sga_mean_term_is_a_size_aware_key():
         keys.append(kb / ci); vals.append(vb / ci); bias.append(math.log(ci))
         got, _ = oracle.biased_attention_rows(q[i:i + 1], np.array(keys), np.array(vals), np.array(bias))
         np.testing.assert_allclose(got[0], out[i], atol=1e-6)   # keys pass through fp32 here
+
+
+# ------------------------------------------------------------------------------ generalised plan
+# "RegimeVGGT ..." Key design 3: fractional per-axis sampling factors, phase shift, frame-0 and
+# camera/register protection, protected salient tokens.
+from fractions import Fraction
+
+
+def _bf_general_kept(N, gh, gw, nsp, sh, sw, phase, ref, protected=()):
+    """Kept set by enumerating the windows with exact fractions (independent of the oracle)."""
+    L = nsp + gh * gw
+    sh, sw = Fraction(*sh), Fraction(*sw)
+    th, tw = math.ceil(sh), math.ceil(sw)
+    kept = set(int(x) for x in protected)
+    for f in range(N):
+        if f == 0 and ref:
+            kept.update(range(L))
+            continue
+        kept.update(f * L + p for p in range(nsp))
+        pr, pc = ((f // tw) % th, f % tw) if phase else (0, 0)
+        rows, i = [], 0
+        while pr + math.ceil(i * sh) < gh:
+            rows.append(pr + math.ceil(i * sh)); i += 1
+        cols, i = [], 0
+        while pc + math.ceil(i * sw) < gw:
+            cols.append(pc + math.ceil(i * sw)); i += 1
+        kept.update(f * L + nsp + r * gw + c for r in rows for c in cols)
+    return kept
+
+
+@pytest.mark.parametrize("sh,sw", [((3, 2), (3, 2)), ((13, 10), (13, 10)), ((17, 10), (17, 10)),
+                                   ((3, 2), (17, 10)), ((2, 1), (3, 1)), ((7, 3), (1, 1))])
+@pytest.mark.parametrize("phase", [False, True])
+@pytest.mark.parametrize("ref", [False, True])
+def test_general_plan_matches_window_enumeration(sh, sw, phase, ref):
+    N, gh, gw, nsp = 7, 11, 13, 5
+    rng = np.random.default_rng(hash((sh, sw, phase, ref)) % 2**32)
+    prot = rng.integers(0, N * (nsp + gh * gw), size=9)
+    p = oracle.plan_general(N, gh, gw, nsp, sh, sw, phase, ref, protected=prot)
+    want = _bf_general_kept(N, gh, gw, nsp, sh, sw, phase, ref, prot)
+    assert set(p.kv_index.tolist()) == want
+    assert np.all(np.diff(p.kv_index) > 0)
+    assert np.array_equal(np.nonzero(p.kept)[0], p.kv_index)
+    L = nsp + gh * gw
+    for f in range(N):
+        assert p.frame_off[f + 1] - p.frame_off[f] == sum(1 for t in want if f * L <= t < (f + 1) * L)
+
+
+@pytest.mark.parametrize("phase", [False, True])
+def test_general_plan_integer_windows_equal_grid_plan(phase):
+    for sigma, sh, sw in _rows("sigma_map.txt"):
+        a = oracle.plan_general(9, 37, 28, 5, (sh, 1), (sw, 1), phase, True)
+        b = oracle.plan(9, 37, 28, 5, sh, sw, phase, True)
+        assert np.array_equal(a.kv_index, b.kv_index) and np.array_equal(a.frame_off, b.frame_off)
+
+
+def test_general_plan_per_axis_closed_form_and_page_retention():
+    gh = gw = 37
+    for num, den, pct in _rows("fractional_retention.txt"):
+        s = Fraction(num, den)
+        p = oracle.plan_general(2, gh, gw, 0, (num, den), (num, den), False, True)
+        per_axis = (gh - 1) * den // num + 1          # #{i : ceil(i * sigma) <= G - 1}
+        assert p.S - gh * gw == per_axis * per_axis
+        # the share of kept patches is close to the page's stated retention
+        assert abs(100.0 * per_axis ** 2 / (gh * gw) - pct) < 3.0, (num, den)
