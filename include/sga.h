@@ -95,6 +95,36 @@ typedef struct sga_plan_s* sga_plan_t;   /* opaque */
 sga_status sga_plan_host(const sga_config* cfg, int32_t* kv_index, int32_t* frame_off,
                          int32_t* slot, int64_t* S_out);
 
+/* Generalised kept-set description ("RegimeVGGT ..." Key design 3): per-axis window sizes that
+ * need not be integers, given exactly as rationals sigma = num/den >= 1 (1.5 = 3/2, 1.3 = 13/10,
+ * 1.7 = 17/10).  Along an axis of length G, window i covers [i*sigma, (i+1)*sigma) and keeps
+ * its first position ceil(i*sigma), about G/sigma positions.  With phase_shift the positions
+ * move by phi_r = (f div t_w) mod t_h, phi_c = f mod t_w, t = ceil(sigma) per axis (the page's
+ * formula with an integer tile).  Integer sigma gives exactly the AVGGT grid of
+ * sga_plan_host / sga_plan_create. */
+typedef struct {
+    int N, grid_h, grid_w, n_special;
+    int sh_num, sh_den;      /* row window sigma_h = sh_num / sh_den */
+    int sw_num, sw_den;      /* column window sigma_w = sw_num / sw_den */
+    int phase_shift, ref_frame_dense;
+} sga_grid_spec;
+
+/* Host-only builder of the generalised kept set: frame 0 (when dense), the camera/register
+ * tokens, the window starts above, and every token of protected_tokens (host int32
+ * [n_protected], any order, repeats allowed -- e.g. the salient tokens RegimeVGGT protects).
+ * Outputs as sga_plan_host (kv_index capacity N*L).  SGA_ERR_INVALID_ARG for a protected index
+ * outside [0, N*L). */
+sga_status sga_plan_host_general(const sga_grid_spec* spec, const int32_t* protected_tokens, int64_t n_protected,
+                                 int32_t* kv_index, int32_t* frame_off, int32_t* slot, int64_t* S_out);
+
+/* A plan from an arbitrary kept set: `kv_index` (host int32 [S], strictly ascending tokens in
+ * [0, T), T = N*L from cfg) replaces the grid rule; cfg's s_h, s_w and phase_shift are not used,
+ * everything else (B, H, frame geometry, diag, mean, dtype, kernel) is.  The same compaction and
+ * attention run on it; the dropped set D is the complement of kv_index.  Allocates like
+ * sga_plan_create.  SGA_ERR_INVALID_ARG if the list is not strictly ascending or out of range. */
+sga_status sga_plan_create_from_index(const sga_config* cfg, const int32_t* kv_index, int64_t S, int device,
+                                      sga_plan_t* out);
+
 /* Build the kept set S for `cfg` on the host (integer arithmetic, O(T)) and upload it to
  * `device`: the token->slot map (int32 [T], -1 = dropped), the kept-token list (int32 [|S|],
  * ascending) and per-frame offsets (int32 [N+1]).  The plan owns these device buffers and a
@@ -146,6 +176,18 @@ sga_status sga_dense_forward(int B, int H, int64_t T, int head_dim, int dtype, i
 sga_status sga_frame_forward(int B, int H, int N, int L, int head_dim, int dtype, int kernel,
                              const void* Q, const void* K, const void* V, void* O, float* lse,
                              float scale, void* stream);
+
+/* Size-aware attention ("RegimeVGGT ..." Key design 2): for every query row of every (b, h),
+ *   O_i = softmax over j of ( scale * q_i . k_j + bias_j ) applied to v_j,
+ * where bias_j is the natural-log bias of key j -- ln g_j for a key that stands for g_j source
+ * tokens (g_j = 1: bias 0), or any real value.  Q: [B, H, Tq, 64]; K, V: [B, H, Tk, 64];
+ * bias: fp32 [B, H, Tk] (4-byte aligned device pointer); O: [B, H, Tq, 64]; lse: optional fp32
+ * [B, H, Tq].  The tensor-core kernel adds the bias inside the QK^T product (an extra K step
+ * holding bias/scale in two bf16 parts, about 2^-16 relative precision); the CUDA-core kernel
+ * adds it in fp32.  Same conventions and errors as sga_dense_forward. */
+sga_status sga_bias_forward(int B, int H, int64_t Tq, int64_t Tk, int head_dim, int dtype, int kernel,
+                            const void* Q, const void* K, const void* V, const float* bias, void* O,
+                            float* lse, float scale, void* stream);
 
 /* Compaction that allocates nothing, for callers that cannot call cudaMalloc.  The pages have
  * no counterpart: this entry point exists for integration only.

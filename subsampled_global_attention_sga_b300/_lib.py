@@ -19,7 +19,8 @@ SGA_KERNEL_AUTO, SGA_KERNEL_TC, SGA_KERNEL_SIMT = 0, 1, 2
 EXPORTS = (
     "sga_plan_host", "sga_plan_create", "sga_plan_info", "sga_plan_copy_indices", "sga_plan_destroy",
     "sga_compact", "sga_forward", "sga_dense_forward", "sga_frame_forward", "sga_device_status",
-    "sga_status_string", "sga_build_info", "sga_compact_noalloc",
+    "sga_status_string", "sga_build_info", "sga_compact_noalloc", "sga_bias_forward",
+    "sga_plan_host_general", "sga_plan_create_from_index",
 )
 
 
@@ -27,6 +28,12 @@ class SgaConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "B", "H", "N", "grid_h", "grid_w", "n_special", "head_dim", "s_h", "s_w",
         "phase_shift", "ref_frame_dense", "diag", "mean", "mean_mode", "dtype", "kernel")]
+
+
+class SgaGridSpec(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "N", "grid_h", "grid_w", "n_special", "sh_num", "sh_den", "sw_num", "sw_den",
+        "phase_shift", "ref_frame_dense")]
 
 
 class SgaError(RuntimeError):
@@ -65,6 +72,9 @@ def lib():
             "sga_dense_forward": (i32, [i32, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp]),
             "sga_frame_forward": (i32, [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp]),
             "sga_compact_noalloc": (i32, [cfgp, vp, vp, vp, vp, vp, vp, vp]),
+            "sga_bias_forward": (i32, [i32, i32, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, f32, vp]),
+            "sga_plan_host_general": (i32, [ctypes.POINTER(SgaGridSpec), vp, i64, vp, vp, vp, ctypes.POINTER(i64)]),
+            "sga_plan_create_from_index": (i32, [cfgp, vp, i64, i32, ctypes.POINTER(vp)]),
             "sga_device_status": (i32, [vp]),
             "sga_status_string": (ctypes.c_char_p, [i32]),
             "sga_build_info": (ctypes.c_char_p, []),

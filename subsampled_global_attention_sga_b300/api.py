@@ -15,7 +15,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import SgaConfig, check, lib
+from ._lib import SgaConfig, SgaGridSpec, check, lib
 
 # sigma -> (s_h, s_w): "AVGGT: Rethinking Global Attention for Accelerating VGGT", Key design 2
 # (sigma = s_h * s_w; 2 -> (1,2), 4 -> (2,2), 6 -> (2,3), 9 -> (3,3)); sigma = 1 keeps every key.
@@ -95,6 +95,29 @@ def plan_host(cfg: SGAConfig):
     return kv[: n.value].copy(), off, slot
 
 
+def plan_host_general(N: int, grid_h: int = 37, grid_w: int = 37, n_special: int = 5, *,
+                      sigma_h=(2, 1), sigma_w=(2, 1), phase_shift: bool = False,
+                      ref_frame_dense: bool = True, protected=()):
+    """Generalised kept set ("RegimeVGGT ..." Key design 3) computed by the library's host
+    builder: per-axis rational window sizes (num, den), e.g. (3, 2) for 1.5, plus protected
+    tokens kept in full.  Returns (kv_index, frame_off, slot)."""
+    g = SgaGridSpec()
+    g.N, g.grid_h, g.grid_w, g.n_special = N, grid_h, grid_w, n_special
+    g.sh_num, g.sh_den = int(sigma_h[0]), int(sigma_h[1])
+    g.sw_num, g.sw_den = int(sigma_w[0]), int(sigma_w[1])
+    g.phase_shift, g.ref_frame_dense = int(phase_shift), int(ref_frame_dense)
+    T = N * (n_special + grid_h * grid_w)
+    prot = np.ascontiguousarray(np.asarray(list(protected), dtype=np.int32).reshape(-1))
+    kv = np.zeros(T, dtype=np.int32)
+    off = np.zeros(N + 1, dtype=np.int32)
+    slot = np.zeros(T, dtype=np.int32)
+    n = ctypes.c_int64(0)
+    check("sga_plan_host_general",
+          lib().sga_plan_host_general(ctypes.byref(g), prot.ctypes.data if len(prot) else None, len(prot),
+                                      kv.ctypes.data, off.ctypes.data, slot.ctypes.data, ctypes.byref(n)))
+    return kv[: n.value].copy(), off, slot
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
@@ -117,7 +140,9 @@ def _check_tensor(name, t, shape, dtype, device):
 class Plan:
     """Device-resident kept set of one layer configuration (owns the library's plan)."""
 
-    def __init__(self, cfg: SGAConfig, device=None):
+    def __init__(self, cfg: SGAConfig, device=None, kv_index=None):
+        """The grid kept set of ``cfg``, or -- with ``kv_index`` (strictly ascending token
+        indices) -- an arbitrary kept set over cfg's frames (``sga_plan_create_from_index``)."""
         if device is None:
             device = torch.device("cuda", torch.cuda.current_device())
         self.device = torch.device(device)
@@ -125,7 +150,14 @@ class Plan:
         self._h = ctypes.c_void_p()
         c = cfg.to_c()
         with torch.cuda.device(self.device):
-            check("sga_plan_create", lib().sga_plan_create(ctypes.byref(c), self.device.index, ctypes.byref(self._h)))
+            if kv_index is None:
+                check("sga_plan_create", lib().sga_plan_create(ctypes.byref(c), self.device.index,
+                                                               ctypes.byref(self._h)))
+            else:
+                kv = np.ascontiguousarray(np.asarray(kv_index, dtype=np.int32).reshape(-1))
+                check("sga_plan_create_from_index",
+                      lib().sga_plan_create_from_index(ctypes.byref(c), kv.ctypes.data if len(kv) else None,
+                                                       len(kv), self.device.index, ctypes.byref(self._h)))
         T, S, D = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
         check("sga_plan_info", lib().sga_plan_info(self._h, ctypes.byref(T), ctypes.byref(S), ctypes.byref(D)))
         self.T, self.S, self.dropped = T.value, S.value, D.value
@@ -243,6 +275,30 @@ def dense_forward(Q, K, V, *, dtype="bf16", kernel="auto", out=None, lse=None, s
 def frame_forward(Q, K, V, N, L, *, dtype="bf16", kernel="auto", out=None, lse=None, scale=None):
     """Frame-local attention ("AVGGT ..." Key design 1, Global-to-Frame)."""
     return _plain("frame", Q, K, V, N, L, dtype, kernel, out, lse, scale)
+
+
+def bias_forward(Q, K, V, bias, *, dtype="bf16", kernel="auto", out=None, lse=None, scale=None):
+    """Size-aware attention softmax(scale * Q K^T + bias) V ("RegimeVGGT ..." Key design 2):
+    Q [B, H, Tq, 64], K/V [B, H, Tk, 64], bias fp32 [B, H, Tk] (ln g for a key standing for g
+    tokens)."""
+    B, H, Tq, d = Q.shape
+    Tk = K.shape[2]
+    tdt = _DTYPES[dtype][1]
+    dev = Q.device
+    _check_tensor("Q", Q, (B, H, Tq, d), tdt, dev)
+    _check_tensor("K", K, (B, H, Tk, d), tdt, dev)
+    _check_tensor("V", V, (B, H, Tk, d), tdt, dev)
+    _check_tensor("bias", bias, (B, H, Tk), torch.float32, dev)
+    out = torch.empty_like(Q) if out is None else out
+    _check_tensor("out", out, (B, H, Tq, d), tdt, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, (B, H, Tq), torch.float32, dev)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        check("sga_bias_forward", lib().sga_bias_forward(B, H, Tq, Tk, d, _DTYPES[dtype][0], _KERNELS[kernel],
+                                                         _ptr(Q), _ptr(K), _ptr(V), _ptr(bias), _ptr(out),
+                                                         _ptr(lse), ctypes.c_float(scale), _stream(dev)))
+    return out
 
 
 def device_status(device=None) -> int:

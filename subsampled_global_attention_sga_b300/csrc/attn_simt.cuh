@@ -23,6 +23,7 @@ struct SimtArgs {
     float* lse;               // [n_seg, seg_rows] or null
     float scale_log2;         // scale * log2(e)
     ExtraArgs ex;             // ex.on only for SGA (segment = batch*head)
+    const float* bias;        // [n_seg, kv_rows] natural-log per-key bias, or null
 };
 
 constexpr int kSimtRows = 128;   // query rows (threads) per block
@@ -33,6 +34,7 @@ template <typename T>
 __global__ void __launch_bounds__(kSimtRows) attn_simt_kernel(SimtArgs p) {
     __shared__ float Ks[kSimtKeys][64];
     __shared__ float Vs[kSimtKeys][64];
+    __shared__ float Bs[kSimtKeys];             // per-key bias in base 2 (0 without a bias)
 
     const int seg = blockIdx.y;
     const long long row = (long long)blockIdx.x * kSimtRows + threadIdx.x;
@@ -79,6 +81,10 @@ __global__ void __launch_bounds__(kSimtRows) attn_simt_kernel(SimtArgs p) {
             Ks[r][c] = kv;
             Vs[r][c] = vv;
         }
+        if (threadIdx.x < kSimtKeys) {
+            const int r = threadIdx.x;
+            Bs[r] = (p.bias && r < nk) ? p.bias[(long long)seg * p.kv_rows + k0 + r] * 1.4426950408889634f : 0.f;
+        }
         __syncthreads();
         for (int c0 = 0; c0 < nk; c0 += kSimtChunk) {
             float s[kSimtChunk];
@@ -88,7 +94,7 @@ __global__ void __launch_bounds__(kSimtRows) attn_simt_kernel(SimtArgs p) {
                 float acc = 0.f;
 #pragma unroll
                 for (int d = 0; d < 64; ++d) acc = fmaf(q[d], Ks[c0 + jj][d], acc);
-                s[jj] = (c0 + jj < nk) ? acc * p.scale_log2 : -INFINITY;
+                s[jj] = (c0 + jj < nk) ? fmaf(acc, p.scale_log2, Bs[c0 + jj]) : -INFINITY;
                 mx = fmaxf(mx, s[jj]);
             }
             const float m_new = fmaxf(m, mx);

@@ -11,12 +11,17 @@
 // Work unit: two 128-row query tiles of one segment (a (batch, head) pair, or one frame of it)
 // against all key tiles of that segment.  Roles (384 threads):
 //   warp 0      TMA producer: the two Q tiles, then a STAGES-deep ring of K and V tiles
-//   warp 1      TMEM owner and MMA issuer (one thread):
+//   warp 1      TMEM owner and MMA issuer (one elected lane issues):
 //                 S_t = Q_t K_j^T  (M=128, N=128, K=64; A, B from shared memory)
 //                 O_t += P_t V_j   (M=128, N=64,  K=128; P from TMEM, V from shared memory)
 //   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
 //   warps 8-11  softmax + epilogue of query tile 1
 // TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384) P_0 [384,448) P_1 [448,512).
+// With a per-key bias (size-aware attention, "RegimeVGGT ..." Key design 2: a key standing
+// for g tokens carries the logit bias ln g), QK^T gets a fifth K = 16 step: the Q side is a
+// constant block with ones in columns 0-1, the K side holds bias/scale split into a bf16 high
+// and low part in columns 0-1 (written by the producer warp from the fp32 bias), so the
+// accumulator already contains q.k + bias/scale and the softmax is unchanged.
 // The two tiles ping-pong: while one tile's rows are exponentiated the tensor core runs the
 // other tile's products.  A running max is only moved (and O rescaled in TMEM) when a row's
 // maximum grows by more than 2^8; the final normalisation uses the same reference, so the
@@ -54,7 +59,13 @@ static_assert(LAUNCH_REGS * NUM_THREADS <= 65536, "register file");
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
-constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+// bias blocks: 128 rows x 16 bf16 columns in the no-swizzle K-major core-matrix layout
+// (8 rows x 16 bytes per core matrix; LBO = 128 B between the two K halves, SBO = 256 B
+// between groups of 8 rows)
+constexpr int EXT_BYTES = 128 * 16 * 2;
+constexpr int OFF_QEXT = OFF_V + STAGES * TILE_BYTES;
+constexpr int OFF_KEXT = OFF_QEXT + EXT_BYTES;
+constexpr int OFF_BAR = OFF_KEXT + STAGES * EXT_BYTES;
 // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
 //           p_ready[2], o_done[2], o_free[2], drain
 constexpr int NUM_BARS = 2 + 4 * STAGES + 8 + 1;
@@ -76,7 +87,14 @@ struct TcArgs {
     __nv_bfloat16* O;       // [n_seg, seg_rows, 64]
     float* lse;             // [n_seg, seg_rows] or null
     ExtraArgs ex;           // ex.on only for SGA (segment = batch*head)
+    const float* bias;      // [n_seg, kv_rows] natural-log per-key bias (size-aware variant)
+    float inv_scale;        // 1 / scale
 };
+
+// byte offset of element (row r, column c) in a bias block
+__host__ __device__ constexpr uint32_t ext_off(int r, int c) {
+    return (uint32_t)((r >> 3) * 256 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
 
 // mbarrier addresses (computed, so that no dynamically indexed array lands in local memory)
 struct Bars {
@@ -122,6 +140,7 @@ __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&s)[128]) {
     }
 }
 
+template <bool kBias>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcArgs p) {
@@ -157,6 +176,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
+    if (kBias && warp < 4) {
+        // constant ones block for Q (columns 0-1 = 1.0) and zeroed bias blocks; the producer
+        // rewrites only columns 0-1 of the bias blocks
+        uint32_t* qe = reinterpret_cast<uint32_t*>(base + OFF_QEXT);
+        for (int i = threadIdx.x; i < (EXT_BYTES + STAGES * EXT_BYTES) / 4; i += 128) qe[i] = 0u;
+        __syncwarp();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int r = threadIdx.x; r < 128; r += 128)
+            *reinterpret_cast<uint32_t*>(base + OFF_QEXT + ext_off(r, 0)) = 0x3F803F80u;   // bf16 1.0, 1.0
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
@@ -191,6 +221,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const int st = kv_it % STAGES;
                 const uint32_t ph = (kv_it / STAGES) & 1;
                 if (!warp_wait(bars.k_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+                if (kBias) {
+                    // columns 0-1 of key row r: bias/scale as bf16 high + low parts
+                    uint8_t* blk = base + OFF_KEXT + st * EXT_BYTES;
+                    const float* brow = p.bias + (long long)seg * p.kv_rows + (long long)j * BN;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = lane * 4 + i;
+                        const float b = (j * BN + r < p.kv_rows) ? __ldg(brow + r) * p.inv_scale : 0.f;
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(b);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(b - __bfloat162float(hi));
+                        *reinterpret_cast<uint32_t*>(blk + ext_off(r, 0)) =
+                            (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                }
                 if (elect_one()) {
                     mbar_arrive_expect_tx(bars.k_full(st), TILE_BYTES);
                     tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, j * BN, seg);
@@ -222,7 +268,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const uint64_t dQ = smem_desc_sw128(sbase + OFF_Q, 16);
         const uint64_t dK = smem_desc_sw128(sbase + OFF_K, 16);
         const uint64_t dV = smem_desc_sw128(sbase + OFF_V, TILE_BYTES);
+        const uint64_t dQe = smem_desc_noswz(sbase + OFF_QEXT, 128, 256);
+        const uint64_t dKe = smem_desc_noswz(sbase + OFF_KEXT, 128, 256);
         constexpr uint64_t kTileStep = TILE_BYTES >> 4;
+        constexpr uint64_t kExtStep = EXT_BYTES >> 4;
         uint32_t kv_it = 0, g_it = 0, u_local = 0;
         bool ok = true;
         auto issue_qk = [&](int t, int st) {
@@ -232,6 +281,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)                  // 16 columns = 32 bytes
                 mma_ss(ts, dq + 2 * kk, dk + 2 * kk, IDESC_QK, kk > 0 ? 1u : 0u);
+            if (kBias) mma_ss(ts, dQe, dKe + (uint64_t)st * kExtStep, IDESC_QK, 1u);
         };
         auto issue_pv = [&](int t, int st, uint32_t acc) {
             const uint64_t dv = dV + (uint64_t)st * kTileStep;

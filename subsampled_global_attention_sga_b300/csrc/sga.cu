@@ -23,7 +23,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool init = false;
     int sm_count = 0;
-    bool tc_smem_set = false;
+    bool tc_ready[2] = {false, false};   // attn_tc_kernel<false>, <true> checked and configured
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -113,7 +113,26 @@ struct AttnProblem {
     float* lse;
     float scale;
     sga::ExtraArgs ex;
+    const float* bias;      // per-key natural-log bias [n_seg, kv_rows], or null
 };
+
+// The tensor-core kernel instantiation for a bias setting, checked once per device: its
+// setmaxnreg split assumes exactly LAUNCH_REGS registers per thread at launch (any other count
+// would leave setmaxnreg.inc unsatisfiable), and it needs the large dynamic shared memory.
+template <bool kBias>
+sga_status prepare_tc(DeviceInfo* di) {
+    namespace T = sga::tc;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (di->tc_ready[kBias]) return SGA_OK;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias>) != cudaSuccess) return SGA_ERR_CUDA;
+    if (fa.numRegs != (int)T::LAUNCH_REGS) return SGA_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             T::SMEM_BYTES) != cudaSuccess)
+        return SGA_ERR_CUDA;
+    di->tc_ready[kBias] = true;
+    return SGA_OK;
+}
 
 sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
     int dev;
@@ -128,20 +147,7 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         if (pb.dtype != SGA_BF16) return SGA_ERR_UNSUPPORTED;
         if (pb.seg_rows > 0x7FFFFFFFLL || pb.kv_rows > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
         namespace T = sga::tc;
-        {
-            std::lock_guard<std::mutex> lk(g_dev_mu);
-            if (!di->tc_smem_set) {
-                // the kernel's setmaxnreg split assumes exactly LAUNCH_REGS registers per thread
-                // at launch; any other count would leave setmaxnreg.inc unsatisfiable
-                cudaFuncAttributes fa;
-                if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel) != cudaSuccess) return SGA_ERR_CUDA;
-                if (fa.numRegs != (int)T::LAUNCH_REGS) return SGA_ERR_UNSUPPORTED;
-                if (cudaFuncSetAttribute(T::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::SMEM_BYTES) != cudaSuccess)
-                    return SGA_ERR_CUDA;
-                di->tc_smem_set = true;
-            }
-        }
+        if ((st = pb.bias ? prepare_tc<true>(di) : prepare_tc<false>(di)) != SGA_OK) return st;
         CUtensorMap mq, mk, mv;
         if ((st = make_map(&mq, pb.Q, pb.seg_rows, pb.n_seg)) != SGA_OK) return st;
         if ((st = make_map(&mk, pb.Kt, pb.kv_rows, pb.n_seg)) != SGA_OK) return st;
@@ -159,8 +165,13 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.O = reinterpret_cast<__nv_bfloat16*>(pb.O);
         a.lse = pb.lse;
         a.ex = pb.ex;
+        a.bias = pb.bias;
+        a.inv_scale = 1.0f / pb.scale;
         const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
-        T::attn_tc_kernel<<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+        if (pb.bias)
+            T::attn_tc_kernel<true><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+        else
+            T::attn_tc_kernel<false><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
         return launch_status();
     }
     if (kern != SGA_KERNEL_SIMT) return SGA_ERR_INVALID_ARG;
@@ -174,6 +185,7 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
     a.lse = pb.lse;
     a.scale_log2 = scale_log2;
     a.ex = pb.ex;
+    a.bias = pb.bias;
     const long long gx = (pb.seg_rows + sga::kSimtRows - 1) / sga::kSimtRows;
     if (gx > 0x7FFFFFFFLL || pb.n_seg > 65535) return SGA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)gx, (unsigned)pb.n_seg);
@@ -276,20 +288,15 @@ const char* sga_status_string(sga_status s) {
 
 const char* sga_build_info(void) { return "libsga sm_103a (tcgen05/TMEM/TMA attention, CUDA-core fp32 path) v1"; }
 
-sga_status sga_plan_create(const sga_config* cfg, int device, sga_plan_t* out) {
-    if (!cfg || !out) return SGA_ERR_INVALID_ARG;
-    *out = nullptr;
-    sga_status st = check_config(cfg);
-    if (st != SGA_OK) return st;
-    const sga_config& c = *cfg;
+}  // extern "C"
+
+namespace {
+
+// Upload a kept set (slot map, ascending kept list, frame offsets) as a plan on `device`.
+sga_status upload_plan(const sga_config& c, const std::vector<int32_t>& slot, const std::vector<int32_t>& kv,
+                       const std::vector<int32_t>& off, int device, sga_plan_t* out) {
     const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
     const long long T = L * c.N;
-
-    std::vector<int32_t> slot((size_t)T);
-    std::vector<int32_t> kv;
-    std::vector<int32_t> off((size_t)c.N + 1);
-    build_plan(c, slot, kv, off);
-
     sga_plan_s* plan = new (std::nothrow) sga_plan_s();
     if (!plan) return SGA_ERR_CUDA;
     plan->magic = kPlanMagic;
@@ -333,6 +340,120 @@ sga_status sga_plan_create(const sga_config* cfg, int device, sga_plan_t* out) {
         return SGA_ERR_CUDA;
     }
     *out = plan;
+    return SGA_OK;
+}
+
+// Generalised kept set ("RegimeVGGT ..." Key design 3): rational per-axis window sizes
+// sigma = num/den >= 1, a window keeping its first position ceil(i*sigma); with the phase
+// shift the positions move by phi_r = (f div t_w) mod t_h, phi_c = f mod t_w with the integer
+// tiles t = ceil(sigma); frame 0 (when dense) and the camera/register tokens kept; protected
+// tokens kept in full.  Exact integer arithmetic.
+bool window_start(long long x, long long phi, long long num, long long den) {
+    if (x < phi) return false;
+    const long long y = x - phi;
+    if (y == 0) return true;
+    const long long i = ((y - 1) * den) / num + 1;     // first window whose start is >= y
+    return (i * num + den - 1) / den == y;
+}
+
+sga_status build_plan_general(const sga_grid_spec& g, const int32_t* prot, int64_t n_prot,
+                              std::vector<int32_t>& slot, std::vector<int32_t>& kv, std::vector<int32_t>& off) {
+    const long long L = (long long)g.n_special + (long long)g.grid_h * g.grid_w;
+    const long long T = L * g.N;
+    std::vector<uint8_t> kept((size_t)T, 0);
+    for (int64_t i = 0; i < n_prot; ++i) {
+        if (prot[i] < 0 || prot[i] >= T) return SGA_ERR_INVALID_ARG;
+        kept[(size_t)prot[i]] = 1;
+    }
+    const long long th = (g.sh_num + g.sh_den - 1) / g.sh_den, tw = (g.sw_num + g.sw_den - 1) / g.sw_den;
+    std::vector<uint8_t> row_ok((size_t)g.grid_h), col_ok((size_t)g.grid_w);
+    slot.assign((size_t)T, -1);
+    kv.clear();
+    off.assign((size_t)g.N + 1, 0);
+    for (int f = 0; f < g.N; ++f) {
+        off[f] = (int32_t)kv.size();
+        const long long pr = g.phase_shift ? (f / tw) % th : 0;
+        const long long pc = g.phase_shift ? f % tw : 0;
+        for (int r = 0; r < g.grid_h; ++r) row_ok[r] = window_start(r, pr, g.sh_num, g.sh_den);
+        for (int c = 0; c < g.grid_w; ++c) col_ok[c] = window_start(c, pc, g.sw_num, g.sw_den);
+        const bool dense = f == 0 && g.ref_frame_dense;
+        for (long long p = 0; p < L; ++p) {
+            const long long t = (long long)f * L + p;
+            bool keep = dense || p < g.n_special || kept[(size_t)t];
+            if (!keep) {
+                const long long q = p - g.n_special;
+                keep = row_ok[q / g.grid_w] && col_ok[q % g.grid_w];
+            }
+            if (keep) {
+                slot[(size_t)t] = (int32_t)kv.size();
+                kv.push_back((int32_t)t);
+            }
+        }
+    }
+    off[g.N] = (int32_t)kv.size();
+    return SGA_OK;
+}
+
+sga_status check_grid_spec(const sga_grid_spec* g) {
+    if (!g) return SGA_ERR_INVALID_ARG;
+    if (g->N <= 0 || g->grid_h <= 0 || g->grid_w <= 0 || g->n_special < 0 || g->sh_den <= 0 || g->sw_den <= 0 ||
+        g->sh_num < g->sh_den || g->sw_num < g->sw_den)
+        return SGA_ERR_INVALID_ARG;
+    const long long L = (long long)g->n_special + (long long)g->grid_h * g->grid_w;
+    if (L * g->N > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    return SGA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sga_status sga_plan_create(const sga_config* cfg, int device, sga_plan_t* out) {
+    if (!cfg || !out) return SGA_ERR_INVALID_ARG;
+    *out = nullptr;
+    sga_status st = check_config(cfg);
+    if (st != SGA_OK) return st;
+    std::vector<int32_t> slot, kv, off;
+    build_plan(*cfg, slot, kv, off);
+    return upload_plan(*cfg, slot, kv, off, device, out);
+}
+
+sga_status sga_plan_create_from_index(const sga_config* cfg, const int32_t* kv_index, int64_t S, int device,
+                                      sga_plan_t* out) {
+    if (!cfg || !out || (S > 0 && !kv_index) || S < 0) return SGA_ERR_INVALID_ARG;
+    *out = nullptr;
+    sga_status st = check_config(cfg);
+    if (st != SGA_OK) return st;
+    const sga_config& c = *cfg;
+    const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
+    const long long T = L * c.N;
+    if (S > T) return SGA_ERR_INVALID_ARG;
+    std::vector<int32_t> slot((size_t)T, -1), kv(kv_index, kv_index + S), off((size_t)c.N + 1, 0);
+    for (int64_t i = 0; i < S; ++i) {
+        if (kv[i] < 0 || kv[i] >= T || (i > 0 && kv[i] <= kv[i - 1])) return SGA_ERR_INVALID_ARG;
+        slot[(size_t)kv[i]] = (int32_t)i;
+    }
+    // off[f] = number of kept tokens before frame f
+    int64_t i = 0;
+    for (int f = 0; f <= c.N; ++f) {
+        while (i < S && kv[i] < (long long)f * L) ++i;
+        off[f] = (int32_t)i;
+    }
+    return upload_plan(c, slot, kv, off, device, out);
+}
+
+sga_status sga_plan_host_general(const sga_grid_spec* spec, const int32_t* protected_tokens, int64_t n_protected,
+                                 int32_t* kv_index, int32_t* frame_off, int32_t* slot, int64_t* S_out) {
+    if (!kv_index || !frame_off || !S_out || n_protected < 0 || (n_protected > 0 && !protected_tokens))
+        return SGA_ERR_INVALID_ARG;
+    sga_status st = check_grid_spec(spec);
+    if (st != SGA_OK) return st;
+    std::vector<int32_t> sl, kv, off;
+    if ((st = build_plan_general(*spec, protected_tokens, n_protected, sl, kv, off)) != SGA_OK) return st;
+    std::memcpy(kv_index, kv.data(), sizeof(int32_t) * kv.size());
+    std::memcpy(frame_off, off.data(), sizeof(int32_t) * off.size());
+    if (slot) std::memcpy(slot, sl.data(), sizeof(int32_t) * sl.size());
+    *S_out = (int64_t)kv.size();
     return SGA_OK;
 }
 
@@ -446,12 +567,13 @@ sga_status sga_forward(sga_plan_t plan, const void* Q, const void* K, const void
     pb.ex.V = V;
     pb.ex.k_sum = k_sum;
     pb.ex.v_sum = v_sum;
+    pb.bias = nullptr;
     return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
 }
 
-static sga_status plain_attention(int n_seg, long long seg_rows, int dtype, int kernel, const void* Q,
-                                  const void* K, const void* V, void* O, float* lse, float scale,
-                                  void* stream) {
+static sga_status plain_attention(int n_seg, long long seg_rows, long long kv_rows, int dtype, int kernel,
+                                  const void* Q, const void* K, const void* V, const float* bias, void* O,
+                                  float* lse, float scale, void* stream) {
     if (!Q || !K || !V || !O) return SGA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (lse && !aligned16(lse)))
         return SGA_ERR_ALIGNMENT;
@@ -462,7 +584,7 @@ static sga_status plain_attention(int n_seg, long long seg_rows, int dtype, int 
     pb.kernel = kernel;
     pb.n_seg = n_seg;
     pb.seg_rows = seg_rows;
-    pb.kv_rows = seg_rows;
+    pb.kv_rows = kv_rows;
     pb.Q = Q;
     pb.Kt = K;
     pb.Vt = V;
@@ -470,6 +592,7 @@ static sga_status plain_attention(int n_seg, long long seg_rows, int dtype, int 
     pb.lse = lse;
     pb.scale = scale;
     pb.ex.on = 0;
+    pb.bias = bias;
     return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -480,7 +603,7 @@ sga_status sga_dense_forward(int B, int H, int64_t T, int head_dim, int dtype, i
     sga_status st = check_common(dtype, head_dim, kernel);
     if (st != SGA_OK) return st;
     if ((long long)B * H > 0x7FFFFFFFLL || T > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
-    return plain_attention(B * H, T, dtype, kernel, Q, K, V, O, lse, scale, stream);
+    return plain_attention(B * H, T, T, dtype, kernel, Q, K, V, nullptr, O, lse, scale, stream);
 }
 
 sga_status sga_frame_forward(int B, int H, int N, int L, int head_dim, int dtype, int kernel,
@@ -490,7 +613,18 @@ sga_status sga_frame_forward(int B, int H, int N, int L, int head_dim, int dtype
     sga_status st = check_common(dtype, head_dim, kernel);
     if (st != SGA_OK) return st;
     if ((long long)B * H * N > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
-    return plain_attention(B * H * N, L, dtype, kernel, Q, K, V, O, lse, scale, stream);
+    return plain_attention(B * H * N, L, L, dtype, kernel, Q, K, V, nullptr, O, lse, scale, stream);
+}
+
+sga_status sga_bias_forward(int B, int H, int64_t Tq, int64_t Tk, int head_dim, int dtype, int kernel,
+                            const void* Q, const void* K, const void* V, const float* bias, void* O,
+                            float* lse, float scale, void* stream) {
+    if (B <= 0 || H <= 0 || Tq <= 0 || Tk <= 0 || !bias) return SGA_ERR_INVALID_ARG;
+    sga_status st = check_common(dtype, head_dim, kernel);
+    if (st != SGA_OK) return st;
+    if ((long long)B * H > 0x7FFFFFFFLL || Tq > 0x7FFFFFFFLL || Tk > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(bias) & 3u) != 0) return SGA_ERR_ALIGNMENT;
+    return plain_attention(B * H, Tq, Tk, dtype, kernel, Q, K, V, bias, O, lse, scale, stream);
 }
 
 sga_status sga_device_status(void* stream) {

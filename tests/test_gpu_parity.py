@@ -305,3 +305,173 @@ def test_sweep_frame_local_sampled(dev):
         gots.append(_host(out[0, h][ridx]))
         refs.append(ref)
     _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "frame sweep")
+
+
+# ------------------------------------------------------------------------------ size-aware bias
+# "RegimeVGGT ..." Key design 2: softmax(QK^T/sqrt(d) + log g) V.
+def _bias_case(dev, Tq, Tk, H, seed, dtype=torch.bfloat16, g_max=8, real=False):
+    q, _, _ = correlated_qkv(1, H, 1, Tq, 64, seed=seed, dtype=dtype, device=dev)
+    _, k, v = correlated_qkv(1, H, 1, Tk, 64, seed=seed + 1, dtype=dtype, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(seed + 2)
+    if real:
+        bias = torch.randn((1, H, Tk), generator=gen, device=dev) * 3.0
+        bias[..., ::7] = -1e4    # effectively removed keys
+    else:
+        g = torch.randint(1, g_max + 1, (1, H, Tk), generator=gen, device=dev)
+        bias = torch.log(g.float())
+    return q, k, v, bias.contiguous()
+
+
+def _check_bias(q, k, v, bias, out, dtype, lse=None, rows=None):
+    H = q.shape[1]
+    for h in range(H):
+        rr = np.arange(q.shape[2]) if rows is None else rows
+        ref, rl = oracle.biased_attention_rows(_host(q[0, h])[rr], _host(k[0, h]), _host(v[0, h]),
+                                               bias[0, h].double().cpu().numpy())
+        _compare(_host(out[0, h])[rr], ref, dtype, f"bias h{h}")
+        if lse is not None:
+            assert np.abs(lse[0, h].cpu().numpy()[rr] - rl).max() < (1e-5 if dtype == "f32" else 2e-3)
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+@pytest.mark.parametrize("Tq,Tk,real", [(700, 450, False), (256, 1000, True), (130, 129, False), (1, 5, True)])
+def test_bias_forward(dev, kernel, Tq, Tk, real):
+    q, k, v, bias = _bias_case(dev, Tq, Tk, 2, seed=40 + Tq, real=real)
+    lse = torch.empty((1, 2, Tq), dtype=torch.float32, device=dev)
+    out = sga.bias_forward(q, k, v, bias, kernel=kernel, lse=lse)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    _check_bias(q, k, v, bias, out, "bf16", lse)
+
+
+def test_bias_forward_f32(dev):
+    q, k, v, bias = _bias_case(dev, 300, 333, 2, seed=50, dtype=torch.float32, real=True)
+    out = sga.bias_forward(q, k, v, bias, dtype="f32")
+    torch.cuda.synchronize(dev)
+    _check_bias(q, k, v, bias, out, "f32")
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_bias_integer_groups_match_expanded_dense(dev, kernel):
+    # the same identity the oracle is pinned with, on the GPU: bias ln g == g copies of the key
+    q, k, v, bias = _bias_case(dev, 384, 200, 2, seed=60, g_max=4)
+    g = torch.round(torch.exp(bias)).long()
+    out = sga.bias_forward(q, k, v, bias, kernel=kernel)
+    for h in range(2):
+        ke = torch.repeat_interleave(k[:, h:h + 1], g[0, h], dim=2).contiguous()
+        ve = torch.repeat_interleave(v[:, h:h + 1], g[0, h], dim=2).contiguous()
+        qe = q[:, h:h + 1].contiguous()
+        oe = torch.empty_like(qe)
+        # dense attention over the expanded keys: queries and keys differ in count, so use the
+        # biased entry point with a zero bias (a separate check that zero bias == dense follows)
+        sga.bias_forward(qe, ke, ve, torch.zeros(ke.shape[:3], device=dev), kernel=kernel, out=oe)
+        torch.cuda.synchronize(dev)
+        ref, _ = oracle.biased_attention_rows(_host(qe[0, 0]), _host(ke[0, 0]), _host(ve[0, 0]),
+                                              np.zeros(ke.shape[2]))
+        _compare(_host(oe[0, 0]), ref, "bf16", "expanded dense")
+        _compare(_host(out[0, h]), ref, "bf16", "biased vs expanded")
+
+
+def test_bias_zero_equals_dense_entry_point(dev):
+    q, k, v = correlated_qkv(1, 2, 3, 300, 64, seed=61, dtype=torch.bfloat16, device=dev)
+    od = sga.dense_forward(q, k, v)
+    ob = sga.bias_forward(q, k, v, torch.zeros(q.shape[:3], device=dev))
+    torch.cuda.synchronize(dev)
+    # same tensor-core kernel, the bias step only adds exact zeros
+    assert torch.equal(od, ob)
+
+
+def test_bias_bad_arguments(dev):
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device=dev)
+    lib = sga.lib()
+    import ctypes
+    p = ctypes.c_void_p(q.data_ptr())
+    assert lib.sga_bias_forward(1, 1, 128, 128, 64, 0, 0, p, p, p, None, p, None, ctypes.c_float(0.125), None) == 1
+    with pytest.raises(ValueError):
+        sga.bias_forward(q, q, q, torch.zeros((1, 1, 127), device=dev))
+
+
+def test_bias_merged_keys_sampled(dev):
+    # a merged-key layer of 32 VGGT frames: 43,968 queries against 12,000 merged keys that
+    # stand for 1-8 tokens each, 16 heads; 2048 sampled query rows against the oracle
+    H, Tq, Tk = 16, 43968, 12000
+    q, k, v, bias = _bias_case(dev, Tq, Tk, H, seed=70)
+    out = sga.bias_forward(q, k, v, bias)
+    torch.cuda.synchronize(dev)
+    gots, refs = [], []
+    for h in range(H):
+        rows = sample_rows(Tq, 1374, 128, seed=300 + h).numpy()
+        ref, _ = oracle.biased_attention_rows(_host(q[0, h])[rows], _host(k[0, h]), _host(v[0, h]),
+                                              bias[0, h].double().cpu().numpy())
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "merged keys")
+
+
+# ------------------------------------------------------------------------------ generalised kept set
+# "RegimeVGGT ..." Key design 3: fractional per-axis windows, phase shift, protected tokens; and
+# any kept set given as an index list, through the same compaction and attention.
+def _general_case(dev, cfg, sh, sw, phase, n_prot, seed, dtype=torch.bfloat16):
+    rng = np.random.default_rng(seed)
+    prot = rng.integers(0, cfg.T, size=n_prot)
+    kv, _, _ = sga.plan_host_general(cfg.N, cfg.grid_h, cfg.grid_w, cfg.n_special, sigma_h=sh, sigma_w=sw,
+                                     phase_shift=phase, ref_frame_dense=cfg.ref_frame_dense, protected=prot)
+    op = oracle.plan_general(cfg.N, cfg.grid_h, cfg.grid_w, cfg.n_special, sh, sw, phase, cfg.ref_frame_dense,
+                             protected=prot)
+    q, k, v = correlated_qkv(cfg.B, cfg.H, cfg.N, cfg.L, 64, seed=seed, dtype=dtype, device=dev)
+    plan = sga.Plan(cfg, dev, kv_index=kv)
+    assert plan.S == op.S
+    out = plan.layer(q, k, v)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    return op, q, k, v, out
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+@pytest.mark.parametrize("sh,sw,phase", [((3, 2), (3, 2), True), ((13, 10), (17, 10), False), ((17, 10), (17, 10), True)])
+def test_general_plan_full(dev, kernel, sh, sw, phase):
+    cfg = sga.SGAConfig(B=1, H=2, N=6, grid_h=13, grid_w=11, kernel=kernel)
+    op, q, k, v, out = _general_case(dev, cfg, sh, sw, phase, n_prot=9, seed=80)
+    for h in range(2):
+        ref, _ = oracle.sga_full(op, _host(q[0, h]), _host(k[0, h]), _host(v[0, h]))
+        _compare(_host(out[0, h]), ref, "bf16", f"general h{h}")
+
+
+def test_arbitrary_kept_set_f32(dev):
+    cfg = sga.SGAConfig(B=1, H=2, N=4, grid_h=9, grid_w=8, dtype="f32")
+    rng = np.random.default_rng(81)
+    kv = np.sort(rng.choice(cfg.T, size=cfg.T // 3, replace=False)).astype(np.int32)
+    q, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=81, dtype=torch.float32, device=dev)
+    plan = sga.Plan(cfg, dev, kv_index=kv)
+    out = plan.layer(q, k, v)
+    torch.cuda.synchronize(dev)
+    kept = np.zeros(cfg.T, dtype=np.uint8)
+    kept[kv] = 1
+    off = np.searchsorted(kv, np.arange(cfg.N + 1) * cfg.L).astype(np.int32)
+    op = oracle.Plan(T=cfg.T, L=cfg.L, kept=kept, kv_index=kv, frame_off=off)
+    got_kv, got_off = plan.indices()
+    assert np.array_equal(got_kv, kv) and np.array_equal(got_off, off)
+    for h in range(2):
+        ref, _ = oracle.sga_full(op, _host(q[0, h]), _host(k[0, h]), _host(v[0, h]))
+        _compare(_host(out[0, h]), ref, "f32", f"arbitrary h{h}")
+
+
+def test_arbitrary_kept_set_rejected(dev):
+    cfg = sga.SGAConfig(B=1, H=1, N=2, grid_h=4, grid_w=4)
+    for bad in ([3, 3, 5], [5, 2], [-1, 4], [0, cfg.T]):
+        with pytest.raises(sga.SgaError):
+            sga.Plan(cfg, dev, kv_index=np.array(bad, dtype=np.int32))
+
+
+def test_general_plan_vggt_sampled(dev):
+    # 32 VGGT frames, RegimeVGGT middle band: sigma_b = 1.3 per axis, phase shift, 10 % of the
+    # patches protected as salient; 4096 sampled rows against the oracle
+    cfg = sga.SGAConfig(B=1, H=16, N=32)
+    op, q, k, v, out = _general_case(dev, cfg, (13, 10), (13, 10), True, n_prot=cfg.T // 10, seed=82)
+    gots, refs = [], []
+    for h in range(cfg.H):
+        rows = sample_rows(cfg.T, cfg.L, 256, seed=400 + h, kept=op.kept).numpy()
+        ref, _ = oracle.sga_rows(op, _host(q[0, h])[rows], _host(k[0, h]), _host(v[0, h]), rows)
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "general sampled")

@@ -106,3 +106,36 @@ def test_null_arguments_rejected_without_device():
     buf = (ctypes.c_char * 64)()
     p = ctypes.addressof(buf) + 1  # misaligned
     assert L.sga_dense_forward(1, 1, 4, 64, 0, 0, p, p, p, p, None, ctypes.c_float(0.125), None) == 3
+
+
+GENERAL_CASES = [
+    # N, gh, gw, nsp, sigma_h, sigma_w, phase, ref, n_protected
+    (7, 11, 13, 5, (3, 2), (3, 2), False, True, 0),
+    (7, 11, 13, 5, (13, 10), (17, 10), True, True, 12),
+    (5, 37, 28, 5, (17, 10), (3, 2), True, False, 40),
+    (9, 37, 37, 5, (2, 1), (2, 1), True, True, 0),
+    (3, 4, 6, 0, (7, 3), (1, 1), True, False, 5),
+    (800, 37, 37, 5, (3, 2), (3, 2), True, True, 1000),
+]
+
+
+@pytest.mark.parametrize("case", GENERAL_CASES)
+def test_general_plan_bit_exact_vs_oracle(case):
+    N, gh, gw, nsp, sh, sw, phase, ref, n_prot = case
+    T = N * (nsp + gh * gw)
+    prot = np.random.default_rng(N * 7 + gh).integers(0, T, size=n_prot)
+    kv, off, slot = sga.plan_host_general(N, gh, gw, nsp, sigma_h=sh, sigma_w=sw, phase_shift=phase,
+                                          ref_frame_dense=ref, protected=prot)
+    op = oracle.plan_general(N, gh, gw, nsp, sh, sw, phase, ref, protected=prot)
+    assert np.array_equal(kv, op.kv_index)
+    assert np.array_equal(off, op.frame_off)
+    want_slot = np.full(op.T, -1, dtype=np.int32)
+    want_slot[op.kv_index] = np.arange(op.S, dtype=np.int32)
+    assert np.array_equal(slot, want_slot)
+
+
+def test_general_plan_rejects_bad_specs():
+    with pytest.raises(sga.SgaError):
+        sga.plan_host_general(2, 4, 4, 5, sigma_h=(1, 2))          # sigma < 1
+    with pytest.raises(sga.SgaError):
+        sga.plan_host_general(2, 4, 4, 5, protected=[2 * 21])      # outside [0, N*L)
