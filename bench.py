@@ -26,6 +26,7 @@ import sys
 import tempfile
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -34,17 +35,51 @@ sys.path.insert(0, ROOT)
 METRIC = "SGA ms/layer and effective TFLOP/s at 800 frames, σ=4 (fraction of bf16 peak)"
 
 WORKLOADS = {
-    "headline": dict(desc="SGA layer: N=800 frames x 1374 tokens (37x37 patches + 5 special), H=16, d=64, "
+    "headline": dict(kind="sga",
+                     desc="SGA layer: N=800 frames x 1374 tokens (37x37 patches + 5 special), H=16, d=64, "
                           "bf16, sigma=4 (2,2), frame 0 and special tokens dense, diagonal + mean "
                           "(leave-one-out, ln count bias)",
                      cfg=dict(B=1, H=16, N=800, sigma=4)),
-    "vggt": dict(desc="SGA layer: N=32 frames x 1374 tokens, H=16, d=64, bf16, sigma=4, diag+mean",
+    "vggt": dict(kind="sga", desc="SGA layer: N=32 frames x 1374 tokens, H=16, d=64, bf16, sigma=4, diag+mean",
                  cfg=dict(B=1, H=16, N=32, sigma=4)),
-    "long": dict(desc="SGA layer: N=200 frames x 1374 tokens, H=16, d=64, bf16, sigma=9 (3,3), diag+mean",
+    "long": dict(kind="sga", desc="SGA layer: N=200 frames x 1374 tokens, H=16, d=64, bf16, sigma=9 (3,3), diag+mean",
                  cfg=dict(B=1, H=16, N=200, sigma=9)),
-    "tiny": dict(desc="SGA layer: N=4 frames x 69 tokens (8x8 + 5), H=2, d=64, fp32, sigma=4, diag+mean",
+    "tiny": dict(kind="sga", desc="SGA layer: N=4 frames x 69 tokens (8x8 + 5), H=2, d=64, fp32, sigma=4, diag+mean",
                  cfg=dict(B=1, H=2, N=4, grid_h=8, grid_w=8, sigma=4, dtype="f32")),
+    "general": dict(kind="sga",
+                    desc="SGA layer, generalised kept set: N=200 frames x 1374 tokens, H=16, d=64, bf16, "
+                         "per-axis sigma_b = 1.3 with phase shift, frame 0 + special tokens dense, 10 % of "
+                         "the tokens protected, diagonal + mean",
+                    cfg=dict(B=1, H=16, N=200), general=dict(sigma=(13, 10), phase=True, protected=0.10)),
+    "merged": dict(kind="bias",
+                   desc="size-aware attention: 274,800 queries (200 frames x 1374) against 137,400 merged "
+                        "keys standing for 1-3 tokens each (bias ln g), H=16, d=64, bf16",
+                   shape=dict(H=16, Tq=274800, Tk=137400)),
+    "dense": dict(kind="dense", desc="dense global attention (sigma = 1): N=32 frames x 1374 tokens, H=16, d=64, bf16",
+                  shape=dict(H=16, N=32, L=1374)),
+    "frame": dict(kind="frame", desc="frame-local attention (Global-to-Frame): N=100 frames x 1374 tokens, H=16, "
+                                     "d=64, bf16", shape=dict(H=16, N=100, L=1374)),
 }
+
+# DRAM traffic of the dominant kernel per launch, measured with
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass) on this file's default
+# workload, keyed by a fingerprint of the kernel's sources; reported only while they are unchanged.
+KERNEL_SOURCES = ("subsampled_global_attention_sga_b300/csrc/attn_tc.cuh",
+                  "subsampled_global_attention_sga_b300/csrc/common.cuh",
+                  "subsampled_global_attention_sga_b300/csrc/extras.cuh")
+TRAFFIC_GB = {
+    # attn_tc_kernel<false> on the 800-frame sigma = 4 layer: 379.49 GB read + 2.71 GB written
+    "40917419ae2423cb": {"headline": 382.20},
+}
+
+
+def _kernel_fingerprint() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def _peaks():
@@ -177,40 +212,172 @@ def cpu_oracle_sample(cfg, q, k, v, target_s: float = 12.0, h: int = 0, max_rows
             "seconds": t_rows, "extrapolated_ms_per_layer": ms_layer}
 
 
+class Job:
+    """One workload on the device: stages run in order per step, FLOPs per step, the dominant
+    stage (name, roofline bound, algorithmic amount per launch) and an end-to-end call."""
+
+    def __init__(self, sga, wl, dev, rank):
+        from subsampled_global_attention_sga_b300.inputs import correlated_qkv
+        self.sga, self.wl, self.dev, self.kind = sga, wl, dev, wl["kind"]
+        seed = 3 * rank
+        if self.kind == "sga":
+            cfg = sga.SGAConfig(**wl["cfg"])
+            self.cfg = cfg
+            q, k, v = correlated_qkv(cfg.B, cfg.H, cfg.N, cfg.L, 64, seed=seed, dtype=cfg.torch_dtype, device=dev)
+            if "general" in wl:
+                g = wl["general"]
+                prot = np.random.default_rng(seed).integers(0, cfg.T, size=int(g["protected"] * cfg.T))
+                kv, _, _ = sga.plan_host_general(cfg.N, cfg.grid_h, cfg.grid_w, cfg.n_special, sigma_h=g["sigma"],
+                                                 sigma_w=g["sigma"], phase_shift=g["phase"],
+                                                 ref_frame_dense=cfg.ref_frame_dense, protected=prot)
+                self.plan = sga.Plan(cfg, dev, kv_index=kv)
+                self.kv_index = kv
+            else:
+                self.plan = sga.Plan(cfg, dev)
+                self.kv_index = None
+            self.inputs = (q, k, v)
+            self.bufs = self.plan.compact(k, v)
+            self.out = torch.empty_like(q)
+            plan, bufs, out = self.plan, self.bufs, self.out
+            self.stages = [("compaction", lambda: plan.compact(k, v, *bufs)),
+                           ("attention", lambda: plan.forward(q, k, v, *bufs, out=out))]
+            self.flops = layer_flops(cfg, plan.S)
+            self.dominant = ("attention", "tensor", self.flops, "sga::tc::attn_tc_kernel<false>")
+            self.secondary = ("compaction", "hbm", compaction_bytes(cfg, plan.S), "sga::compact_kernel")
+            self.dtype = cfg.dtype
+            self.config = {"B_per_rank": cfg.B, "H": cfg.H, "N": cfg.N, "L": cfg.L, "T": cfg.T, "S": plan.S,
+                           "sigma": cfg.sigma, "flops_per_layer": self.flops}
+        elif self.kind == "bias":
+            sh = wl["shape"]
+            H, Tq, Tk = sh["H"], sh["Tq"], sh["Tk"]
+            q, _, _ = correlated_qkv(1, H, 1, Tq, 64, seed=seed, dtype=torch.bfloat16, device=dev)
+            _, k, v = correlated_qkv(1, H, 1, Tk, 64, seed=seed + 1, dtype=torch.bfloat16, device=dev)
+            gen = torch.Generator(device=dev).manual_seed(seed + 2)
+            bias = torch.log(torch.randint(1, 4, (1, H, Tk), generator=gen, device=dev).float()).contiguous()
+            self.inputs = (q, k, v, bias)
+            self.out = torch.empty_like(q)
+            out = self.out
+            self.stages = [("attention", lambda: sga.bias_forward(q, k, v, bias, out=out))]
+            self.flops = 4.0 * Tq * Tk * 64 * H
+            self.dominant = ("attention", "tensor", self.flops, "sga::tc::attn_tc_kernel<true>")
+            self.secondary = None
+            self.dtype = "bf16"
+            self.config = {"H": H, "Tq": Tq, "Tk": Tk, "flops_per_layer": self.flops}
+        else:
+            sh = wl["shape"]
+            H, N, L = sh["H"], sh["N"], sh["L"]
+            q, k, v = correlated_qkv(1, H, N, L, 64, seed=seed, dtype=torch.bfloat16, device=dev)
+            self.inputs = (q, k, v)
+            self.out = torch.empty_like(q)
+            out = self.out
+            if self.kind == "dense":
+                self.stages = [("attention", lambda: sga.dense_forward(q, k, v, out=out))]
+                self.flops = 4.0 * (N * L) ** 2 * 64 * H
+            else:
+                self.stages = [("attention", lambda: sga.frame_forward(q, k, v, N, L, out=out))]
+                self.flops = 4.0 * N * L * L * 64 * H
+            self.dominant = ("attention", "tensor", self.flops, "sga::tc::attn_tc_kernel<false>")
+            self.secondary = None
+            self.dtype = "bf16"
+            self.config = {"H": H, "N": N, "L": L, "T": N * L, "flops_per_layer": self.flops}
+
+    def step(self, ev=None, stream=None):
+        for i, (_, fn) in enumerate(self.stages):
+            if ev is not None:
+                ev[i].record(stream)
+            fn()
+        if ev is not None:
+            ev[len(self.stages)].record(stream)
+
+    def e2e_call(self, host_in, out_host):
+        """Copy this step's inputs from pinned host memory, run the layer, copy the result back."""
+        sga, dev = self.sga, self.dev
+        if self.kind == "sga":
+            return sga.layer_from_host(self.plan, *host_in, out_host=out_host)
+        dev_in = [x.to(dev, non_blocking=True) for x in host_in]
+        if self.kind == "bias":
+            o = sga.bias_forward(*dev_in)
+        elif self.kind == "dense":
+            o = sga.dense_forward(*dev_in)
+        else:
+            sh = self.wl["shape"]
+            o = sga.frame_forward(*dev_in, sh["N"], sh["L"])
+        out_host.copy_(o, non_blocking=True)
+        return out_host
+
+    def cpu_sample(self, target_s=12.0, h=0, max_rows=4096):
+        """Time the fp64 oracle on sampled query rows of one (batch, head)."""
+        import oracle
+        from subsampled_global_attention_sga_b300.inputs import sample_rows
+        kind = self.kind
+        hx = [x[0, h].float().cpu().numpy() for x in self.inputs[:3]]
+        qh, kh, vh = hx
+        Tq = qh.shape[0]
+        extra_t, pre = 0.0, None
+        if kind == "sga":
+            cfg = self.cfg
+            if self.kv_index is None:
+                s_h, s_w = cfg.s_hw
+                op = oracle.plan(cfg.N, cfg.grid_h, cfg.grid_w, cfg.n_special, s_h, s_w, cfg.phase_shift,
+                                 cfg.ref_frame_dense)
+            else:
+                kept = np.zeros(cfg.T, dtype=np.uint8)
+                kept[self.kv_index] = 1
+                op = oracle.Plan(T=cfg.T, L=cfg.L, kept=kept, kv_index=self.kv_index,
+                                 frame_off=np.searchsorted(self.kv_index, np.arange(cfg.N + 1) * cfg.L).astype(np.int32))
+            t0 = time.perf_counter()
+            sums = oracle.dropped_sums(op, kh, vh)
+            extra_t = time.perf_counter() - t0
+            n_keys = op.S + (2 if (cfg.diag or cfg.mean) else 0)
+            run = lambda rows: oracle.sga_rows(op, qh[rows], kh, vh, rows, diag=cfg.diag, mean=cfg.mean, sums=sums)
+            L = cfg.L
+        elif kind == "bias":
+            b = self.inputs[3][0, h].double().cpu().numpy()
+            n_keys = kh.shape[0]
+            run = lambda rows: oracle.biased_attention_rows(qh[rows], kh, vh, b)
+            L = 1374
+        else:
+            L = self.wl["shape"]["L"]
+            fl = L if kind == "frame" else 0
+            n_keys = L if kind == "frame" else kh.shape[0]
+            run = lambda rows: oracle.attention_rows(qh[rows], kh, vh, rows, frame_len=fl)
+        calib = min(64, Tq)
+        rows = sample_rows(Tq, L, calib, seed=77).numpy()
+        t0 = time.perf_counter()
+        run(rows)
+        t_cal = time.perf_counter() - t0
+        n = int(max(calib, min(max_rows, Tq, calib * max(1.0, (target_s - t_cal) / max(t_cal, 1e-6)))))
+        rows = sample_rows(Tq, L, n, seed=78).numpy()
+        t0 = time.perf_counter()
+        run(rows)
+        t_rows = time.perf_counter() - t0
+        n = len(rows)
+        flops = 4.0 * n * n_keys * 64
+        heads = self.flops / (4.0 * Tq * n_keys * 64)
+        ms_layer = (t_rows / n * Tq + extra_t) * heads * 1e3
+        return {"value": flops / t_rows / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": f"{n} query rows of head {h} (of {Tq} rows x {heads:.0f} heads); fp64 C oracle, OpenMP",
+                "seconds": t_rows, "extrapolated_ms_per_layer": ms_layer}
+
+
 def run_ours(args):
     import subsampled_global_attention_sga_b300 as sga
-    from subsampled_global_attention_sga_b300.inputs import correlated_qkv
 
     rank, world, local = _dist()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = WORKLOADS[args.workload]
-    cfg = sga.SGAConfig(**wl["cfg"])
-    tdt = cfg.torch_dtype
-    # each rank its own batch element: independent seeds
-    q, k, v = correlated_qkv(1, cfg.H, cfg.N, cfg.L, 64, seed=3 * rank, dtype=tdt, device=dev)
-    plan = sga.Plan(cfg, dev)
-    K_S, V_S, k_sum, v_sum = plan.compact(k, v)
-    out = torch.empty_like(q)
+    job = Job(sga, wl, dev, rank)
     stream = torch.cuda.current_stream(dev)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        plan.compact(k, v, K_S, V_S, k_sum, v_sum)
-        if ev is not None:
-            ev[1].record(stream)
-        plan.forward(q, k, v, K_S, V_S, k_sum, v_sum, out=out)
-        if ev is not None:
-            ev[2].record(stream)
+    n_st = len(job.stages)
 
     for _ in range(args.warmup):
-        step()
+        job.step()
     torch.cuda.synchronize(dev)
     if sga.device_status(dev) != 0:
         raise RuntimeError("device status not OK after warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     _barrier(world)
@@ -221,70 +388,80 @@ def run_ours(args):
         torch.cuda._sleep(int(2e6 * (2 + args.steps)))
         t_start.record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            job.step(evs[i], stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
     _barrier(world)
     status = sga.device_status(dev)
     total_ms = _max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    comp_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    stage_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, (name, _) in enumerate(job.stages)}
     clocks = clk.summary()
 
-    flops = layer_flops(cfg, plan.S)
     ms_step = total_ms / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = world * job.flops / (ms_step * 1e-3) / 1e12
     peaks = _peaks()
-    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
-    comp_gbs = compaction_bytes(cfg, plan.S) / (comp_ms * 1e-3) / 1e9
+    d_name, d_bound, d_amount, d_kernel = job.dominant
+    d_ms = stage_ms[d_name]
+    achieved = d_amount / (d_ms * 1e-3) / 1e12
+    fp = _kernel_fingerprint()
+    traffic = TRAFFIC_GB.get(fp, {}).get(args.workload)
+    # the dominant kernel runs back to back for seconds inside the timed steps, so its peak is
+    # the sustained (power-capped) bf16 figure; the burst fraction is given beside it
+    roofline = {"bound": d_bound, "kernel": d_kernel, "achieved": achieved, "peak": peaks["bf16_sus"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sus"],
+                "peak_kind": f"bf16 dense sustained ({peaks['source']})",
+                "frac_of_burst": achieved / peaks["bf16"], "burst_peak": peaks["bf16"],
+                "traffic": traffic * 1e9 if traffic is not None else None,
+                "traffic_unit": "bytes per launch (dram read + write, ncu)", "kernel_fingerprint": fp,
+                "kernel_ms": d_ms}
+    secondary = None
+    if job.secondary is not None:
+        s_name, _, s_bytes, s_kernel = job.secondary
+        s_ms = stage_ms[s_name]
+        gbs = s_bytes / (s_ms * 1e-3) / 1e9
+        secondary = {"kernel": s_kernel, "ms": s_ms, "achieved_gbs": gbs, "bytes": s_bytes,
+                     "frac_hbm": gbs / peaks["hbm"], "frac_8tbs": gbs / 8000.0, "peak_source": peaks["source"]}
 
     e2e = None
     if not args.no_e2e:
-        qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
-        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        host_in = [x.cpu().pin_memory() for x in job.inputs]
+        oh = torch.empty(job.out.shape, dtype=job.out.dtype, pin_memory=True)
         for _ in range(2):
-            sga.layer_from_host(plan, qh, kh, vh, out_host=oh)
+            job.e2e_call(host_in, oh)
         torch.cuda.synchronize(dev)
         _barrier(world)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(args.steps):
-            sga.layer_from_host(plan, qh, kh, vh, out_host=oh)
+            job.e2e_call(host_in, oh)
         b.record(stream)
         torch.cuda.synchronize(dev)
         _barrier(world)
         e_ms = _max_over_ranks(a.elapsed_time(b), world, dev) / args.steps
-        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (qh, kh, vh)),
+        e2e = {"value": world * job.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host_in),
                "d2h_bytes_per_step": oh.numel() * oh.element_size()}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_oracle_sample(cfg, q, k, v)
+        cpu = job.cpu_sample()
 
     if rank != 0:
         return
+    q = job.inputs[0]
+    metric = METRIC if args.workload == "headline" else f"{args.workload}: ms/layer and effective TFLOP/s"
+    config = {"workload": wl["desc"], **job.config,
+              "l2": "inputs larger than L2 (Q %.2f GB); no flush" % (q.numel() * q.element_size() / 1e9)
+              if q.numel() * q.element_size() > 126e6 else "inputs smaller than L2: steady-state, L2-warm",
+              "parallelism": f"dp{world} (independent layers per rank)", "stage_ms": stage_ms}
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": wl["desc"], "B_per_rank": cfg.B, "H": cfg.H, "N": cfg.N, "L": cfg.L, "T": cfg.T,
-                   "S": plan.S, "sigma": cfg.sigma, "flops_per_layer": flops,
-                   "l2": "inputs larger than L2 (Q, K, V %.2f GB each); no flush" % (q.numel() * q.element_size() / 1e9),
-                   "parallelism": f"dp{world} (independent layers per rank)"},
-        "roofline": {"bound": "tensor", "kernel": "sga::tc::attn_tc_kernel", "achieved": attn_tflops,
-                     "peak": peaks["bf16_sus"], "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_sus"],
-                     "peak_kind": f"bf16 dense sustained ({peaks['source']})",
-                     "frac_of_burst": attn_tflops / peaks["bf16"], "traffic": None,
-                     "attention_ms": attn_ms},
-        "compaction": {"ms": comp_ms, "achieved_gbs": comp_gbs, "bytes": compaction_bytes(cfg, plan.S),
-                       "frac_hbm": comp_gbs / peaks["hbm"], "frac_8tbs": comp_gbs / 8000.0,
-                       "peak_source": peaks["source"]},
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
-        "clocks": clocks,
-        "device_status": status,
+        "vs_baseline": None, "dtype": "bf16" if job.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config, "roofline": roofline, "compaction": secondary, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": (n_st + (1 if job.secondary is not None else 0)) * args.steps,
+        "clocks": clocks, "device_status": status,
     }
     print(json.dumps(line), flush=True)
 
@@ -298,6 +475,9 @@ def run_reference(args):
     import subsampled_global_attention_sga_b300 as sga
     from subsampled_global_attention_sga_b300.inputs import correlated_qkv
     wl = WORKLOADS[args.workload]
+    if wl["kind"] != "sga":
+        print(json.dumps({"impl": "reference", "unavailable": "the CPU reference arm covers the SGA workloads"}))
+        return
     cfg = sga.SGAConfig(**wl["cfg"])
     # one (batch, head) of the same workload, generated on the host
     q, k, v = correlated_qkv(1, 1, cfg.N, cfg.L, 64, seed=0, dtype=cfg.torch_dtype, device="cpu")
