@@ -53,6 +53,8 @@ def _load():
         lib.oracle_plan_general.argtypes = [i32] * 10 + [p, i64, p, p, p]
         lib.oracle_biased_attention_rows.restype = None
         lib.oracle_biased_attention_rows.argtypes = [i64, i32, p, p, p, p, i64, f64, p, p]
+        lib.oracle_rope2d.restype = None
+        lib.oracle_rope2d.argtypes = [i64, i32, i64, i32, i32, f64, i32, p, p]
         lib.oracle_num_threads.restype = i32
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -181,6 +183,15 @@ def biased_attention_rows(Qrows, K, V, bias, *, scale=0.125):
     _load().oracle_biased_attention_rows(Tk, d, _ptr(Qrows), _ptr(K), _ptr(V), _ptr(bias), n,
                                          float(scale), _ptr(out), _ptr(lse))
     return out, lse
+
+
+def rope2d(X, L: int, n_special: int, grid_w: int, base: float, pos_offset: int) -> np.ndarray:
+    """2D rotary position embedding of one (batch, head)'s tokens X [T, d] (fp64 result)."""
+    X = _f32(X)
+    T, d = X.shape
+    Y = np.zeros((T, d), dtype=np.float64)
+    _load().oracle_rope2d(T, d, L, n_special, grid_w, float(base), int(pos_offset), _ptr(X), _ptr(Y))
+    return Y
 
 
 def sga_full(p: Plan, Q, K, V, **kw):

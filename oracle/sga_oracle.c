@@ -388,3 +388,40 @@ int64_t oracle_plan_general(int N, int grid_h, int grid_w, int n_special,
     frame_off[N] = (int32_t)n_kept;
     return n_kept;
 }
+
+/* ---------------------------------------------------------------------------------------
+ * 2D rotary position embedding of one (batch, head)'s tokens, the step before the attention:
+ * VGGT re-applies rotary position encoding to Q and K in every layer ("HTTM: Head-wise Temporal
+ * Token Merging for Faster VGGT", blog digest, section 3 "core insight: VGGT's token similarity
+ * patterns", the RoPE architecture effect).  The pages give no frequency convention, so it is
+ * parametrised here (the same reading in the CUDA path):
+ *   dims [0, d/2) rotate by the row position, dims [d/2, d) by the column position;
+ *   within a half of size h = d/2 the pairs (j, j + h/2), j < h/2, rotate by the angle
+ *   pos * base^(-2j/h);
+ *   a patch (r, c) sits at (r + pos_offset, c + pos_offset); the n_special camera/register
+ *   tokens sit at position 0 (no rotation).
+ * X: [T, d] in (fp32), Y: [T, d] out (fp64); T = N * L, L = n_special + grid_h * grid_w.
+ * ------------------------------------------------------------------------------------ */
+void oracle_rope2d(int64_t T, int d, int64_t L, int n_special, int grid_w, double base,
+                   int pos_offset, const float* X, double* Y)
+{
+    const int h = d / 2, q = h / 2;
+    #pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t p = t % L;
+        double pos[2] = {0.0, 0.0};
+        if (p >= n_special) {
+            pos[0] = (double)((p - n_special) / grid_w + pos_offset);   /* row */
+            pos[1] = (double)((p - n_special) % grid_w + pos_offset);   /* column */
+        }
+        for (int a = 0; a < 2; ++a) {
+            for (int j = 0; j < q; ++j) {
+                const double ang = pos[a] * pow(base, -2.0 * j / h);
+                const double x0 = (double)X[t * d + a * h + j];
+                const double x1 = (double)X[t * d + a * h + j + q];
+                Y[t * d + a * h + j] = x0 * cos(ang) - x1 * sin(ang);
+                Y[t * d + a * h + j + q] = x0 * sin(ang) + x1 * cos(ang);
+            }
+        }
+    }
+}

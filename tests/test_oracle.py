@@ -439,3 +439,55 @@ def test_general_plan_per_axis_closed_form_and_page_retention():
         assert p.S - gh * gw == per_axis * per_axis
         # the share of kept patches is close to the page's stated retention
         assert abs(100.0 * per_axis ** 2 / (gh * gw) - pct) < 3.0, (num, den)
+
+
+# ------------------------------------------------------------------------------ 2D RoPE
+def _rope_complex(X, L, nsp, gw, base, off):
+    """The same rotation written with complex numbers: z_j = x_j + i x_{j+q}, z_j * e^{i pos theta_j}."""
+    T, d = X.shape
+    h, q = d // 2, d // 4
+    Y = np.array(X, dtype=np.float64)
+    p = np.arange(T) % L
+    patch = p >= nsp
+    pos = np.zeros((T, 2))
+    pos[patch, 0] = (p[patch] - nsp) // gw + off
+    pos[patch, 1] = (p[patch] - nsp) % gw + off
+    theta = base ** (-2.0 * np.arange(q) / h)
+    for a in range(2):
+        z = X[:, a * h:a * h + q].astype(np.float64) + 1j * X[:, a * h + q:(a + 1) * h].astype(np.float64)
+        z = z * np.exp(1j * pos[:, a:a + 1] * theta[None, :])
+        Y[:, a * h:a * h + q], Y[:, a * h + q:(a + 1) * h] = z.real, z.imag
+    return Y
+
+
+@pytest.mark.parametrize("base,off", [(100.0, 1), (10000.0, 0), (100.0, 3)])
+def test_rope2d_matches_complex_rotation(base, off):
+    N, gh, gw, nsp = 3, 6, 7, 5
+    L = nsp + gh * gw
+    _, k, _ = _qkv(N, L, seed=30)
+    got = oracle.rope2d(k[0], L, nsp, gw, base, off)
+    np.testing.assert_allclose(got, _rope_complex(k[0], L, nsp, gw, base, off), atol=1e-12)
+    # special tokens (position 0) are not rotated; norms are preserved
+    sp = (np.arange(N * L) % L) < nsp
+    np.testing.assert_allclose(got[sp], k[0][sp].astype(np.float64), atol=0)
+    np.testing.assert_allclose(np.linalg.norm(got, axis=1), np.linalg.norm(k[0].astype(np.float64), axis=1),
+                               rtol=1e-12)
+
+
+def test_rope2d_scores_depend_on_relative_position_only():
+    # RoPE's defining property: q(p1) . k(p2) depends only on p1 - p2; shifting every position by
+    # the same amount (a different pos_offset) leaves all patch-patch scores unchanged
+    N, gh, gw, nsp = 2, 5, 6, 5
+    L = nsp + gh * gw
+    q, k, _ = _qkv(N, L, seed=31)
+    patch = (np.arange(N * L) % L) >= nsp
+    s = {}
+    for off in (0, 4):
+        qr = oracle.rope2d(q[0], L, nsp, gw, 100.0, off)[patch]
+        kr = oracle.rope2d(k[0], L, nsp, gw, 100.0, off)[patch]
+        s[off] = qr @ kr.T
+    np.testing.assert_allclose(s[0], s[4], atol=1e-10)
+    # and a sign error in the rotation (a planted mistake) breaks the match with the complex form
+    bad = _rope_complex(k[0], L, nsp, gw, 100.0, 1)
+    bad[:, 16:32] *= -1
+    assert np.abs(oracle.rope2d(k[0], L, nsp, gw, 100.0, 1) - bad).max() > 1e-3
