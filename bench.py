@@ -51,6 +51,14 @@ WORKLOADS = {
                          "per-axis sigma_b = 1.3 with phase shift, frame 0 + special tokens dense, 10 % of "
                          "the tokens protected, diagonal + mean",
                     cfg=dict(B=1, H=16, N=200), general=dict(sigma=(13, 10), phase=True, protected=0.10)),
+    "rope": dict(kind="sga",
+                 desc="SGA layer with fused 2D RoPE (base 100, position offset 1): N=800 frames x 1374 "
+                      "tokens, H=16, d=64, bf16, sigma=4, diag+mean",
+                 cfg=dict(B=1, H=16, N=800, sigma=4, rope=True, rope_base=100.0, rope_pos_offset=1)),
+    "rope_long": dict(kind="sga",
+                      desc="SGA layer with fused 2D RoPE: N=200 frames x 1374 tokens, H=16, d=64, bf16, "
+                           "sigma=9, diag+mean",
+                      cfg=dict(B=1, H=16, N=200, sigma=9, rope=True, rope_base=100.0, rope_pos_offset=1)),
     "merged": dict(kind="bias",
                    desc="size-aware attention: 274,800 queries (200 frames x 1374) against 137,400 merged "
                         "keys standing for 1-3 tokens each (bias ln g), H=16, d=64, bf16",
@@ -325,6 +333,9 @@ class Job:
                 kept[self.kv_index] = 1
                 op = oracle.Plan(T=cfg.T, L=cfg.L, kept=kept, kv_index=self.kv_index,
                                  frame_off=np.searchsorted(self.kv_index, np.arange(cfg.N + 1) * cfg.L).astype(np.int32))
+            if cfg.rope:
+                qh = oracle.rope2d(qh, cfg.L, cfg.n_special, cfg.grid_w, cfg.rope_base, cfg.rope_pos_offset).astype(np.float32)
+                kh = oracle.rope2d(kh, cfg.L, cfg.n_special, cfg.grid_w, cfg.rope_base, cfg.rope_pos_offset).astype(np.float32)
             t0 = time.perf_counter()
             sums = oracle.dropped_sums(op, kh, vh)
             extra_t = time.perf_counter() - t0

@@ -83,6 +83,18 @@ typedef struct {
     int mean_mode;           /* sga_mean_mode */
     int dtype;               /* sga_dtype of Q, K, V, O, K_S, V_S */
     int kernel;              /* sga_kernel */
+    /* 2D rotary position embedding of Q and K, fused into the layer (VGGT re-applies RoPE in
+     * every layer: "HTTM: Head-wise Temporal Token Merging for Faster VGGT", section 3).  The
+     * pages give no convention; the one used: head dims [0, 32) rotate by the row position,
+     * [32, 64) by the column position; in each half the pairs (j, j+16), j < 16, rotate by
+     * pos * rope_base^(-j/16); a patch (r, c) sits at (r + rope_pos_offset, c + rope_pos_offset),
+     * the n_special tokens at position 0 (not rotated).  With rope = 1, sga_compact writes the
+     * rotated kept keys and sums the rotated dropped keys, and sga_forward rotates Q and the
+     * diagonal / leave-one-out keys itself: K and Q in memory stay unrotated.  V is never
+     * rotated. */
+    int rope;                /* 0: off, 1: on */
+    float rope_base;         /* frequency base (> 1) */
+    int rope_pos_offset;     /* >= 0 */
 } sga_config;
 
 typedef struct sga_plan_s* sga_plan_t;   /* opaque */
@@ -189,6 +201,11 @@ sga_status sga_bias_forward(int B, int H, int64_t Tq, int64_t Tk, int head_dim, 
                             const void* Q, const void* K, const void* V, const float* bias, void* O,
                             float* lse, float scale, void* stream);
 
+/* Rotate X [B, H, T, 64] (the plan's shape and dtype) in place with the plan's 2D rotary
+ * embedding (cfg.rope must be 1): for a dense or frame-local layer with RoPE, rotate Q and K with
+ * this call, then call sga_dense_forward / sga_frame_forward.  HBM-bound, one pass. */
+sga_status sga_rope2d(sga_plan_t plan, void* X, void* stream);
+
 /* Compaction that allocates nothing, for callers that cannot call cudaMalloc.  The pages have
  * no counterpart: this entry point exists for integration only.
  *
@@ -205,6 +222,8 @@ sga_status sga_bias_forward(int B, int H, int64_t Tq, int64_t Tk, int head_dim, 
  * sga_plan_info), and k_sum, v_sum (fp32 [B, H, 64]) get the sums of the dropped rows.  All
  * pointers are caller-owned device memory, 16-byte aligned.  No cudaMalloc, cudaFree or other
  * allocating call is made.
+ *
+ * No rotary embedding: a configuration with rope = 1 returns SGA_ERR_UNSUPPORTED.
  *
  * Limit: B * H * ceil(T / 2048) <= 16384 (the scratch holds 2^21 floats, 8 MiB, which every
  * GPU that loads the library keeps until the process exits); larger problems return

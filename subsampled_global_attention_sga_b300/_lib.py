@@ -20,14 +20,15 @@ EXPORTS = (
     "sga_plan_host", "sga_plan_create", "sga_plan_info", "sga_plan_copy_indices", "sga_plan_destroy",
     "sga_compact", "sga_forward", "sga_dense_forward", "sga_frame_forward", "sga_device_status",
     "sga_status_string", "sga_build_info", "sga_compact_noalloc", "sga_bias_forward",
-    "sga_plan_host_general", "sga_plan_create_from_index",
+    "sga_plan_host_general", "sga_plan_create_from_index", "sga_rope2d",
 )
 
 
 class SgaConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "B", "H", "N", "grid_h", "grid_w", "n_special", "head_dim", "s_h", "s_w",
-        "phase_shift", "ref_frame_dense", "diag", "mean", "mean_mode", "dtype", "kernel")]
+        "phase_shift", "ref_frame_dense", "diag", "mean", "mean_mode", "dtype", "kernel", "rope")] + [
+        ("rope_base", ctypes.c_float), ("rope_pos_offset", ctypes.c_int)]
 
 
 class SgaGridSpec(ctypes.Structure):
@@ -75,6 +76,7 @@ def lib():
             "sga_bias_forward": (i32, [i32, i32, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, f32, vp]),
             "sga_plan_host_general": (i32, [ctypes.POINTER(SgaGridSpec), vp, i64, vp, vp, vp, ctypes.POINTER(i64)]),
             "sga_plan_create_from_index": (i32, [cfgp, vp, i64, i32, ctypes.POINTER(vp)]),
+            "sga_rope2d": (i32, [vp, vp, vp]),
             "sga_device_status": (i32, [vp]),
             "sga_status_string": (ctypes.c_char_p, [i32]),
             "sga_build_info": (ctypes.c_char_p, []),

@@ -52,6 +52,9 @@ class SGAConfig:
     dtype: str = "bf16"
     kernel: str = "auto"
     head_dim: int = 64
+    rope: bool = False                  # fused 2D rotary embedding of Q and K
+    rope_base: float = 100.0
+    rope_pos_offset: int = 1
 
     @property
     def L(self) -> int:
@@ -80,6 +83,7 @@ class SGAConfig:
         c.mean_mode = _MEAN_MODES[self.mean_mode]
         c.dtype = _DTYPES[self.dtype][0]
         c.kernel = _KERNELS[self.kernel]
+        c.rope, c.rope_base, c.rope_pos_offset = int(self.rope), float(self.rope_base), int(self.rope_pos_offset)
         return c
 
 
@@ -216,6 +220,14 @@ class Plan:
                                                    _ptr(k_sum), _ptr(v_sum), _ptr(out), _ptr(lse),
                                                    ctypes.c_float(scale), _stream(dev)))
         return out
+
+    def rope2d(self, X):
+        """Rotate X [B, H, T, 64] in place with this plan's 2D rotary embedding."""
+        cfg, dev = self.cfg, self.device
+        _check_tensor("X", X, (cfg.B, cfg.H, self.T, 64), cfg.torch_dtype, dev)
+        with torch.cuda.device(dev):
+            check("sga_rope2d", lib().sga_rope2d(self._h, _ptr(X), _stream(dev)))
+        return X
 
     def layer(self, Q, K, V, out=None, lse=None, scale=None):
         """The whole SGA layer: compaction, then attention."""

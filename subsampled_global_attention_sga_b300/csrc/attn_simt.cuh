@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kSimtRows) attn_simt_kernel(SimtArgs p) {
     float q[64];
     if (valid) {
         load_row64<T>(Qb + row * 64, q);
+        if (p.ex.rope.on) rope_row64(p.ex.rope, row, q);
     } else {
 #pragma unroll
         for (int j = 0; j < 64; ++j) q[j] = 0.f;
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(kSimtRows) attn_simt_kernel(SimtArgs p) {
 
     ExtraRow xr{};
     if (p.ex.on && valid) {
-        xr = extra_logits<T>(p.ex, seg, row, q, p.scale_log2);
+        xr = p.ex.rope.on ? extra_logits<T, true>(p.ex, seg, row, q, p.scale_log2)
+                          : extra_logits<T, false>(p.ex, seg, row, q, p.scale_log2);
         m = fmaxf(xr.s_diag, xr.s_mean);
         if (m != -INFINITY) {
             l = (xr.s_diag == -INFINITY ? 0.f : exp2f(xr.s_diag - m)) +

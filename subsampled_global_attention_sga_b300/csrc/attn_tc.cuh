@@ -67,8 +67,8 @@ constexpr int OFF_QEXT = OFF_V + STAGES * TILE_BYTES;
 constexpr int OFF_KEXT = OFF_QEXT + EXT_BYTES;
 constexpr int OFF_BAR = OFF_KEXT + STAGES * EXT_BYTES;
 // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
-//           p_ready[2], o_done[2], o_free[2], drain
-constexpr int NUM_BARS = 2 + 4 * STAGES + 8 + 1;
+//           p_ready[2], o_done[2], o_free[2], drain, q_rot
+constexpr int NUM_BARS = 2 + 4 * STAGES + 8 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
 
@@ -110,8 +110,9 @@ struct Bars {
     __device__ __forceinline__ uint32_t o_done(int t) const { return base + 16 + 8 * (4 * STAGES + 4 + t); }
     __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (4 * STAGES + 6 + t); }
     __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (4 * STAGES + 8); }
+    __device__ __forceinline__ uint32_t q_rot() const { return base + 16 + 8 * (4 * STAGES + 9); }
 };
-static_assert(16 + 8 * (4 * STAGES + 9) == NUM_BARS * 8, "barrier block size");
+static_assert(16 + 8 * (4 * STAGES + 10) == NUM_BARS * 8, "barrier block size");
 
 // Bounded wait without the abort check: used only to drain work already in flight.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -140,7 +141,7 @@ __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&s)[128]) {
     }
 }
 
-template <bool kBias>
+template <bool kBias, bool kRope>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcArgs p) {
@@ -170,6 +171,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(bars.o_free(t), 128);
         }
         mbar_init(bars.drain(), 1);
+        mbar_init(bars.q_rot(), 256);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
@@ -291,7 +293,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 mma_ts(to, tp + 8 * kk, dv + 128 * kk, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
         };
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-            if (!warp_wait(bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
+            // Q tiles loaded (and, with the rotary embedding, rotated by the softmax warps)
+            if (!warp_wait(kRope ? bars.q_rot() : bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
             {
                 const int st = kv_it % STAGES;
                 if (!warp_wait(bars.k_full(st), (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
@@ -359,12 +362,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const int row = (int)(u % p.n_pairs) * 2 * BM + t * BM + r_in_tile;
             const bool valid = row < p.seg_rows;
 
+            if constexpr (kRope) {
+                // rotate this thread's row of the Q tile in shared memory (128-byte swizzle: the
+                // 16-byte chunk c of row r sits at chunk c ^ (r mod 8)), then release it to the MMA
+                if (!warp_wait(bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
+                if (valid) {
+                    uint8_t* qrow = base + OFF_Q + t * TILE_BYTES + r_in_tile * 128;
+                    float x[64];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(qrow + ((c ^ (r_in_tile & 7)) * 16));
+                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) { x[8 * c + 2 * i] = bf16_lo(ww[i]); x[8 * c + 2 * i + 1] = bf16_hi(ww[i]); }
+                    }
+                    rope_row64(p.ex.rope, row, x);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(qrow + ((c ^ (r_in_tile & 7)) * 16)) =
+                            make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                                       pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                mbar_arrive(bars.q_rot());
+            }
+
             float m = -INFINITY, l = 0.f;
             ExtraRow xr{};
             if (p.ex.on && valid) {
                 float q[64];
                 load_row64<__nv_bfloat16>(p.Q + ((long long)seg * p.seg_rows + row) * 64, q);
-                xr = extra_logits<__nv_bfloat16>(p.ex, seg, row, q, sl2);
+                if (kRope) rope_row64(p.ex.rope, row, q);
+                xr = extra_logits<__nv_bfloat16, kRope>(p.ex, seg, row, q, sl2);
                 m = fmaxf(xr.s_diag, xr.s_mean);
                 if (m != -INFINITY)
                     l = (xr.s_diag == -INFINITY ? 0.f : exp2f(xr.s_diag - m)) +

@@ -12,7 +12,7 @@
 // depend on scheduling.
 #pragma once
 
-#include "common.cuh"
+#include "rope.cuh"
 
 namespace sga {
 
@@ -30,9 +30,35 @@ struct CompactArgs {
     void* KS;
     void* VS;
     float* partials;        // [BH, n_chunks, 128] (64 key sums, then 64 value sums)
+    RopeArgs rope;          // with kRope: keys are rotated before they are stored or summed
 };
 
-template <typename T>
+// 16-byte vector of T <-> its E = 16 / sizeof(T) elements as fp32
+template <typename T> struct Vec16;
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int E = 8;
+    static __device__ __forceinline__ void unpack(const uint4& v, float (&x)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&x)[8]) {
+        return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                          pack_bf16x2(x[6], x[7]));
+    }
+};
+template <> struct Vec16<float> {
+    static constexpr int E = 4;
+    static __device__ __forceinline__ void unpack(const uint4& v, float (&x)[4]) {
+        x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&x)[4]) {
+        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+    }
+};
+
+template <typename T, bool kRope>
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(CompactArgs a) {
     constexpr int kLanesPerRow = 64 * (int)sizeof(T) / 16;     // 8 (bf16) or 16 (fp32)
     constexpr int kRowsPerPass = kCompactThreads / kLanesPerRow;
@@ -56,6 +82,47 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(CompactArgs a)
     const long long r_begin = (long long)chunk * a.rows_per_chunk;
     const long long r_end = (r_begin + a.rows_per_chunk < a.T) ? r_begin + a.rows_per_chunk : a.T;
 
+    if constexpr (kRope) {
+        // rotated keys: the (cos, sin) table in shared memory; every lane takes part in each
+        // row group's shuffles, rows past the chunk end with zeros
+        extern __shared__ float2 rope_s[];
+        for (int i = threadIdx.x; i < a.rope.P * 16; i += kCompactThreads) rope_s[i] = a.rope.tab[i];
+        __syncthreads();
+        using VT = Vec16<T>;
+        for (long long r0 = r_begin; r0 < r_end; r0 += (long long)kRowsPerPass * kCompactUnroll) {
+            uint4 kv[kCompactUnroll], vv[kCompactUnroll];
+            int sl[kCompactUnroll];
+#pragma unroll
+            for (int u = 0; u < kCompactUnroll; ++u) {
+                const long long t = r0 + (long long)u * kRowsPerPass + rsub;
+                sl[u] = -2;
+                kv[u] = make_uint4(0u, 0u, 0u, 0u);
+                vv[u] = kv[u];
+                if (t < r_end) {
+                    sl[u] = __ldg(a.slot + t);
+                    kv[u] = __ldcs(K + t * kLanesPerRow + vec);
+                    vv[u] = __ldcs(V + t * kLanesPerRow + vec);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kCompactUnroll; ++u) {
+                const long long t = r0 + (long long)u * kRowsPerPass + rsub;
+                int pr, pc;
+                rope_pos(a.rope, t < r_end ? t : 0, pr, pc);
+                float xk[kElemsPerVec], xv[kElemsPerVec];
+                VT::unpack(kv[u], xk);
+                rope_lane<kElemsPerVec>(rope_s, pr, pc, vec * kElemsPerVec, xk);
+                if (sl[u] >= 0) {
+                    KS[(long long)sl[u] * kLanesPerRow + vec] = VT::pack(xk);
+                    VS[(long long)sl[u] * kLanesPerRow + vec] = vv[u];
+                } else if (sl[u] == -1) {
+                    VT::unpack(vv[u], xv);
+#pragma unroll
+                    for (int e = 0; e < kElemsPerVec; ++e) { ks[e] += xk[e]; vs[e] += xv[e]; }
+                }
+            }
+        }
+    } else {
     for (long long r0 = r_begin; r0 < r_end; r0 += (long long)kRowsPerPass * kCompactUnroll) {
         uint4 kv[kCompactUnroll], vv[kCompactUnroll];
         int sl[kCompactUnroll];
@@ -93,6 +160,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(CompactArgs a)
                 }
             }
         }
+    }
     }
 
 #pragma unroll

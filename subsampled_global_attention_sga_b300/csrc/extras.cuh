@@ -11,7 +11,7 @@
 // Logits here are in the base-2 domain: s2 = log2(e) * (scale * q.k + ln count).
 #pragma once
 
-#include "common.cuh"
+#include "rope.cuh"
 
 namespace sga {
 
@@ -25,6 +25,7 @@ struct ExtraArgs {
     const void* V;          // [BH, T, 64] full values
     const float* k_sum;     // [BH, 64] sums of the dropped keys
     const float* v_sum;     // [BH, 64] sums of the dropped values
+    RopeArgs rope;          // rope.on: keys (and the caller's q) are rotated; k_sum already is
 };
 
 struct ExtraRow {
@@ -34,8 +35,9 @@ struct ExtraRow {
     float inv_c;    // 1 / count of the mean term
 };
 
-// Logits of the extra components of query row i (token i of pair bh) with query q.
-template <typename T>
+// Logits of the extra components of query row i (token i of pair bh) with query q (already
+// rotated when kRope); with kRope the key row k_i is rotated here (k_sum already is).
+template <typename T, bool kRope = false>
 __device__ __forceinline__ ExtraRow extra_logits(const ExtraArgs& a, int bh, long long i,
                                                  const float (&q)[64], float scale_log2) {
     ExtraRow r;
@@ -48,6 +50,7 @@ __device__ __forceinline__ ExtraRow extra_logits(const ExtraArgs& a, int bh, lon
     if (a.diag && dropped_row) {
         float kk[64];
         load_row64<T>(krow, kk);
+        if (kRope) rope_row64(a.rope, i, kk);
         float s = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) s = fmaf(q[j], kk[j], s);
@@ -59,7 +62,10 @@ __device__ __forceinline__ ExtraRow extra_logits(const ExtraArgs& a, int bh, lon
         if (ci > 0) {
             const float* ks = a.k_sum + (long long)bh * 64;
             float kk[64];
-            if (loo) load_row64<T>(krow, kk);
+            if (loo) {
+                load_row64<T>(krow, kk);
+                if (kRope) rope_row64(a.rope, i, kk);
+            }
             float s = 0.f;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {

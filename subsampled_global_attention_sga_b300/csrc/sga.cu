@@ -23,7 +23,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool init = false;
     int sm_count = 0;
-    bool tc_ready[2] = {false, false};   // attn_tc_kernel<false>, <true> checked and configured
+    bool tc_ready[2][2] = {{false, false}, {false, false}};   // attn_tc_kernel<bias, rope> ready
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -40,6 +40,8 @@ struct sga_plan_s {
     int32_t* d_kv_index;    // [S]
     int32_t* d_frame_off;   // [N+1]
     float* d_partials;      // [B*H, n_chunks, 128]
+    float2* d_rope;         // [rope_P, 16] (cos, sin), or null without the rotary embedding
+    int rope_P;
     std::vector<int32_t> h_kv_index;
     std::vector<int32_t> h_frame_off;
 };
@@ -114,23 +116,24 @@ struct AttnProblem {
     float scale;
     sga::ExtraArgs ex;
     const float* bias;      // per-key natural-log bias [n_seg, kv_rows], or null
+    bool rope;              // rotate Q (and the extras' keys) with ex.rope
 };
 
 // The tensor-core kernel instantiation for a bias setting, checked once per device: its
 // setmaxnreg split assumes exactly LAUNCH_REGS registers per thread at launch (any other count
 // would leave setmaxnreg.inc unsatisfiable), and it needs the large dynamic shared memory.
-template <bool kBias>
+template <bool kBias, bool kRope>
 sga_status prepare_tc(DeviceInfo* di) {
     namespace T = sga::tc;
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (di->tc_ready[kBias]) return SGA_OK;
+    if (di->tc_ready[kBias][kRope]) return SGA_OK;
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias>) != cudaSuccess) return SGA_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias, kRope>) != cudaSuccess) return SGA_ERR_CUDA;
     if (fa.numRegs != (int)T::LAUNCH_REGS) return SGA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias, kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_BYTES) != cudaSuccess)
         return SGA_ERR_CUDA;
-    di->tc_ready[kBias] = true;
+    di->tc_ready[kBias][kRope] = true;
     return SGA_OK;
 }
 
@@ -147,7 +150,10 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         if (pb.dtype != SGA_BF16) return SGA_ERR_UNSUPPORTED;
         if (pb.seg_rows > 0x7FFFFFFFLL || pb.kv_rows > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
         namespace T = sga::tc;
-        if ((st = pb.bias ? prepare_tc<true>(di) : prepare_tc<false>(di)) != SGA_OK) return st;
+        if (pb.bias && pb.rope) return SGA_ERR_UNSUPPORTED;
+        if ((st = pb.bias ? prepare_tc<true, false>(di) : pb.rope ? prepare_tc<false, true>(di)
+                                                               : prepare_tc<false, false>(di)) != SGA_OK)
+            return st;
         CUtensorMap mq, mk, mv;
         if ((st = make_map(&mq, pb.Q, pb.seg_rows, pb.n_seg)) != SGA_OK) return st;
         if ((st = make_map(&mk, pb.Kt, pb.kv_rows, pb.n_seg)) != SGA_OK) return st;
@@ -169,9 +175,11 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.inv_scale = 1.0f / pb.scale;
         const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
         if (pb.bias)
-            T::attn_tc_kernel<true><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+            T::attn_tc_kernel<true, false><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+        else if (pb.rope)
+            T::attn_tc_kernel<false, true><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
         else
-            T::attn_tc_kernel<false><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+            T::attn_tc_kernel<false, false><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
         return launch_status();
     }
     if (kern != SGA_KERNEL_SIMT) return SGA_ERR_INVALID_ARG;
@@ -196,6 +204,21 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
     else
         return SGA_ERR_UNSUPPORTED;
     return launch_status();
+}
+
+sga::RopeArgs rope_args(sga_plan_t plan) {
+    sga::RopeArgs r;
+    std::memset(&r, 0, sizeof(r));
+    if (plan->cfg.rope) {
+        r.on = 1;
+        r.tab = plan->d_rope;
+        r.P = plan->rope_P;
+        r.L = (int)plan->L;
+        r.n_special = plan->cfg.n_special;
+        r.grid_w = plan->cfg.grid_w;
+        r.pos_offset = plan->cfg.rope_pos_offset;
+    }
+    return r;
 }
 
 sga_status check_plan(sga_plan_t plan) {
@@ -261,6 +284,10 @@ sga_status check_config(const sga_config* cfg) {
         c.s_h <= 0 || c.s_w <= 0)
         return SGA_ERR_INVALID_ARG;
     if (c.mean_mode != SGA_MEAN_LOO && c.mean_mode != SGA_MEAN_GLOBAL) return SGA_ERR_INVALID_ARG;
+    if (c.rope != 0 && c.rope != 1) return SGA_ERR_INVALID_ARG;
+    if (c.rope && (!(c.rope_base > 1.0f) || !std::isfinite(c.rope_base) || c.rope_pos_offset < 0 ||
+                   (long long)c.rope_pos_offset + (c.grid_h > c.grid_w ? c.grid_h : c.grid_w) > 4096))
+        return SGA_ERR_INVALID_ARG;
     sga_status st = check_common(c.dtype, c.head_dim, c.kernel);
     if (st != SGA_OK) return st;
     const long long L = (long long)c.n_special + (long long)c.grid_h * c.grid_w;
@@ -313,6 +340,20 @@ sga_status upload_plan(const sga_config& c, const std::vector<int32_t>& slot, co
     plan->d_kv_index = nullptr;
     plan->d_frame_off = nullptr;
     plan->d_partials = nullptr;
+    plan->d_rope = nullptr;
+    plan->rope_P = 0;
+    std::vector<float> rope_tab;
+    if (c.rope) {
+        // positions 0 .. max(grid) - 1 + offset; angle pos * base^(-j/16), computed in double
+        plan->rope_P = (c.grid_h > c.grid_w ? c.grid_h : c.grid_w) + c.rope_pos_offset;
+        rope_tab.resize((size_t)plan->rope_P * 32);
+        for (int pos = 0; pos < plan->rope_P; ++pos)
+            for (int j = 0; j < 16; ++j) {
+                const double ang = pos * std::pow((double)c.rope_base, -2.0 * j / 32.0);
+                rope_tab[(size_t)(pos * 16 + j) * 2] = (float)std::cos(ang);
+                rope_tab[(size_t)(pos * 16 + j) * 2 + 1] = (float)std::sin(ang);
+            }
+    }
 
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
@@ -325,6 +366,11 @@ sga_status upload_plan(const sga_config& c, const std::vector<int32_t>& slot, co
     okc = okc && cudaMalloc(&plan->d_kv_index, sizeof(int32_t) * (size_t)(plan->S > 0 ? plan->S : 1)) == cudaSuccess;
     okc = okc && cudaMalloc(&plan->d_frame_off, sizeof(int32_t) * (size_t)(c.N + 1)) == cudaSuccess;
     okc = okc && cudaMalloc(&plan->d_partials, part_bytes) == cudaSuccess;
+    if (c.rope) {
+        okc = okc && cudaMalloc(&plan->d_rope, sizeof(float) * rope_tab.size()) == cudaSuccess;
+        okc = okc && cudaMemcpy(plan->d_rope, rope_tab.data(), sizeof(float) * rope_tab.size(),
+                                cudaMemcpyHostToDevice) == cudaSuccess;
+    }
     okc = okc && cudaMemcpy(plan->d_slot, slot.data(), sizeof(int32_t) * (size_t)T, cudaMemcpyHostToDevice) == cudaSuccess;
     if (plan->S > 0)
         okc = okc && cudaMemcpy(plan->d_kv_index, kv.data(), sizeof(int32_t) * (size_t)plan->S,
@@ -495,6 +541,7 @@ void sga_plan_destroy(sga_plan_t plan) {
     cudaFree(plan->d_kv_index);
     cudaFree(plan->d_frame_off);
     cudaFree(plan->d_partials);
+    cudaFree(plan->d_rope);
     if (switched) cudaSetDevice(prev);
     plan->magic = 0;
     delete plan;
@@ -522,12 +569,22 @@ sga_status sga_compact(sga_plan_t plan, const void* K, const void* V, void* K_S,
     a.KS = K_S;
     a.VS = V_S;
     a.partials = plan->d_partials;
+    a.rope = rope_args(plan);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     dim3 grid((unsigned)plan->n_chunks, (unsigned)BH);
-    if (c.dtype == SGA_BF16)
-        sga::compact_kernel<__nv_bfloat16><<<grid, sga::kCompactThreads, 0, s>>>(a);
-    else
-        sga::compact_kernel<float><<<grid, sga::kCompactThreads, 0, s>>>(a);
+    const size_t rope_smem = c.rope ? sizeof(float2) * (size_t)plan->rope_P * 16 : 0;
+    if (rope_smem > 48 * 1024) return SGA_ERR_UNSUPPORTED;
+    if (c.dtype == SGA_BF16) {
+        if (c.rope)
+            sga::compact_kernel<__nv_bfloat16, true><<<grid, sga::kCompactThreads, rope_smem, s>>>(a);
+        else
+            sga::compact_kernel<__nv_bfloat16, false><<<grid, sga::kCompactThreads, 0, s>>>(a);
+    } else {
+        if (c.rope)
+            sga::compact_kernel<float, true><<<grid, sga::kCompactThreads, rope_smem, s>>>(a);
+        else
+            sga::compact_kernel<float, false><<<grid, sga::kCompactThreads, 0, s>>>(a);
+    }
     if ((st = launch_status()) != SGA_OK) return st;
     sga::compact_finalize_kernel<<<BH, 128, 0, s>>>(plan->d_partials, plan->n_chunks, k_sum, v_sum);
     return launch_status();
@@ -567,7 +624,9 @@ sga_status sga_forward(sga_plan_t plan, const void* Q, const void* K, const void
     pb.ex.V = V;
     pb.ex.k_sum = k_sum;
     pb.ex.v_sum = v_sum;
+    pb.ex.rope = rope_args(plan);
     pb.bias = nullptr;
+    pb.rope = c.rope != 0;
     return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -593,6 +652,7 @@ static sga_status plain_attention(int n_seg, long long seg_rows, long long kv_ro
     pb.scale = scale;
     pb.ex.on = 0;
     pb.bias = bias;
+    pb.rope = false;
     return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -625,6 +685,25 @@ sga_status sga_bias_forward(int B, int H, int64_t Tq, int64_t Tk, int head_dim, 
     if ((long long)B * H > 0x7FFFFFFFLL || Tq > 0x7FFFFFFFLL || Tk > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(bias) & 3u) != 0) return SGA_ERR_ALIGNMENT;
     return plain_attention(B * H, Tq, Tk, dtype, kernel, Q, K, V, bias, O, lse, scale, stream);
+}
+
+sga_status sga_rope2d(sga_plan_t plan, void* X, void* stream) {
+    sga_status st = check_plan(plan);
+    if (st != SGA_OK) return st;
+    if (!X) return SGA_ERR_INVALID_ARG;
+    if (!aligned16(X)) return SGA_ERR_ALIGNMENT;
+    if (!plan->cfg.rope) return SGA_ERR_INVALID_ARG;
+    const long long rows = (long long)plan->cfg.B * plan->cfg.H * plan->T;
+    const long long blocks = (rows + 255) / 256;
+    if (blocks > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan->cfg.dtype == SGA_BF16)
+        sga::rope2d_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+            reinterpret_cast<__nv_bfloat16*>(X), rows, plan->T, rope_args(plan));
+    else
+        sga::rope2d_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<float*>(X), rows, plan->T,
+                                                                     rope_args(plan));
+    return launch_status();
 }
 
 sga_status sga_device_status(void* stream) {
@@ -695,6 +774,7 @@ extern "C" sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, 
                                           void* V_S, float* k_sum, float* v_sum, void* stream) {
     sga_status st = check_config(cfg);
     if (st != SGA_OK) return st;
+    if (cfg->rope) return SGA_ERR_UNSUPPORTED;
     if (!K || !V || !K_S || !V_S || !k_sum || !v_sum) return SGA_ERR_INVALID_ARG;
     if (!aligned16(K) || !aligned16(V) || !aligned16(K_S) || !aligned16(V_S) || !aligned16(k_sum) ||
         !aligned16(v_sum))

@@ -475,3 +475,107 @@ def test_general_plan_vggt_sampled(dev):
         gots.append(_host(out[0, h])[rows])
         refs.append(ref)
     _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "general sampled")
+
+
+# ------------------------------------------------------------------------------ fused 2D RoPE
+# VGGT re-applies RoPE in every layer ("HTTM ..." section 3); the convention is a parameter.
+def _rope_ref(x, cfg):
+    """Oracle rotation of one (batch, head) [T, 64] tensor, rounded once to fp32 for the oracle's
+    attention routines (relative 6e-8, far below any tolerance here)."""
+    return oracle.rope2d(_host(x), cfg.L, cfg.n_special, cfg.grid_w, cfg.rope_base, cfg.rope_pos_offset).astype(np.float32)
+
+
+@pytest.mark.parametrize("dtype,tdt", [("bf16", torch.bfloat16), ("f32", torch.float32)])
+def test_rope_compaction(dev, dtype, tdt):
+    cfg = sga.SGAConfig(B=1, H=2, N=5, grid_h=11, grid_w=9, sigma=4, phase_shift=True, dtype=dtype, rope=True,
+                        rope_base=100.0, rope_pos_offset=1)
+    _, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=90, dtype=tdt, device=dev)
+    plan = sga.Plan(cfg, dev)
+    K_S, V_S, ks, vs = plan.compact(k, v)
+    torch.cuda.synchronize(dev)
+    op = _oracle_plan(cfg)
+    idx = torch.as_tensor(op.kv_index.astype(np.int64), device=dev)
+    assert torch.equal(V_S, v[:, :, idx])                       # values are never rotated
+    for h in range(2):
+        kr = _rope_ref(k[0, h], cfg)
+        got = _host(K_S[0, h])
+        tol = 1e-6 if dtype == "f32" else 8e-3                      # one bf16 rounding of |x| < 2
+        assert np.abs(got - kr[op.kv_index]).max() <= tol * max(1.0, np.abs(kr).max())
+        rk, _, _ = oracle.dropped_sums(op, kr, _host(v[0, h]))
+        g = ks[0, h].cpu().numpy().astype(np.float64)
+        assert np.abs(g - rk).max() <= 1e-5 * max(1.0, np.abs(rk).max())
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+@pytest.mark.parametrize("sigma,phase,base,off", [(4, False, 100.0, 1), (9, True, 10000.0, 0), (1, False, 100.0, 2)])
+def test_rope_sga_full(dev, kernel, sigma, phase, base, off):
+    cfg = sga.SGAConfig(B=1, H=2, N=6, grid_h=13, grid_w=11, sigma=sigma, phase_shift=phase, kernel=kernel,
+                        rope=True, rope_base=base, rope_pos_offset=off)
+    q, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=91, dtype=torch.bfloat16, device=dev)
+    _, out, lse, _ = _run(cfg, q, k, v, dev, lse=True)
+    op = _oracle_plan(cfg)
+    for h in range(2):
+        ref, rl = oracle.sga_full(op, _rope_ref(q[0, h], cfg), _rope_ref(k[0, h], cfg), _host(v[0, h]))
+        _compare(_host(out[0, h]), ref, "bf16", f"rope h{h}")
+        assert np.abs(lse[0, h].cpu().numpy() - rl).max() < 2e-3
+
+
+def test_rope_sga_f32(dev):
+    cfg = sga.SGAConfig(B=1, H=2, N=4, grid_h=9, grid_w=7, sigma=6, phase_shift=True, dtype="f32", rope=True)
+    q, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=92, dtype=torch.float32, device=dev)
+    _, out, _, _ = _run(cfg, q, k, v, dev)
+    op = _oracle_plan(cfg)
+    for h in range(2):
+        ref, _ = oracle.sga_full(op, _rope_ref(q[0, h], cfg), _rope_ref(k[0, h], cfg), _host(v[0, h]))
+        _compare(_host(out[0, h]), ref, "f32", f"rope f32 h{h}")
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_rope_standalone_dense_and_frame(dev, kernel):
+    cfg = sga.SGAConfig(B=1, H=2, N=3, grid_h=10, grid_w=12, sigma=1, rope=True, rope_base=100.0, rope_pos_offset=1)
+    q, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=93, dtype=torch.bfloat16, device=dev)
+    qr, kr = q.clone(), k.clone()
+    plan = sga.Plan(cfg, dev)
+    plan.rope2d(qr)
+    plan.rope2d(kr)
+    od = sga.dense_forward(qr, kr, v, kernel=kernel)
+    of = sga.frame_forward(qr, kr, v, cfg.N, cfg.L, kernel=kernel)
+    torch.cuda.synchronize(dev)
+    rows = np.arange(cfg.T)
+    for h in range(2):
+        qo, ko = _rope_ref(q[0, h], cfg), _rope_ref(k[0, h], cfg)
+        assert np.abs(_host(qr[0, h]) - qo).max() <= 8e-3 * max(1.0, np.abs(qo).max())
+        ref, _ = oracle.attention_rows(qo, ko, _host(v[0, h]), rows)
+        _compare(_host(od[0, h]), ref, "bf16", "rope dense")
+        ref, _ = oracle.attention_rows(qo, ko, _host(v[0, h]), rows, frame_len=cfg.L)
+        _compare(_host(of[0, h]), ref, "bf16", "rope frame")
+
+
+def test_rope_rejected_where_unsupported(dev):
+    cfg = sga.SGAConfig(B=1, H=1, N=2, grid_h=4, grid_w=4, rope=True)
+    k = torch.zeros((1, 1, cfg.T, 64), dtype=torch.bfloat16, device=dev)
+    _, S = None, sga.plan_host(cfg)[0].shape[0]
+    out = [torch.zeros((1, 1, S, 64), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    sums = [torch.zeros((1, 1, 64), dtype=torch.float32, device=dev) for _ in range(2)]
+    with pytest.raises(sga.SgaError):
+        sga.compact_noalloc(cfg, k, k, *out, *sums)
+    with pytest.raises(sga.SgaError):
+        sga.Plan(sga.SGAConfig(B=1, H=1, N=2, grid_h=4, grid_w=4, rope=True, rope_base=1.0), dev)
+
+
+def test_rope_vggt_sampled(dev):
+    cfg = sga.SGAConfig(B=1, H=16, N=32, sigma=4, rope=True, rope_base=100.0, rope_pos_offset=1)
+    q, k, v = correlated_qkv(1, cfg.H, cfg.N, cfg.L, 64, seed=94, dtype=torch.bfloat16, device=dev)
+    plan = sga.Plan(cfg, dev)
+    out = plan.layer(q, k, v)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    op = _oracle_plan(cfg)
+    gots, refs = [], []
+    for h in range(cfg.H):
+        rows = sample_rows(cfg.T, cfg.L, 256, seed=500 + h, kept=op.kept).numpy()
+        qr, kr = _rope_ref(q[0, h], cfg), _rope_ref(k[0, h], cfg)
+        ref, _ = oracle.sga_rows(op, qr[rows], kr, _host(v[0, h]), rows)
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "rope sampled")

@@ -19,7 +19,7 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "sga.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(sga_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(sga_[a-z_0-9]+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_symbol():
