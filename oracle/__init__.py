@@ -26,9 +26,11 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile ``sga_oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP, no fast-math)."""
+    """Compile ``sga_oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP, no fast-math, no FMA
+    contraction: the fp32 decisions of the token merging use explicit fmaf only)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", _LIB_PATH, _SRC, "-lm"]
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-o", _LIB_PATH,
+               _SRC, "-lm"]
         subprocess.run(cmd, check=True)
     return _LIB_PATH
 
@@ -55,6 +57,8 @@ def _load():
         lib.oracle_biased_attention_rows.argtypes = [i64, i32, p, p, p, p, i64, f64, p, p]
         lib.oracle_rope2d.restype = None
         lib.oracle_rope2d.argtypes = [i64, i32, i64, i32, i32, f64, i32, p, p]
+        lib.oracle_merge_match.restype = i64
+        lib.oracle_merge_match.argtypes = [i32] * 8 + [p, p]
         lib.oracle_num_threads.restype = i32
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -192,6 +196,39 @@ def rope2d(X, L: int, n_special: int, grid_w: int, base: float, pos_offset: int)
     Y = np.zeros((T, d), dtype=np.float64)
     _load().oracle_rope2d(T, d, L, n_special, grid_w, float(base), int(pos_offset), _ptr(X), _ptr(Y))
     return Y
+
+
+def merge_match(X, N, grid_h, grid_w, n_special, n_t, n_s, r_permille):
+    """Head-wise temporal token merging of one (batch, head)'s tokens X [T, d]: match[t] = the
+    destination token a merged source t joins, else -1 (see the C source for the rules)."""
+    X = _f32(X)
+    T, d = X.shape
+    match = np.zeros(T, dtype=np.int32)
+    n = _load().oracle_merge_match(N, grid_h, grid_w, n_special, n_t, n_s, r_permille, d, _ptr(X), _ptr(match))
+    if n < 0:
+        raise ValueError("oracle_merge_match: bad argument")
+    return match
+
+
+def merge_groups(match):
+    """The merged sequence of a match vector: kept tokens (every token that is not a merged
+    source) in token order; returns (kept tokens, group id of every token, group sizes)."""
+    T = len(match)
+    kept = np.nonzero(match < 0)[0]
+    gid = np.full(T, -1, dtype=np.int64)
+    gid[kept] = np.arange(len(kept))
+    srcs = np.nonzero(match >= 0)[0]
+    gid[srcs] = gid[match[srcs]]
+    sizes = np.bincount(gid, minlength=len(kept))
+    return kept, gid, sizes
+
+
+def merge_apply(X, gid, n_groups):
+    """Group means (fp64) of the tokens X [T, d] by group id."""
+    X = np.asarray(X, dtype=np.float64)
+    out = np.zeros((n_groups, X.shape[1]))
+    np.add.at(out, gid, X)
+    return out / np.bincount(gid, minlength=n_groups)[:, None]
 
 
 def sga_full(p: Plan, Q, K, V, **kw):

@@ -425,3 +425,91 @@ void oracle_rope2d(int64_t T, int d, int64_t L, int n_special, int grid_w, doubl
         }
     }
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Head-wise temporal token merging ("HTTM: Head-wise Temporal Token Merging for Faster VGGT",
+ * blog digest, section 2 "core method": head-wise merging, temporal reordering and block-level
+ * merging, first-frame anchoring; "RegimeVGGT ..." Key design 1-2: merged keys carry log g).
+ * One (batch, head), tokens X [T, d] (the keys; the values follow the keys' matching).
+ *
+ * Reading (where the pages leave the details open):
+ *   - frames are grouped in chunks of n_t consecutive frames; a block is the same run of n_s
+ *     consecutive patch tokens (row-major, the last run of a frame may be shorter) in every
+ *     frame of one chunk;
+ *   - in a block, the tokens of the chunk's first frame are the destinations (anchors), the
+ *     tokens of its other frames the sources; special tokens are never merged;
+ *   - each source s is matched to the destination d with the largest cosine similarity (ties:
+ *     the lowest token index); the r = floor(|sources| * r_permille / 1000) sources with the
+ *     largest similarity (ties: lowest token index) are merged into their destination;
+ *   - the cosine is decided in IEEE fp32 with one fixed operation order (the same in the CUDA
+ *     kernel): n_x = sqrt(fma-chain of x_i^2, i = 0..d-1), dot = fma-chain of x_i y_i,
+ *     cos = dot / (n_s * n_d), and 0 when n_s * n_d == 0.
+ * Output: match[t] = destination token of a merged source t, else -1.  Returns the number of
+ * merged sources, or -1 on a bad argument.
+ * ------------------------------------------------------------------------------------ */
+static float cos_f32(const float* x, const float* y, int d, float nx, float ny)
+{
+    float dot = 0.0f;
+    for (int i = 0; i < d; ++i) dot = fmaf(x[i], y[i], dot);
+    const float den = nx * ny;
+    return den == 0.0f ? 0.0f : dot / den;
+}
+
+static float norm_f32(const float* x, int d)
+{
+    float s = 0.0f;
+    for (int i = 0; i < d; ++i) s = fmaf(x[i], x[i], s);
+    return sqrtf(s);
+}
+
+int64_t oracle_merge_match(int N, int grid_h, int grid_w, int n_special, int n_t, int n_s,
+                           int r_permille, int d, const float* X, int32_t* match)
+{
+    if (N <= 0 || grid_h <= 0 || grid_w <= 0 || n_special < 0 || n_t <= 0 || n_s <= 0 ||
+        r_permille < 0 || r_permille > 1000)
+        return -1;
+    const int64_t P = (int64_t)grid_h * grid_w, L = n_special + P, T = (int64_t)N * L;
+    for (int64_t t = 0; t < T; ++t) match[t] = -1;
+    int64_t merged = 0;
+    float* sim = (float*)malloc(sizeof(float) * (size_t)(n_t * n_s));
+    int64_t* best = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_t * n_s));
+    int64_t* src = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_t * n_s));
+    for (int f0 = 0; f0 < N; f0 += n_t) {
+        const int nf = (f0 + n_t <= N) ? n_t : N - f0;
+        for (int64_t w0 = 0; w0 < P; w0 += n_s) {
+            const int64_t ws = (w0 + n_s <= P) ? n_s : P - w0;
+            /* match every source of the block (frames f0+1 .. f0+nf-1) to a destination */
+            int64_t n_src = 0;
+            for (int f = f0 + 1; f < f0 + nf; ++f) {
+                for (int64_t k = 0; k < ws; ++k) {
+                    const int64_t s = (int64_t)f * L + n_special + w0 + k;
+                    const float ns = norm_f32(X + s * d, d);
+                    float bs = -INFINITY;
+                    int64_t bd = -1;
+                    for (int64_t k2 = 0; k2 < ws; ++k2) {
+                        const int64_t dd = (int64_t)f0 * L + n_special + w0 + k2;
+                        const float c = cos_f32(X + s * d, X + dd * d, d, ns, norm_f32(X + dd * d, d));
+                        if (c > bs) { bs = c; bd = dd; }       /* strict: the first maximum wins */
+                    }
+                    src[n_src] = s;
+                    sim[n_src] = bs;
+                    best[n_src] = bd;
+                    ++n_src;
+                }
+            }
+            /* merge the r most similar sources: rank = number of sources ahead of s */
+            const int64_t r = n_src * r_permille / 1000;
+            for (int64_t a = 0; a < n_src; ++a) {
+                int64_t rank = 0;
+                for (int64_t b = 0; b < n_src; ++b)
+                    if (sim[b] > sim[a] || (sim[b] == sim[a] && src[b] < src[a])) ++rank;
+                if (rank < r) {
+                    match[src[a]] = (int32_t)best[a];
+                    ++merged;
+                }
+            }
+        }
+    }
+    free(sim); free(best); free(src);
+    return merged;
+}

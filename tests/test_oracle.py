@@ -491,3 +491,102 @@ def test_rope2d_scores_depend_on_relative_position_only():
     bad = _rope_complex(k[0], L, nsp, gw, 100.0, 1)
     bad[:, 16:32] *= -1
     assert np.abs(oracle.rope2d(k[0], L, nsp, gw, 100.0, 1) - bad).max() > 1e-3
+
+
+# ------------------------------------------------------------------------------ token merging
+# "HTTM: Head-wise Temporal Token Merging for Faster VGGT" section 2 (head-wise matching, temporal
+# blocks, first-frame anchors); merged keys carry log g ("RegimeVGGT ..." Key design 2).
+def _blocks(N, gh, gw, nsp, n_t, n_s):
+    L, P = nsp + gh * gw, gh * gw
+    for f0 in range(0, N, n_t):
+        nf = min(n_t, N - f0)
+        for w0 in range(0, P, n_s):
+            ws = min(n_s, P - w0)
+            dst = [f0 * L + nsp + w0 + k for k in range(ws)]
+            src = [f * L + nsp + w0 + k for f in range(f0 + 1, f0 + nf) for k in range(ws)]
+            yield dst, src
+
+
+def _match_fp64(X, N, gh, gw, nsp, n_t, n_s, r_permille):
+    """An independent fp64 statement of the matching rule (valid where the fp32 decisions are
+    not near-ties)."""
+    Xn = X.astype(np.float64)
+    nrm = np.linalg.norm(Xn, axis=1)
+    match = np.full(len(X), -1)
+    for dst, src in _blocks(N, gh, gw, nsp, n_t, n_s):
+        if not src:
+            continue
+        c = (Xn[src] @ Xn[dst].T) / np.outer(nrm[src], nrm[dst])
+        best = np.array(dst)[np.argmax(c, axis=1)]
+        sim = c.max(axis=1)
+        order = sorted(range(len(src)), key=lambda a: (-sim[a], src[a]))
+        r = len(src) * r_permille // 1000
+        for a in order[:r]:
+            match[src[a]] = best[a]
+    return match
+
+
+def _separated_tokens(N, L, d, rng, nsp, gh, gw, n_t, n_s):
+    """Sources = a destination of their block plus noise of a distinct size each, so every
+    similarity decision is far from a tie."""
+    X = rng.standard_normal((N * L, d)).astype(np.float32)
+    for dst, src in _blocks(N, gh, gw, nsp, n_t, n_s):
+        for i, s in enumerate(src):
+            X[s] = X[dst[rng.integers(len(dst))]] + (0.02 + 0.01 * i) * rng.standard_normal(d).astype(np.float32)
+    return X
+
+
+@pytest.mark.parametrize("n_t,n_s,r", [(4, 8, 500), (3, 13, 250), (2, 5, 1000), (5, 64, 600)])
+def test_merge_match_rule(n_t, n_s, r):
+    N, gh, gw, nsp = 9, 6, 7, 5
+    L = nsp + gh * gw
+    rng = np.random.default_rng(n_t * 100 + n_s)
+    X = _separated_tokens(N, L, 64, rng, nsp, gh, gw, n_t, n_s)
+    m = oracle.merge_match(X, N, gh, gw, nsp, n_t, n_s, r)
+    np.testing.assert_array_equal(m, _match_fp64(X, N, gh, gw, nsp, n_t, n_s, r))
+    p = np.arange(N * L) % L
+    assert np.all(m[p < nsp] == -1)                          # special tokens are never merged
+    f = np.arange(N * L) // L
+    assert np.all(m[f % n_t == 0] == -1)                     # a chunk's first frame anchors
+    assert np.all(m[m >= 0] // L % n_t == 0)                 # ... and receives the sources
+    m0 = oracle.merge_match(X, N, gh, gw, nsp, n_t, n_s, 0)
+    assert np.all(m0 == -1)
+
+
+def test_merge_exact_copies_keep_attention_exact():
+    # every source an exact copy (key and value) of a destination of its block: whichever sources
+    # are merged, mean key/value = the copy and bias ln g, so size-aware attention over the
+    # merged keys equals dense attention over all tokens
+    N, gh, gw, nsp, n_t, n_s = 6, 5, 6, 5, 3, 7
+    L = nsp + gh * gw
+    rng = np.random.default_rng(3)
+    q, k, v = _qkv(N, L, seed=33)
+    k, v = k[0].copy(), v[0].copy()
+    for dst, src in _blocks(N, gh, gw, nsp, n_t, n_s):
+        for s in src:
+            j = dst[rng.integers(len(dst))]
+            k[s], v[s] = k[j], v[j]
+    m = oracle.merge_match(k, N, gh, gw, nsp, n_t, n_s, 700)
+    assert (m >= 0).sum() > 0
+    kept, gid, sizes = oracle.merge_groups(m)
+    km, vm = oracle.merge_apply(k, gid, len(kept)), oracle.merge_apply(v, gid, len(kept))
+    out, _ = oracle.biased_attention_rows(q[0], km, vm, np.log(sizes))
+    np.testing.assert_allclose(out, _sdpa(q[0], k, v), atol=1e-12)
+    # without the ln g bias the merged attention is wrong (the bias is what keeps it exact)
+    bad, _ = oracle.biased_attention_rows(q[0], km, vm, np.zeros(len(kept)))
+    assert np.abs(bad - out).max() > 1e-4
+
+
+def test_merge_groups_and_unmerge():
+    N, gh, gw, nsp, n_t, n_s = 5, 4, 5, 5, 2, 6
+    L = nsp + gh * gw
+    X = _separated_tokens(N, L, 64, np.random.default_rng(5), nsp, gh, gw, n_t, n_s)
+    m = oracle.merge_match(X, N, gh, gw, nsp, n_t, n_s, 800)
+    kept, gid, sizes = oracle.merge_groups(m)
+    assert sizes.sum() == N * L and np.all(sizes >= 1)
+    # unmerging a per-group quantity copies it to every member: group means of group means
+    means = oracle.merge_apply(X, gid, len(kept))
+    np.testing.assert_allclose(oracle.merge_apply(means[gid], gid, len(kept)), means, atol=1e-12)
+    for t in range(N * L):
+        members = np.nonzero(gid == gid[t])[0]
+        np.testing.assert_allclose(means[gid[t]], X[members].astype(np.float64).mean(axis=0), atol=1e-12)
