@@ -59,6 +59,12 @@ WORKLOADS = {
                       desc="SGA layer with fused 2D RoPE: N=200 frames x 1374 tokens, H=16, d=64, bf16, "
                            "sigma=9, diag+mean",
                       cfg=dict(B=1, H=16, N=200, sigma=9, rope=True, rope_base=100.0, rope_pos_offset=1)),
+    "httm": dict(kind="merge",
+                 desc="head-wise temporal token merging (HTTM-style): 200 frames x 1374 tokens, H=16, d=64, "
+                      "bf16; keys/values merged per head in blocks of 4 frames x 37 patches, 50 % of the "
+                      "sources merged into the first frame of the chunk, then size-aware attention (ln g) "
+                      "of all 274,800 queries over the merged keys",
+                 mcfg=dict(B=1, H=16, N=200, n_t=4, n_s=37, r_permille=500)),
     "merged": dict(kind="bias",
                    desc="size-aware attention: 274,800 queries (200 frames x 1374) against 137,400 merged "
                         "keys standing for 1-3 tokens each (bias ln g), H=16, d=64, bf16",
@@ -78,6 +84,8 @@ KERNEL_SOURCES = ("subsampled_global_attention_sga_b300/csrc/attn_tc.cuh",
 TRAFFIC_GB = {
     # attn_tc_kernel<false> on the 800-frame sigma = 4 layer: 379.49 GB read + 2.71 GB written
     "40917419ae2423cb": {"headline": 382.20},
+    # after the size-aware and rotary variants were added (same main path): 304.64 + 2.71 GB
+    "585bb52597cd6808": {"headline": 307.35},
 }
 
 
@@ -271,6 +279,24 @@ class Job:
             self.secondary = None
             self.dtype = "bf16"
             self.config = {"H": H, "Tq": Tq, "Tk": Tk, "flops_per_layer": self.flops}
+        elif self.kind == "merge":
+            mc = sga.MergeConfig(**wl["mcfg"])
+            L = mc.n_special + mc.grid_h * mc.grid_w
+            q, k, v = correlated_qkv(mc.B, mc.H, mc.N, L, 64, seed=seed, dtype=torch.bfloat16, device=dev)
+            M = sga.merge_size(mc)
+            bufs = sga.merge(mc, k, v)
+            self.mcfg, self.inputs = mc, (q, k, v)
+            self.out = torch.empty_like(q)
+            out = self.out
+            self.stages = [("merge", lambda: sga.merge(mc, k, v, out=bufs)),
+                           ("attention", lambda: sga.bias_forward(q, bufs[0], bufs[1], bufs[2], out=out))]
+            self.flops = 4.0 * mc.T * M * 64 * mc.H * mc.B
+            self.dominant = ("attention", "tensor", self.flops, "sga::tc::attn_tc_kernel<true, false>")
+            self.secondary = None
+            self.merge_stage = True
+            self.dtype = "bf16"
+            self.config = {"H": mc.H, "N": mc.N, "T": mc.T, "M": M, "n_t": mc.n_t, "n_s": mc.n_s,
+                           "r_permille": mc.r_permille, "flops_per_layer": self.flops}
         else:
             sh = wl["shape"]
             H, N, L = sh["H"], sh["N"], sh["L"]
@@ -302,6 +328,10 @@ class Job:
         sga, dev = self.sga, self.dev
         if self.kind == "sga":
             return sga.layer_from_host(self.plan, *host_in, out_host=out_host)
+        if self.kind == "merge":
+            q, k, v = [x.to(dev, non_blocking=True) for x in host_in]
+            out_host.copy_(sga.merged_attention(self.mcfg, q, k, v), non_blocking=True)
+            return out_host
         dev_in = [x.to(dev, non_blocking=True) for x in host_in]
         if self.kind == "bias":
             o = sga.bias_forward(*dev_in)
@@ -342,6 +372,17 @@ class Job:
             n_keys = op.S + (2 if (cfg.diag or cfg.mean) else 0)
             run = lambda rows: oracle.sga_rows(op, qh[rows], kh, vh, rows, diag=cfg.diag, mean=cfg.mean, sums=sums)
             L = cfg.L
+        elif kind == "merge":
+            mc = self.mcfg
+            t0 = time.perf_counter()
+            m = oracle.merge_match(kh, mc.N, mc.grid_h, mc.grid_w, mc.n_special, mc.n_t, mc.n_s, mc.r_permille)
+            kept, gid, sizes = oracle.merge_groups(m)
+            km, vm = oracle.merge_apply(kh, gid, len(kept)), oracle.merge_apply(vh, gid, len(kept))
+            extra_t = time.perf_counter() - t0
+            b = np.log(sizes)
+            n_keys = len(kept)
+            run = lambda rows: oracle.biased_attention_rows(qh[rows], km, vm, b)
+            L = mc.n_special + mc.grid_h * mc.grid_w
         elif kind == "bias":
             b = self.inputs[3][0, h].double().cpu().numpy()
             n_keys = kh.shape[0]
@@ -427,6 +468,8 @@ def run_ours(args):
                 "traffic_unit": "bytes per launch (dram read + write, ncu)", "kernel_fingerprint": fp,
                 "kernel_ms": d_ms}
     secondary = None
+    if "merge" in stage_ms:
+        secondary = {"kernel": "sga::merge_kernel<bf16>", "ms": stage_ms["merge"]}
     if job.secondary is not None:
         s_name, _, s_bytes, s_kernel = job.secondary
         s_ms = stage_ms[s_name]

@@ -206,6 +206,40 @@ sga_status sga_bias_forward(int B, int H, int64_t Tq, int64_t Tk, int head_dim, 
  * this call, then call sga_dense_forward / sga_frame_forward.  HBM-bound, one pass. */
 sga_status sga_rope2d(sga_plan_t plan, void* X, void* stream);
 
+/* Head-wise temporal token merging ("HTTM: Head-wise Temporal Token Merging for Faster VGGT",
+ * section 2; "RegimeVGGT ..." Key designs 1-2).  Every (batch, head) merges its own tokens:
+ *   - frames are grouped in chunks of n_t; a block is the run of n_s consecutive patch tokens
+ *     (row-major; the last run of a frame may be shorter) in every frame of one chunk;
+ *     n_t * min(n_s, grid_h*grid_w) <= 512;
+ *   - the chunk's first frame holds the destinations (first-frame anchoring), the other frames
+ *     the sources; special tokens are never merged;
+ *   - each source joins the destination of its block with the largest cosine similarity of X
+ *     (first maximum), and the floor(#sources * r_permille / 1000) most similar sources of the
+ *     block are merged (ties: lower token index); the cosine is decided in IEEE fp32 with one
+ *     fixed order (fma chains over the 64 dims, correctly rounded sqrt and division);
+ *   - a merged token is the mean of its members; Y (values) follows X's matching.
+ * The merged sequence (M tokens per (b, h), sga_merge_size) is block-major: for each chunk its
+ * special tokens, then each window's kept tokens (destinations and unmerged sources), in token
+ * order.  map[t] is the merged index that token t belongs to, log_g (nullable) the natural log
+ * of each merged token's group size -- the bias of sga_bias_forward (size-aware attention).
+ * X [B, H, N*L, 64]; Y nullable (then Y_m must be null); X_m, Y_m [B, H, M, 64];
+ * log_g fp32 [B, H, M]; map int32 [B, H, N*L]. */
+typedef struct {
+    int B, H, N, grid_h, grid_w, n_special, head_dim;
+    int n_t;                 /* frames per chunk (temporal block depth) */
+    int n_s;                 /* patch tokens per spatial run */
+    int r_permille;          /* share of a block's sources merged, in 1/1000 */
+    int dtype;               /* sga_dtype */
+} sga_merge_config;
+
+sga_status sga_merge_size(const sga_merge_config* cfg, int64_t* M);
+sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, void* X_m, void* Y_m,
+                     float* log_g, int32_t* map, void* stream);
+
+/* Unmerge: Y[b, h, t] = Y_m[b, h, map[b, h, t]] -- every token receives the output of the
+ * merged token it belongs to (merged queries' attention outputs copied back). */
+sga_status sga_unmerge(const sga_merge_config* cfg, const int32_t* map, const void* Y_m, void* Y, void* stream);
+
 /* Compaction that allocates nothing, for callers that cannot call cudaMalloc.  The pages have
  * no counterpart: this entry point exists for integration only.
  *

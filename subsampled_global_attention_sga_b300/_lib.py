@@ -21,6 +21,7 @@ EXPORTS = (
     "sga_compact", "sga_forward", "sga_dense_forward", "sga_frame_forward", "sga_device_status",
     "sga_status_string", "sga_build_info", "sga_compact_noalloc", "sga_bias_forward",
     "sga_plan_host_general", "sga_plan_create_from_index", "sga_rope2d",
+    "sga_merge_size", "sga_merge", "sga_unmerge",
 )
 
 
@@ -35,6 +36,11 @@ class SgaGridSpec(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "N", "grid_h", "grid_w", "n_special", "sh_num", "sh_den", "sw_num", "sw_den",
         "phase_shift", "ref_frame_dense")]
+
+
+class SgaMergeConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "B", "H", "N", "grid_h", "grid_w", "n_special", "head_dim", "n_t", "n_s", "r_permille", "dtype")]
 
 
 class SgaError(RuntimeError):
@@ -77,6 +83,9 @@ def lib():
             "sga_plan_host_general": (i32, [ctypes.POINTER(SgaGridSpec), vp, i64, vp, vp, vp, ctypes.POINTER(i64)]),
             "sga_plan_create_from_index": (i32, [cfgp, vp, i64, i32, ctypes.POINTER(vp)]),
             "sga_rope2d": (i32, [vp, vp, vp]),
+            "sga_merge_size": (i32, [ctypes.POINTER(SgaMergeConfig), ctypes.POINTER(i64)]),
+            "sga_merge": (i32, [ctypes.POINTER(SgaMergeConfig), vp, vp, vp, vp, vp, vp, vp]),
+            "sga_unmerge": (i32, [ctypes.POINTER(SgaMergeConfig), vp, vp, vp, vp]),
             "sga_device_status": (i32, [vp]),
             "sga_status_string": (ctypes.c_char_p, [i32]),
             "sga_build_info": (ctypes.c_char_p, []),

@@ -15,7 +15,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import SgaConfig, SgaGridSpec, check, lib
+from ._lib import SgaConfig, SgaGridSpec, SgaMergeConfig, check, lib
 
 # sigma -> (s_h, s_w): "AVGGT: Rethinking Global Attention for Accelerating VGGT", Key design 2
 # (sigma = s_h * s_w; 2 -> (1,2), 4 -> (2,2), 6 -> (2,3), 9 -> (3,3)); sigma = 1 keeps every key.
@@ -311,6 +311,95 @@ def bias_forward(Q, K, V, bias, *, dtype="bf16", kernel="auto", out=None, lse=No
                                                          _ptr(Q), _ptr(K), _ptr(V), _ptr(bias), _ptr(out),
                                                          _ptr(lse), ctypes.c_float(scale), _stream(dev)))
     return out
+
+
+@dataclass
+class MergeConfig:
+    """Head-wise temporal token merging ("HTTM ..." section 2): chunks of n_t frames, runs of n_s
+    patch tokens, r_permille of each block's sources merged into the chunk's first frame."""
+    B: int
+    H: int
+    N: int
+    grid_h: int = 37
+    grid_w: int = 37
+    n_special: int = 5
+    n_t: int = 4
+    n_s: int = 37
+    r_permille: int = 500
+    dtype: str = "bf16"
+
+    @property
+    def T(self) -> int:
+        return self.N * (self.n_special + self.grid_h * self.grid_w)
+
+    def to_c(self) -> SgaMergeConfig:
+        c = SgaMergeConfig()
+        c.B, c.H, c.N, c.grid_h, c.grid_w, c.n_special = self.B, self.H, self.N, self.grid_h, self.grid_w, self.n_special
+        c.head_dim, c.n_t, c.n_s, c.r_permille = 64, self.n_t, self.n_s, self.r_permille
+        c.dtype = _DTYPES[self.dtype][0]
+        return c
+
+
+def merge_size(mcfg: MergeConfig) -> int:
+    """Merged tokens per (batch, head)."""
+    c = mcfg.to_c()
+    m = ctypes.c_int64(0)
+    check("sga_merge_size", lib().sga_merge_size(ctypes.byref(c), ctypes.byref(m)))
+    return m.value
+
+
+def merge(mcfg: MergeConfig, X, Y=None, out=None):
+    """Merge X [B, H, T, 64] (matched by its own cosine similarity) and Y (following X's match):
+    returns (X_m, Y_m or None, log_g [B, H, M], map [B, H, T]); ``out`` may hold those four."""
+    dev = X.device
+    tdt = _DTYPES[mcfg.dtype][1]
+    shp = (mcfg.B, mcfg.H, mcfg.T, 64)
+    _check_tensor("X", X, shp, tdt, dev)
+    if Y is not None:
+        _check_tensor("Y", Y, shp, tdt, dev)
+    M = merge_size(mcfg)
+    if out is None:
+        Xm = torch.empty((mcfg.B, mcfg.H, M, 64), dtype=tdt, device=dev)
+        Ym = torch.empty_like(Xm) if Y is not None else None
+        log_g = torch.empty((mcfg.B, mcfg.H, M), dtype=torch.float32, device=dev)
+        mp = torch.empty((mcfg.B, mcfg.H, mcfg.T), dtype=torch.int32, device=dev)
+    else:
+        Xm, Ym, log_g, mp = out
+        _check_tensor("X_m", Xm, (mcfg.B, mcfg.H, M, 64), tdt, dev)
+        if Y is not None:
+            _check_tensor("Y_m", Ym, (mcfg.B, mcfg.H, M, 64), tdt, dev)
+        _check_tensor("log_g", log_g, (mcfg.B, mcfg.H, M), torch.float32, dev)
+        _check_tensor("map", mp, (mcfg.B, mcfg.H, mcfg.T), torch.int32, dev)
+    c = mcfg.to_c()
+    with torch.cuda.device(dev):
+        check("sga_merge", lib().sga_merge(ctypes.byref(c), _ptr(X), _ptr(Y), _ptr(Xm), _ptr(Ym), _ptr(log_g),
+                                           _ptr(mp), _stream(dev)))
+    return Xm, Ym, log_g, mp
+
+
+def unmerge(mcfg: MergeConfig, mp, Ym, out=None):
+    """Every token receives the row of the merged token it belongs to: out[..., t, :] = Ym[..., map[t], :]."""
+    dev = Ym.device
+    tdt = _DTYPES[mcfg.dtype][1]
+    out = torch.empty((mcfg.B, mcfg.H, mcfg.T, 64), dtype=tdt, device=dev) if out is None else out
+    _check_tensor("out", out, (mcfg.B, mcfg.H, mcfg.T, 64), tdt, dev)
+    _check_tensor("map", mp, (mcfg.B, mcfg.H, mcfg.T), torch.int32, dev)
+    c = mcfg.to_c()
+    with torch.cuda.device(dev):
+        check("sga_unmerge", lib().sga_unmerge(ctypes.byref(c), _ptr(mp), _ptr(Ym), _ptr(out), _stream(dev)))
+    return out
+
+
+def merged_attention(mcfg: MergeConfig, Q, K, V, *, merge_queries=False, scale=None):
+    """Attention over head-wise merged keys/values with the ln g size bias ("HTTM ..." section 2,
+    "RegimeVGGT ..." Key design 2).  With merge_queries, queries are merged by their own
+    similarity and the merged outputs are copied back to every query (unmerge)."""
+    Km, Vm, log_g, _ = merge(mcfg, K, V)
+    if not merge_queries:
+        return bias_forward(Q, Km, Vm, log_g, dtype=mcfg.dtype, scale=scale)
+    Qm, _, _, mq = merge(mcfg, Q)
+    Om = bias_forward(Qm, Km, Vm, log_g, dtype=mcfg.dtype, scale=scale)
+    return unmerge(mcfg, mq, Om)
 
 
 def device_status(device=None) -> int:

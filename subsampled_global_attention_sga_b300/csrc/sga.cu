@@ -13,6 +13,8 @@
 #include "attn_tc.cuh"
 #include "compact.cuh"
 #include "compact_noalloc.cuh"
+#include "merge.cuh"
+#include "rope.cuh"
 
 namespace {
 
@@ -703,6 +705,112 @@ sga_status sga_rope2d(sga_plan_t plan, void* X, void* stream) {
     else
         sga::rope2d_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<float*>(X), rows, plan->T,
                                                                      rope_args(plan));
+    return launch_status();
+}
+
+}  // extern "C"
+
+namespace {
+
+sga_status merge_geom(const sga_merge_config* c, sga::MergeGeom* g) {
+    if (!c) return SGA_ERR_INVALID_ARG;
+    if (c->B <= 0 || c->H <= 0 || c->N <= 0 || c->grid_h <= 0 || c->grid_w <= 0 || c->n_special < 0 ||
+        c->n_t <= 0 || c->n_s <= 0 || c->r_permille < 0 || c->r_permille > 1000)
+        return SGA_ERR_INVALID_ARG;
+    if (c->head_dim != 64) return SGA_ERR_UNSUPPORTED;
+    if (c->dtype != SGA_BF16 && c->dtype != SGA_F32) return SGA_ERR_UNSUPPORTED;
+    const long long P = (long long)c->grid_h * c->grid_w, L = c->n_special + P;
+    if (L * c->N > 0x7FFFFFFFLL || (long long)c->n_t * (c->n_s < P ? c->n_s : P) > sga::kMergeMaxBlock)
+        return SGA_ERR_UNSUPPORTED;
+    g->N = c->N;
+    g->L = (int)L;
+    g->P = (int)P;
+    g->n_special = c->n_special;
+    g->n_t = c->n_t;
+    g->n_s = (int)(c->n_s < P ? c->n_s : P);
+    g->r_permille = c->r_permille;
+    g->n_chunks = (c->N + c->n_t - 1) / c->n_t;
+    g->n_windows = (int)((P + g->n_s - 1) / g->n_s);
+    g->T = L * c->N;
+    const int nf_last = c->N - (g->n_chunks - 1) * c->n_t;
+    g->M = (long long)(g->n_chunks - 1) * sga::merge_chunk_size(*g, c->n_t) + sga::merge_chunk_size(*g, nf_last);
+    if ((long long)c->B * c->H > 65535 || g->n_chunks > 65535) return SGA_ERR_UNSUPPORTED;
+    return SGA_OK;
+}
+
+bool g_merge_smem_set[kMaxDevices][2];
+
+}  // namespace
+
+extern "C" {
+
+sga_status sga_merge_size(const sga_merge_config* cfg, int64_t* M) {
+    sga::MergeGeom g;
+    sga_status st = merge_geom(cfg, &g);
+    if (st != SGA_OK) return st;
+    if (!M) return SGA_ERR_INVALID_ARG;
+    *M = g.M;
+    return SGA_OK;
+}
+
+sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, void* X_m, void* Y_m,
+                     float* log_g, int32_t* map, void* stream) {
+    sga::MergeGeom g;
+    sga_status st = merge_geom(cfg, &g);
+    if (st != SGA_OK) return st;
+    if (!X || !X_m || !map || (Y != nullptr) != (Y_m != nullptr)) return SGA_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(X_m) || (Y && (!aligned16(Y) || !aligned16(Y_m))) ||
+        (reinterpret_cast<uintptr_t>(map) & 3u) || (reinterpret_cast<uintptr_t>(log_g) & 3u))
+        return SGA_ERR_ALIGNMENT;
+    int dev;
+    if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_INVALID_ARG;
+    const int di = cfg->dtype == SGA_BF16 ? 0 : 1;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!g_merge_smem_set[dev][di]) {
+            const cudaError_t e = di == 0 ? cudaFuncSetAttribute(sga::merge_kernel<__nv_bfloat16>,
+                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                 sga::kMergeSmemBytes)
+                                          : cudaFuncSetAttribute(sga::merge_kernel<float>,
+                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                 sga::kMergeSmemBytes);
+            if (e != cudaSuccess) return SGA_ERR_CUDA;
+            g_merge_smem_set[dev][di] = true;
+        }
+    }
+    sga::MergeArgs a;
+    a.g = g;
+    a.X = X;
+    a.Y = Y;
+    a.Xm = X_m;
+    a.Ym = Y_m;
+    a.log_g = log_g;
+    a.map = map;
+    dim3 grid((unsigned)g.n_windows + 1, (unsigned)g.n_chunks, (unsigned)(cfg->B * cfg->H));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (di == 0)
+        sga::merge_kernel<__nv_bfloat16><<<grid, sga::kMergeThreads, sga::kMergeSmemBytes, s>>>(a);
+    else
+        sga::merge_kernel<float><<<grid, sga::kMergeThreads, sga::kMergeSmemBytes, s>>>(a);
+    return launch_status();
+}
+
+sga_status sga_unmerge(const sga_merge_config* cfg, const int32_t* map, const void* Y_m, void* Y, void* stream) {
+    sga::MergeGeom g;
+    sga_status st = merge_geom(cfg, &g);
+    if (st != SGA_OK) return st;
+    if (!map || !Y_m || !Y) return SGA_ERR_INVALID_ARG;
+    if (!aligned16(Y_m) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(map) & 3u)) return SGA_ERR_ALIGNMENT;
+    const long long rows = (long long)cfg->B * cfg->H * g.T;
+    const int vec = cfg->dtype == SGA_BF16 ? 8 : 16;
+    const long long blocks = (rows * vec + 255) / 256;
+    if (blocks > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cfg->dtype == SGA_BF16)
+        sga::unmerge_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(map, Y_m, Y, g.T, g.M, rows);
+    else
+        sga::unmerge_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(map, Y_m, Y, g.T, g.M, rows);
     return launch_status();
 }
 

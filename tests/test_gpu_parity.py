@@ -579,3 +579,83 @@ def test_rope_vggt_sampled(dev):
         gots.append(_host(out[0, h])[rows])
         refs.append(ref)
     _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "rope sampled")
+
+
+# ------------------------------------------------------------------------------ token merging
+# "HTTM ..." section 2 (head-wise temporal merging, first-frame anchors, unmerge); merged keys
+# carry ln g ("RegimeVGGT ..." Key design 2).
+def _merge_check(mc, X, Y, Xm, Ym, lg, mp, b, h):
+    """The GPU's grouping equals the oracle's bit for bit; merged rows are the group means."""
+    m_or = oracle.merge_match(_host(X[b, h]), mc.N, mc.grid_h, mc.grid_w, mc.n_special, mc.n_t,
+                              min(mc.n_s, mc.grid_h * mc.grid_w), mc.r_permille)
+    kept, gid, sizes = oracle.merge_groups(m_or)
+    g = mp[b, h].cpu().numpy().astype(np.int64)
+    pairs = set(zip(gid.tolist(), g.tolist()))
+    assert len(pairs) == len(kept) == len(set(g.tolist())) == Xm.shape[2], "partitions differ"
+    perm = np.zeros(len(kept), dtype=np.int64)            # oracle group -> GPU merged row
+    perm[gid] = g
+    ref = oracle.merge_apply(_host(X[b, h]), gid, len(kept))
+    _compare(_host(Xm[b, h])[perm], ref, mc.dtype, "merged X")
+    if Y is not None:
+        _compare(_host(Ym[b, h])[perm], oracle.merge_apply(_host(Y[b, h]), gid, len(kept)), mc.dtype, "merged Y")
+    np.testing.assert_allclose(lg[b, h].cpu().numpy()[perm], np.log(sizes), atol=1e-6)
+    return kept, gid, sizes, perm
+
+
+@pytest.mark.parametrize("dtype,tdt", [("bf16", torch.bfloat16), ("f32", torch.float32)])
+@pytest.mark.parametrize("n_t,n_s,r", [(4, 8, 500), (3, 13, 1000), (2, 64, 250)])
+def test_merge_matches_oracle(dev, dtype, tdt, n_t, n_s, r):
+    mc = sga.MergeConfig(B=2, H=2, N=9, grid_h=6, grid_w=7, n_t=n_t, n_s=n_s, r_permille=r, dtype=dtype)
+    _, k, v = correlated_qkv(2, 2, mc.N, mc.n_special + mc.grid_h * mc.grid_w, 64, seed=100 + n_s, dtype=tdt,
+                             device=dev)
+    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    for b in range(2):
+        for h in range(2):
+            _merge_check(mc, k, v, Km, Vm, lg, mp, b, h)
+
+
+@pytest.mark.parametrize("merge_queries", [False, True])
+def test_merged_attention(dev, merge_queries):
+    mc = sga.MergeConfig(B=1, H=2, N=8, grid_h=9, grid_w=10, n_t=4, n_s=10, r_permille=600)
+    L = mc.n_special + mc.grid_h * mc.grid_w
+    q, k, v = correlated_qkv(1, 2, mc.N, L, 64, seed=110, dtype=torch.bfloat16, device=dev)
+    out = sga.merged_attention(mc, q, k, v, merge_queries=merge_queries)
+    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    torch.cuda.synchronize(dev)
+    for h in range(2):
+        kept, gid, sizes, _ = _merge_check(mc, k, v, Km, Vm, lg, mp, 0, h)
+        km = oracle.merge_apply(_host(k[0, h]), gid, len(kept))
+        vm = oracle.merge_apply(_host(v[0, h]), gid, len(kept))
+        if merge_queries:
+            mq = oracle.merge_match(_host(q[0, h]), mc.N, mc.grid_h, mc.grid_w, mc.n_special, mc.n_t, mc.n_s,
+                                    mc.r_permille)
+            qk, qgid, _ = oracle.merge_groups(mq)
+            qm = oracle.merge_apply(_host(q[0, h]), qgid, len(qk))
+            om, _ = oracle.biased_attention_rows(qm, km, vm, np.log(sizes))
+            ref = om[qgid]                                  # unmerge: every query gets its group's row
+        else:
+            ref, _ = oracle.biased_attention_rows(_host(q[0, h]), km, vm, np.log(sizes))
+        _compare(_host(out[0, h]), ref, "bf16", f"merged attention h{h}")
+
+
+def test_merge_vggt_sampled(dev):
+    # 32 VGGT frames, chunks of 4 frames, one patch row per run, half of the sources merged
+    mc = sga.MergeConfig(B=1, H=16, N=32, n_t=4, n_s=37, r_permille=500)
+    L = 1374
+    q, k, v = correlated_qkv(1, mc.H, mc.N, L, 64, seed=120, dtype=torch.bfloat16, device=dev)
+    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    out = sga.bias_forward(q, Km, Vm, lg)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    gots, refs = [], []
+    for h in range(mc.H):
+        kept, gid, sizes, _ = _merge_check(mc, k, v, Km, Vm, lg, mp, 0, h)
+        km = oracle.merge_apply(_host(k[0, h]), gid, len(kept))
+        vm = oracle.merge_apply(_host(v[0, h]), gid, len(kept))
+        rows = sample_rows(mc.T, L, 128, seed=600 + h).numpy()
+        ref, _ = oracle.biased_attention_rows(_host(q[0, h])[rows], km, vm, np.log(sizes))
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "merged sampled")

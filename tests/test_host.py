@@ -139,3 +139,26 @@ def test_general_plan_rejects_bad_specs():
         sga.plan_host_general(2, 4, 4, 5, sigma_h=(1, 2))          # sigma < 1
     with pytest.raises(sga.SgaError):
         sga.plan_host_general(2, 4, 4, 5, protected=[2 * 21])      # outside [0, N*L)
+
+
+@pytest.mark.parametrize("N,gh,gw,nsp,n_t,n_s,r", [(9, 6, 7, 5, 4, 8, 500), (800, 37, 37, 5, 4, 37, 500),
+                                                   (7, 5, 5, 0, 3, 25, 1000), (5, 4, 9, 5, 5, 13, 0),
+                                                   (11, 37, 28, 5, 2, 100, 333)])
+def test_merge_size_matches_oracle_merge_count(N, gh, gw, nsp, n_t, n_s, r):
+    mc = sga.MergeConfig(B=1, H=1, N=N, grid_h=gh, grid_w=gw, n_special=nsp, n_t=n_t, n_s=n_s, r_permille=r)
+    if N > 100:   # count per block in closed form (the oracle merges exactly floor(#src * r / 1000))
+        P, ns = gh * gw, min(n_s, gh * gw)
+        merged = sum(((min(n_t, N - f0) - 1) * min(ns, P - w0) * r) // 1000
+                     for f0 in range(0, N, n_t) for w0 in range(0, P, ns))
+    else:
+        X = np.random.default_rng(N).standard_normal((mc.T, 64)).astype(np.float32)
+        merged = int((oracle.merge_match(X, N, gh, gw, nsp, n_t, min(n_s, gh * gw), r) >= 0).sum())
+    assert sga.merge_size(mc) == mc.T - merged
+
+
+def test_merge_rejects_bad_configs():
+    for bad in (dict(n_t=0), dict(r_permille=1001), dict(n_t=9, n_s=100)):   # 9 x 64 > 512
+        kw = dict(B=1, H=1, N=4, grid_h=8, grid_w=8, n_s=16)
+        kw.update(bad)
+        with pytest.raises(sga.SgaError):
+            sga.merge_size(sga.MergeConfig(**kw))
