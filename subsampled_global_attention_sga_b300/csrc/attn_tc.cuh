@@ -67,8 +67,8 @@ constexpr int OFF_QEXT = OFF_V + STAGES * TILE_BYTES;
 constexpr int OFF_KEXT = OFF_QEXT + EXT_BYTES;
 constexpr int OFF_BAR = OFF_KEXT + STAGES * EXT_BYTES;
 // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
-//           p_ready[2], o_done[2], o_free[2], drain, q_rot
-constexpr int NUM_BARS = 2 + 4 * STAGES + 8 + 2;
+//           p_ready[2], o_done[2], o_free[2], drain, q_rot, pv_done[2]
+constexpr int NUM_BARS = 2 + 4 * STAGES + 8 + 2 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
 
@@ -111,8 +111,9 @@ struct Bars {
     __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (4 * STAGES + 6 + t); }
     __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (4 * STAGES + 8); }
     __device__ __forceinline__ uint32_t q_rot() const { return base + 16 + 8 * (4 * STAGES + 9); }
+    __device__ __forceinline__ uint32_t pv_done(int t) const { return base + 16 + 8 * (4 * STAGES + 10 + t); }
 };
-static_assert(16 + 8 * (4 * STAGES + 10) == NUM_BARS * 8, "barrier block size");
+static_assert(16 + 8 * (4 * STAGES + 12) == NUM_BARS * 8, "barrier block size");
 
 // Bounded wait without the abort check: used only to drain work already in flight.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -172,6 +173,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         mbar_init(bars.drain(), 1);
         mbar_init(bars.q_rot(), 256);
+        mbar_init(bars.pv_done(0), 1);
+        mbar_init(bars.pv_done(1), 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
@@ -322,14 +325,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     if (j == 0 && !warp_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     if (elect_one()) {
-                        issue_pv(t, st, j > 0 ? 1u : 0u);
-                        if (t == 1) mma_commit(bars.v_empty(st));
+                        // the next S of this tile first (its softmax warps have read S_t), then
+                        // this tile's PV: the tensor pipe is in order, so S_t(j+1) is ready a PV
+                        // earlier; the softmax warps wait for pv_done before they touch P_t or O_t
                         if (has_next) {
                             issue_qk(t, stn);
                             mma_commit(bars.s_full(t));
-                        } else {
-                            mma_commit(bars.o_done(t));
                         }
+                        issue_pv(t, st, j > 0 ? 1u : 0u);
+                        mma_commit(bars.pv_done(t));
+                        if (t == 1) mma_commit(bars.v_empty(st));
+                        if (!has_next) mma_commit(bars.o_done(t));
                     }
                     __syncwarp();
                 }
@@ -432,6 +438,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     l *= alpha;
                     m = m_new;
                 }
+                // P_t and O_t are free once this tile's previous PV has completed (it was issued
+                // after the QK that produced this S, so it is usually done already)
+                if (j > 0) {
+                    if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                }
                 // p = 2^(s * scale_log2 - m), two columns per packed FMA; P goes back to TMEM
                 // as bf16 pairs one 32-column chunk at a time
                 const uint64_t sc2 = f2_pack(sl2, sl2);
@@ -456,8 +468,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
                     l += a0 + a1;
                 }
-                // O *= alpha when the reference max moved (the logits are dead by now); the
-                // PV product of this tile waits for p_ready, so it sees both updates
+                // O *= alpha when the reference max moved (the logits are dead by now; the
+                // previous PV has completed); this tile's next PV waits for p_ready, so it sees
+                // both updates
                 if (rescale && j > 0) {
                     uint32_t r[32];
 #pragma unroll

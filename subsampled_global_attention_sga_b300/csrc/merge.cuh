@@ -63,8 +63,12 @@ struct MergeArgs {
 };
 
 // grid: (n_windows + 1, n_chunks, BH); blockIdx.x == n_windows handles the chunk's specials.
+// Dynamic shared memory: the block's rows as fp32 with a padded stride of 65 (conflict-free
+// per-thread rows), then norms, similarities, destinations and ranks; sized for nb_max entries.
+__host__ __device__ constexpr int merge_smem_bytes(int nb_max) { return nb_max * 65 * 4 + 4 * nb_max * 4; }
+
 template <typename T>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
+__global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a, int nb_max) {
     const MergeGeom& g = a.g;
     const int c = blockIdx.y;
     const long long bh = blockIdx.z;
@@ -102,10 +106,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
 
     extern __shared__ uint8_t smem[];
     float* xs = reinterpret_cast<float*>(smem);                  // [nb][65] (padded rows)
-    float* nrm = xs + kMergeMaxBlock * 65;                      // [nb]
-    float* sim = nrm + kMergeMaxBlock;                          // [n_src]
-    int* best = reinterpret_cast<int*>(sim + kMergeMaxBlock);   // [n_src] block index of the destination
-    int* rank = best + kMergeMaxBlock;                          // [nb]: merged index within block, or -1
+    float* nrm = xs + nb_max * 65;                               // [nb]
+    float* sim = nrm + nb_max;                                   // [n_src]
+    int* best = reinterpret_cast<int*>(sim + nb_max);            // [n_src] block index of the destination
+    int* rank = best + nb_max;                                   // [nb]: merged index within block, or -1
 
     auto tok = [&](int i) -> long long {                        // token of block entry i
         return (long long)(f0 + i / ws) * g.L + g.n_special + (long long)w * g.n_s + i % ws;
@@ -124,11 +128,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
     // every source (entries ws .. nb-1) finds its destination (entries 0 .. ws-1)
     for (int a2 = threadIdx.x; a2 < n_src; a2 += kMergeThreads) {
         const int k = ws + a2;
+        float xk[64];                                            // the source row, in registers
+#pragma unroll
+        for (int e = 0; e < 64; ++e) xk[e] = xs[k * 65 + e];
         float bs = -INFINITY;
         int bd = -1;
         for (int d = 0; d < ws; ++d) {
             float dot = 0.f;
-            for (int e = 0; e < 64; ++e) dot = __fmaf_rn(xs[k * 65 + e], xs[d * 65 + e], dot);
+#pragma unroll
+            for (int e = 0; e < 64; ++e) dot = __fmaf_rn(xk[e], xs[d * 65 + e], dot);
             const float den = __fmul_rn(nrm[k], nrm[d]);
             const float cs = den == 0.f ? 0.f : __fdiv_rn(dot, den);
             if (cs > bs) { bs = cs; bd = d; }
@@ -158,7 +166,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
     }
     __syncthreads();
     // group means: a kept entry plus the sources merged into it (destinations only), summed in
-    // entry order
+    // entry order, 16 dims at a time
     for (int k = threadIdx.x; k < nb; k += kMergeThreads) {
         const long long t = tok(k);
         if (rank[k] < 0) {
@@ -167,33 +175,38 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
         }
         const long long mi = base + rank[k];
         map[t] = (int32_t)mi;
-        float sx[64], sy[64];
-        for (int e = 0; e < 64; ++e) {
-            sx[e] = xs[k * 65 + e];
-            sy[e] = Y ? Elem<T>::to_f(Y[t * 64 + e]) : 0.f;
-        }
         int cnt = 1;
-        if (k < ws) {
-            for (int a2 = 0; a2 < n_src; ++a2) {
-                if (rank[ws + a2] >= 0 || best[a2] != k) continue;
-                ++cnt;
-                const long long ts = tok(ws + a2);
-                for (int e = 0; e < 64; ++e) {
-                    sx[e] += xs[(ws + a2) * 65 + e];
-                    if (Y) sy[e] += Elem<T>::to_f(Y[ts * 64 + e]);
+        if (k < ws)
+            for (int a2 = 0; a2 < n_src; ++a2) cnt += (rank[ws + a2] < 0 && best[a2] == k) ? 1 : 0;
+        const float inv = 1.0f / (float)cnt;
+        for (int e0 = 0; e0 < 64; e0 += 16) {
+            float sx[16], sy[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                sx[e] = xs[k * 65 + e0 + e];
+                sy[e] = Y ? Elem<T>::to_f(Y[t * 64 + e0 + e]) : 0.f;
+            }
+            if (k < ws && cnt > 1) {
+                for (int a2 = 0; a2 < n_src; ++a2) {
+                    if (rank[ws + a2] >= 0 || best[a2] != k) continue;
+                    const long long ts = tok(ws + a2);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        sx[e] += xs[(ws + a2) * 65 + e0 + e];
+                        if (Y) sy[e] += Elem<T>::to_f(Y[ts * 64 + e0 + e]);
+                    }
                 }
             }
-        }
-        const float inv = 1.0f / (float)cnt;
-        for (int e = 0; e < 64; ++e) {
-            Xm[mi * 64 + e] = Elem<T>::from_f(sx[e] * inv);
-            if (Ym) Ym[mi * 64 + e] = Elem<T>::from_f(sy[e] * inv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                Xm[mi * 64 + e0 + e] = Elem<T>::from_f(sx[e] * inv);
+                if (Ym) Ym[mi * 64 + e0 + e] = Elem<T>::from_f(sy[e] * inv);
+            }
         }
         if (lg) lg[mi] = logf((float)cnt);
     }
 }
 
-constexpr int kMergeSmemBytes = (kMergeMaxBlock * 65 + 3 * kMergeMaxBlock) * 4 + kMergeMaxBlock * 4;
 
 // Y[bh, t] = Ym[bh, map[bh, t]]: one thread per 16 bytes of a row.
 template <typename T>

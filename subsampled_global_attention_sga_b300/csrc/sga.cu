@@ -766,15 +766,16 @@ sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, 
     if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_INVALID_ARG;
     const int di = cfg->dtype == SGA_BF16 ? 0 : 1;
+    const int nb_max = g.n_t * g.n_s;                   // entries of the largest block
+    const int smem = sga::merge_smem_bytes(nb_max);
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         if (!g_merge_smem_set[dev][di]) {
+            const int most = sga::merge_smem_bytes(sga::kMergeMaxBlock);
             const cudaError_t e = di == 0 ? cudaFuncSetAttribute(sga::merge_kernel<__nv_bfloat16>,
-                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                                 sga::kMergeSmemBytes)
+                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most)
                                           : cudaFuncSetAttribute(sga::merge_kernel<float>,
-                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                                 sga::kMergeSmemBytes);
+                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
             if (e != cudaSuccess) return SGA_ERR_CUDA;
             g_merge_smem_set[dev][di] = true;
         }
@@ -790,9 +791,9 @@ sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, 
     dim3 grid((unsigned)g.n_windows + 1, (unsigned)g.n_chunks, (unsigned)(cfg->B * cfg->H));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (di == 0)
-        sga::merge_kernel<__nv_bfloat16><<<grid, sga::kMergeThreads, sga::kMergeSmemBytes, s>>>(a);
+        sga::merge_kernel<__nv_bfloat16><<<grid, sga::kMergeThreads, smem, s>>>(a, nb_max);
     else
-        sga::merge_kernel<float><<<grid, sga::kMergeThreads, sga::kMergeSmemBytes, s>>>(a);
+        sga::merge_kernel<float><<<grid, sga::kMergeThreads, smem, s>>>(a, nb_max);
     return launch_status();
 }
 
