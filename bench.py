@@ -86,6 +86,8 @@ TRAFFIC_GB = {
     "40917419ae2423cb": {"headline": 382.20},
     # after the size-aware and rotary variants were added (same main path): 304.64 + 2.71 GB
     "585bb52597cd6808": {"headline": 307.35},
+    # key tiles swept in alternating directions per round of units: 92.52 + 2.44 GB
+    "ae0006a668381cc7": {"headline": 94.96},
 }
 
 

@@ -115,6 +115,14 @@ struct Bars {
 };
 static_assert(16 + 8 * (4 * STAGES + 12) == NUM_BARS * 8, "barrier block size");
 
+// Key tile processed at step j of a CTA's u_local-th unit.  All CTAs work on units of the same
+// head at the same time and sweep its key tiles; consecutive rounds sweep in opposite
+// directions, so a round starts on the tiles the previous one touched last (still in L2).  The
+// online softmax does not depend on the order.
+__device__ __forceinline__ int key_tile(int j, int n_kv, uint32_t u_local) {
+    return (u_local & 1) ? n_kv - 1 - j : j;
+}
+
 // Bounded wait without the abort check: used only to drain work already in flight.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
@@ -225,15 +233,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             for (int j = 0; j < n_kv; ++j, ++kv_it) {
                 const int st = kv_it % STAGES;
                 const uint32_t ph = (kv_it / STAGES) & 1;
+                const int jt = key_tile(j, n_kv, u_local);
                 if (!warp_wait(bars.k_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
                 if (kBias) {
                     // columns 0-1 of key row r: bias/scale as bf16 high + low parts
                     uint8_t* blk = base + OFF_KEXT + st * EXT_BYTES;
-                    const float* brow = p.bias + (long long)seg * p.kv_rows + (long long)j * BN;
+                    const float* brow = p.bias + (long long)seg * p.kv_rows + (long long)jt * BN;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int r = lane * 4 + i;
-                        const float b = (j * BN + r < p.kv_rows) ? __ldg(brow + r) * p.inv_scale : 0.f;
+                        const float b = (jt * BN + r < p.kv_rows) ? __ldg(brow + r) * p.inv_scale : 0.f;
                         const __nv_bfloat16 hi = __float2bfloat16_rn(b);
                         const __nv_bfloat16 lo = __float2bfloat16_rn(b - __bfloat162float(hi));
                         *reinterpret_cast<uint32_t*>(blk + ext_off(r, 0)) =
@@ -244,14 +253,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 if (elect_one()) {
                     mbar_arrive_expect_tx(bars.k_full(st), TILE_BYTES);
-                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, j * BN, seg);
+                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, jt * BN, seg);
                 }
                 __syncwarp();
                 ++k_issued;
                 if (!warp_wait(bars.v_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
                 if (elect_one()) {
                     mbar_arrive_expect_tx(bars.v_full(st), TILE_BYTES);
-                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.v_full(st), 0, j * BN, seg);
+                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.v_full(st), 0, jt * BN, seg);
                 }
                 __syncwarp();
                 ++v_issued;
@@ -412,7 +421,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 float s[128];
                 ld_row128(tS, s);
                 tmem_wait_ld();
-                if (j == n_kv - 1 && last_valid < BN) {
+                if (key_tile(j, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (c >= last_valid) s[c] = -INFINITY;
