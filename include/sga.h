@@ -278,6 +278,16 @@ sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, const void*
  * synchronisation itself failed. */
 sga_status sga_device_status(void* stream);
 
+/* Failure-detection self-test of the bounded waits (no counterpart on the pages; it checks
+ * the error path of this library).  Runs the tensor-core attention kernel on a small dense
+ * problem (buffers of its own, allocated and freed here) in which the TMA producer never loads
+ * one key tile, so nothing ever completes that tile's barrier.  The MMA warp's bounded wait
+ * expires (about 2 s of SM clocks), the CTA aborts -- every role leaves its loop, waits (again
+ * bounded) for the copies and products already in flight, frees its Tensor Memory and returns
+ * -- and the kernel records SGA_ERR_TIMEOUT.  Synchronises `stream` and returns the status it
+ * read (and cleared): SGA_ERR_TIMEOUT when the mechanism works.  The context stays usable. */
+sga_status sga_selftest_timeout(void* stream);
+
 /* Static description of a status code. */
 const char* sga_status_string(sga_status s);
 

@@ -21,7 +21,7 @@ EXPORTS = (
     "sga_compact", "sga_forward", "sga_dense_forward", "sga_frame_forward", "sga_device_status",
     "sga_status_string", "sga_build_info", "sga_compact_noalloc", "sga_bias_forward",
     "sga_plan_host_general", "sga_plan_create_from_index", "sga_rope2d",
-    "sga_merge_size", "sga_merge", "sga_unmerge",
+    "sga_merge_size", "sga_merge", "sga_unmerge", "sga_selftest_timeout",
 )
 
 
@@ -84,6 +84,7 @@ def lib():
             "sga_plan_create_from_index": (i32, [cfgp, vp, i64, i32, ctypes.POINTER(vp)]),
             "sga_rope2d": (i32, [vp, vp, vp]),
             "sga_merge_size": (i32, [ctypes.POINTER(SgaMergeConfig), ctypes.POINTER(i64)]),
+            "sga_selftest_timeout": (i32, [vp]),
             "sga_merge": (i32, [ctypes.POINTER(SgaMergeConfig), vp, vp, vp, vp, vp, vp, vp]),
             "sga_unmerge": (i32, [ctypes.POINTER(SgaMergeConfig), vp, vp, vp, vp]),
             "sga_device_status": (i32, [vp]),

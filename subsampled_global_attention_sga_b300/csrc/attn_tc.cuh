@@ -89,6 +89,8 @@ struct TcArgs {
     ExtraArgs ex;           // ex.on only for SGA (segment = batch*head)
     const float* bias;      // [n_seg, kv_rows] natural-log per-key bias (size-aware variant)
     float inv_scale;        // 1 / scale
+    long long drop_kv;      // failure-detection self-test: the producer never loads this key
+                            // tile (global ring index), so its wait expires; -1 in normal use
 };
 
 // byte offset of element (row r, column c) in a bias block
@@ -251,12 +253,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                 }
-                if (elect_one()) {
-                    mbar_arrive_expect_tx(bars.k_full(st), TILE_BYTES);
-                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, jt * BN, seg);
+                if ((long long)kv_it != p.drop_kv) {
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(bars.k_full(st), TILE_BYTES);
+                        tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, jt * BN, seg);
+                    }
+                    __syncwarp();
+                    k_issued = kv_it + 1;            // key tiles [0, k_issued) are issued (but drop_kv)
                 }
-                __syncwarp();
-                ++k_issued;
                 if (!warp_wait(bars.v_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
                 if (elect_one()) {
                     mbar_arrive_expect_tx(bars.v_full(st), TILE_BYTES);
@@ -269,7 +273,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (!ok) {
             // let the copies already issued land before the CTA leaves
             for (uint32_t i = (k_issued > STAGES ? k_issued - STAGES : 0); i < k_issued; ++i)
-                drain_wait(bars.k_full(i % STAGES), (i / STAGES) & 1);
+                if ((long long)i != p.drop_kv) drain_wait(bars.k_full(i % STAGES), (i / STAGES) & 1);
             for (uint32_t i = (v_issued > STAGES ? v_issued - STAGES : 0); i < v_issued; ++i)
                 drain_wait(bars.v_full(i % STAGES), (i / STAGES) & 1);
             if (q_issued > 0) drain_wait(bars.q_full(), (q_issued - 1) & 1);

@@ -119,6 +119,7 @@ struct AttnProblem {
     sga::ExtraArgs ex;
     const float* bias;      // per-key natural-log bias [n_seg, kv_rows], or null
     bool rope;              // rotate Q (and the extras' keys) with ex.rope
+    long long drop_kv;      // failure-detection self-test only (-1: off)
 };
 
 // The tensor-core kernel instantiation for a bias setting, checked once per device: its
@@ -175,6 +176,7 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.ex = pb.ex;
         a.bias = pb.bias;
         a.inv_scale = 1.0f / pb.scale;
+        a.drop_kv = pb.drop_kv;
         const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
         if (pb.bias)
             T::attn_tc_kernel<true, false><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
@@ -629,6 +631,7 @@ sga_status sga_forward(sga_plan_t plan, const void* Q, const void* K, const void
     pb.ex.rope = rope_args(plan);
     pb.bias = nullptr;
     pb.rope = c.rope != 0;
+    pb.drop_kv = -1;
     return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -655,6 +658,7 @@ static sga_status plain_attention(int n_seg, long long seg_rows, long long kv_ro
     pb.ex.on = 0;
     pb.bias = bias;
     pb.rope = false;
+    pb.drop_kv = -1;
     return run_attention(pb, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -813,6 +817,38 @@ sga_status sga_unmerge(const sga_merge_config* cfg, const int32_t* map, const vo
     else
         sga::unmerge_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(map, Y_m, Y, g.T, g.M, rows);
     return launch_status();
+}
+
+sga_status sga_selftest_timeout(void* stream) {
+    // a small dense problem on buffers of its own; the producer never loads key tile 1, so the
+    // MMA warp's bounded wait for it expires, the CTA aborts (every role leaves its loop, drains
+    // what is in flight, frees TMEM) and the kernel records SGA_ERR_TIMEOUT
+    const long long T = 4 * 128;
+    const size_t bytes = (size_t)T * 64 * 2;
+    void* buf = nullptr;
+    if (cudaMalloc(&buf, 4 * bytes) != cudaSuccess) return SGA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    sga_status st = cudaMemsetAsync(buf, 0, 4 * bytes, s) == cudaSuccess ? SGA_OK : SGA_ERR_CUDA;
+    if (st == SGA_OK) {
+        AttnProblem pb;
+        std::memset(&pb, 0, sizeof(pb));
+        pb.dtype = SGA_BF16;
+        pb.kernel = SGA_KERNEL_TC;
+        pb.n_seg = 1;
+        pb.seg_rows = T;
+        pb.kv_rows = T;
+        pb.Q = buf;
+        pb.Kt = static_cast<char*>(buf) + bytes;
+        pb.Vt = static_cast<char*>(buf) + 2 * bytes;
+        pb.O = static_cast<char*>(buf) + 3 * bytes;
+        pb.scale = 0.125f;
+        pb.ex.on = 0;
+        pb.drop_kv = 1;
+        st = run_attention(pb, s);
+    }
+    if (st == SGA_OK) st = sga_device_status(stream);       // expected: SGA_ERR_TIMEOUT
+    cudaFree(buf);
+    return st;
 }
 
 sga_status sga_device_status(void* stream) {
