@@ -329,7 +329,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const bool has_next = (j + 1 < n_kv);
                 const int stn = (kv_it + 1) % STAGES;
                 const uint32_t phn = ((kv_it + 1) / STAGES) & 1;
-                if (elect_one()) mma_commit(bars.k_empty(st));      // both QK_j issued
+                if (elect_one()) {
+                    mma_commit(bars.k_empty(st));                   // both QK_j issued
+                    // on the unit's last key tile every QK of the unit has been issued: the Q
+                    // tiles are free once they complete, so the next unit's Q loads during
+                    // this tile's softmax and PV
+                    if (!has_next) mma_commit(bars.q_empty());
+                }
                 __syncwarp();
                 if (has_next && !warp_wait(bars.k_full(stn), phn, abort_flag)) { ok = false; break; }
                 if (!warp_wait(bars.v_full(st), ph, abort_flag)) { ok = false; break; }
@@ -355,8 +361,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (!ok) break;
             }
             if (!ok) break;
-            if (elect_one()) mma_commit(bars.q_empty());
-            __syncwarp();
         }
         // every MMA issued so far completes before TMEM is released
         if (elect_one()) mma_commit(bars.drain());
