@@ -291,7 +291,8 @@ sga_status sga_selftest_timeout(void* stream);
 /* Static description of a status code. */
 const char* sga_status_string(sga_status s);
 
-/* Library build identification: compute capability targeted ("sm_103a") and version. */
+/* Library build identification: compute capability targeted ("sm_103a"), version, and
+ * "src=<fingerprint>" of the sources it was compiled from (the build passes SGA_SOURCE_HASH). */
 const char* sga_build_info(void);
 
 #ifdef __cplusplus

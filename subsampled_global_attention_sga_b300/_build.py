@@ -2,6 +2,7 @@
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
 import subprocess
 
@@ -19,8 +20,19 @@ NVCC_FLAGS = [
 ]
 
 
-def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))) + [HEADER]
+def _sources(csrc: str = CSRC, header: str = HEADER):
+    return sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))) + [header]
+
+
+def source_hash(csrc: str = CSRC, header: str = HEADER) -> str:
+    """Fingerprint of the library's sources (file names and contents).  It is compiled into the
+    library (``sga_build_info``), and the binding refuses a library built from other sources."""
+    h = hashlib.sha256()
+    for path in _sources(csrc, header):
+        h.update(os.path.basename(path).encode() + b"\0")
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def needs_build() -> bool:
@@ -35,7 +47,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     nvcc = os.environ.get("NVCC", "nvcc")
     tmp = LIB + ".tmp"
-    cmd = [nvcc, *NVCC_FLAGS, "-o", tmp, os.path.join(CSRC, "sga.cu")]
+    cmd = [nvcc, *NVCC_FLAGS, f'-DSGA_SOURCE_HASH="{source_hash()}"', "-o", tmp, os.path.join(CSRC, "sga.cu")]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)

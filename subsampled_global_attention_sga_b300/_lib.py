@@ -4,6 +4,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+from . import _build
 from ._build import LIB
 
 SGA_OK = 0
@@ -95,8 +96,20 @@ def lib():
             fn = getattr(L, name)
             fn.restype = res
             fn.argtypes = args
+        # a library compiled from other sources than the ones in the tree is refused, so a
+        # stale build can never stand in for the current code
+        info = L.sga_build_info().decode()
+        built = info.rsplit("src=", 1)[-1] if "src=" in info else "unknown"
+        tree = _tree_source_hash()
+        if built != tree:
+            raise RuntimeError(f"libsga.so was built from other sources (library {built}, tree {tree}); "
+                               "run __graft_entry__.build()")
         _lib = L
     return _lib
+
+
+def _tree_source_hash() -> str:
+    return _build.source_hash()
 
 
 def check(call: str, status: int) -> None:

@@ -317,7 +317,12 @@ const char* sga_status_string(sga_status s) {
     return "unknown status";
 }
 
-const char* sga_build_info(void) { return "libsga sm_103a (tcgen05/TMEM/TMA attention, CUDA-core fp32 path) v1"; }
+#ifndef SGA_SOURCE_HASH
+#define SGA_SOURCE_HASH "unknown"
+#endif
+const char* sga_build_info(void) {
+    return "libsga sm_103a (tcgen05/TMEM/TMA attention, CUDA-core fp32 path) v1 src=" SGA_SOURCE_HASH;
+}
 
 }  // extern "C"
 

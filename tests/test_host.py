@@ -32,6 +32,18 @@ def test_library_exports_every_declared_symbol():
     assert b"sm_103a" in L.sga_build_info()
 
 
+def test_library_carries_its_source_fingerprint(monkeypatch):
+    """The library names the sources it was compiled from, and the binding refuses a library
+    whose fingerprint differs from the tree's (a stale build)."""
+    from subsampled_global_attention_sga_b300 import _build
+    info = _lib.lib().sga_build_info().decode()
+    assert info.endswith("src=" + _build.source_hash())
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "_tree_source_hash", lambda: "0000000000000000")
+    with pytest.raises(RuntimeError, match="other sources"):
+        _lib.lib()
+
+
 def test_status_strings():
     L = sga.lib()
     for s in range(7):
