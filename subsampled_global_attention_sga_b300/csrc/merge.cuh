@@ -60,15 +60,63 @@ struct MergeArgs {
     void* Ym;               // [BH, M, 64] or null
     float* log_g;           // [BH, M] natural log of the group size, or null
     int32_t* map;           // [BH, T] merged index of every token
+    int nb_max;             // entries of the largest block (n_t * n_s)
+    int y_smem;             // 1: the block's Y rows are staged in shared memory
 };
 
-// grid: (n_windows + 1, n_chunks, BH); blockIdx.x == n_windows handles the chunk's specials.
-// Dynamic shared memory: the block's rows as fp32 with a padded stride of 65 (conflict-free
-// per-thread rows), then norms, similarities, destinations and ranks; sized for nb_max entries.
-__host__ __device__ constexpr int merge_smem_bytes(int nb_max) { return nb_max * 65 * 4 + 4 * nb_max * 4; }
+// Dynamic shared memory of one block, sized for nb_max entries:
+//   Y rows as stored (only when staged), X rows as fp32 with a padded stride of 65 (conflict-free
+//   per-thread rows), norms, similarity / destination partials (at least one per thread), kept
+//   ranks, and the per-warp totals of the rank scan.
+__host__ __device__ constexpr int merge_partials(int nb_max) { return nb_max > kMergeThreads ? nb_max : kMergeThreads; }
+__host__ __device__ constexpr int merge_smem_bytes(int nb_max, int elem_bytes, bool y_smem) {
+    return (y_smem ? nb_max * 64 * elem_bytes : 0) +
+           4 * (nb_max * 65 + nb_max + 2 * merge_partials(nb_max) + nb_max + kMergeThreads / 32);
+}
+
+// 16 consecutive elements of a row (generic address: shared or global) to fp32
+template <typename T>
+__device__ __forceinline__ void load16(const T* src, float (&x)[16]) {
+    const uint4* v = reinterpret_cast<const uint4*>(src);
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint4 w = v[i];
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) { x[8 * i + 2 * k] = bf16_lo(ww[k]); x[8 * i + 2 * k + 1] = bf16_hi(ww[k]); }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 w = v[i];
+            x[4 * i] = __uint_as_float(w.x); x[4 * i + 1] = __uint_as_float(w.y);
+            x[4 * i + 2] = __uint_as_float(w.z); x[4 * i + 3] = __uint_as_float(w.w);
+        }
+    }
+}
 
 template <typename T>
-__global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a, int nb_max) {
+__device__ __forceinline__ void store16(T* dst, const float (&x)[16]) {
+    uint4* v = reinterpret_cast<uint4*>(dst);
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            v[i] = make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
+                              pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = make_uint4(__float_as_uint(x[4 * i]), __float_as_uint(x[4 * i + 1]),
+                              __float_as_uint(x[4 * i + 2]), __float_as_uint(x[4 * i + 3]));
+    }
+}
+
+// grid: (n_windows + 1, n_chunks, BH); blockIdx.x == n_windows handles the chunk's specials.
+template <typename T>
+__global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
+    constexpr int VPR = 64 * (int)sizeof(T) / 16;       // 16-byte vectors per row
+    constexpr int EPV = 16 / (int)sizeof(T);            // elements per vector
     const MergeGeom& g = a.g;
     const int c = blockIdx.y;
     const long long bh = blockIdx.z;
@@ -80,19 +128,22 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a, in
     T* Ym = a.Ym ? reinterpret_cast<T*>(a.Ym) + bh * g.M * 64 : nullptr;
     float* lg = a.log_g ? a.log_g + bh * g.M : nullptr;
     int32_t* map = a.map + bh * g.T;
+    const int tid = threadIdx.x;
 
     if ((int)blockIdx.x == g.n_windows) {
         // special tokens of the chunk's frames: copied, group size 1
         const long long base = merge_block_base(g, c, -1);
-        for (int i = threadIdx.x; i < nf * g.n_special * 64; i += kMergeThreads) {
-            const int k = i / 64, e = i % 64;
+        const int n = nf * g.n_special;
+        for (int i = tid; i < n * VPR; i += kMergeThreads) {
+            const int k = i / VPR, v = i % VPR;
             const long long t = (long long)(f0 + k / g.n_special) * g.L + k % g.n_special;
-            Xm[(base + k) * 64 + e] = X[t * 64 + e];
-            if (Ym) Ym[(base + k) * 64 + e] = Y[t * 64 + e];
-            if (e == 0) {
-                map[t] = (int32_t)(base + k);
-                if (lg) lg[base + k] = 0.f;
-            }
+            reinterpret_cast<uint4*>(Xm + (base + k) * 64)[v] = __ldg(reinterpret_cast<const uint4*>(X + t * 64) + v);
+            if (Ym) reinterpret_cast<uint4*>(Ym + (base + k) * 64)[v] = __ldg(reinterpret_cast<const uint4*>(Y + t * 64) + v);
+        }
+        for (int k = tid; k < n; k += kMergeThreads) {
+            const long long t = (long long)(f0 + k / g.n_special) * g.L + k % g.n_special;
+            map[t] = (int32_t)(base + k);
+            if (lg) lg[base + k] = 0.f;
         }
         return;
     }
@@ -103,107 +154,171 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a, in
     const int n_src = (nf - 1) * ws;
     const long long r = ((long long)n_src * g.r_permille) / 1000;
     const long long base = merge_block_base(g, c, w);
+    const int nb_max = a.nb_max;
+    const bool y_smem = a.y_smem && Y;
 
-    extern __shared__ uint8_t smem[];
-    float* xs = reinterpret_cast<float*>(smem);                  // [nb][65] (padded rows)
-    float* nrm = xs + nb_max * 65;                               // [nb]
-    float* sim = nrm + nb_max;                                   // [n_src]
-    int* best = reinterpret_cast<int*>(sim + nb_max);            // [n_src] block index of the destination
-    int* rank = best + nb_max;                                   // [nb]: merged index within block, or -1
+    extern __shared__ __align__(16) uint8_t smem[];
+    T* ys = reinterpret_cast<T*>(smem);                                     // [nb][64] when staged
+    float* xs = reinterpret_cast<float*>(smem + (a.y_smem ? nb_max * 64 * (int)sizeof(T) : 0));  // [nb][65]
+    float* nrm = xs + nb_max * 65;                                          // [nb]
+    float* sim = nrm + nb_max;                                              // partials, then [n_src]
+    int* best = reinterpret_cast<int*>(sim + merge_partials(nb_max));      // partials, then [n_src]
+    int* rank = best + merge_partials(nb_max);                              // [nb]: merged index in block, or -1
+    int* wtot = rank + nb_max;                                              // [8] warp totals of the scan
 
     auto tok = [&](int i) -> long long {                        // token of block entry i
         return (long long)(f0 + i / ws) * g.L + g.n_special + (long long)w * g.n_s + i % ws;
     };
-    for (int i = threadIdx.x; i < nb * 64; i += kMergeThreads) {
-        const int k = i / 64, e = i % 64;
-        xs[k * 65 + e] = Elem<T>::to_f(X[tok(k) * 64 + e]);
+    // 1. the block's rows: X as fp32 (exact), Y as stored
+    for (int i = tid; i < nb * VPR; i += kMergeThreads) {
+        const int k = i / VPR, v = i % VPR;
+        const long long t = tok(k);
+        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(X + t * 64) + v);
+        float* dst = xs + k * 65 + v * EPV;
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) { dst[2 * q] = bf16_lo(ww[q]); dst[2 * q + 1] = bf16_hi(ww[q]); }
+        } else {
+            dst[0] = __uint_as_float(wv.x); dst[1] = __uint_as_float(wv.y);
+            dst[2] = __uint_as_float(wv.z); dst[3] = __uint_as_float(wv.w);
+        }
+        if (y_smem) reinterpret_cast<uint4*>(ys + k * 64)[v] = __ldg(reinterpret_cast<const uint4*>(Y + t * 64) + v);
     }
     __syncthreads();
-    for (int k = threadIdx.x; k < nb; k += kMergeThreads) {
+    // 2. norms: sqrt_rn of the fma chain of squares, dimensions in order
+    for (int k = tid; k < nb; k += kMergeThreads) {
         float s = 0.f;
         for (int e = 0; e < 64; ++e) s = __fmaf_rn(xs[k * 65 + e], xs[k * 65 + e], s);
         nrm[k] = __fsqrt_rn(s);
     }
     __syncthreads();
-    // every source (entries ws .. nb-1) finds its destination (entries 0 .. ws-1)
-    for (int a2 = threadIdx.x; a2 < n_src; a2 += kMergeThreads) {
+    // 3. every source (entries ws .. nb-1) finds its destination (entries 0 .. ws-1): the first
+    //    maximum of cos = dot / (n_a * n_b), each dot an fma chain over the dimensions in order.
+    //    The destinations are split into G contiguous groups so that all threads work; each
+    //    (source, group) item keeps four dot products in flight, and the groups' first maxima are
+    //    combined in ascending order, which gives the first maximum over all destinations.
+    const int G = n_src > 0 ? max(1, min(4, kMergeThreads / n_src)) : 1;
+    for (int it = tid; it < n_src * G; it += kMergeThreads) {
+        const int a2 = it % n_src, grp = it / n_src;
         const int k = ws + a2;
+        const int d_beg = (grp * ws) / G, d_end = ((grp + 1) * ws) / G;
         float xk[64];                                            // the source row, in registers
 #pragma unroll
         for (int e = 0; e < 64; ++e) xk[e] = xs[k * 65 + e];
+        const float nk = nrm[k];
         float bs = -INFINITY;
         int bd = -1;
-        for (int d = 0; d < ws; ++d) {
-            float dot = 0.f;
+        for (int d0 = d_beg; d0 < d_end; d0 += 4) {
+            const int d1 = min(d0 + 1, d_end - 1), d2 = min(d0 + 2, d_end - 1), d3 = min(d0 + 3, d_end - 1);
+            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 64; ++e) dot = __fmaf_rn(xk[e], xs[d * 65 + e], dot);
-            const float den = __fmul_rn(nrm[k], nrm[d]);
-            const float cs = den == 0.f ? 0.f : __fdiv_rn(dot, den);
-            if (cs > bs) { bs = cs; bd = d; }
+            for (int e = 0; e < 64; ++e) {
+                p0 = __fmaf_rn(xk[e], xs[d0 * 65 + e], p0);
+                p1 = __fmaf_rn(xk[e], xs[d1 * 65 + e], p1);
+                p2 = __fmaf_rn(xk[e], xs[d2 * 65 + e], p2);
+                p3 = __fmaf_rn(xk[e], xs[d3 * 65 + e], p3);
+            }
+            const float dots[4] = {p0, p1, p2, p3};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int d = d0 + q;
+                if (d < d_end) {
+                    const float den = __fmul_rn(nk, nrm[d]);
+                    const float cs = den == 0.f ? 0.f : __fdiv_rn(dots[q], den);
+                    if (cs > bs) { bs = cs; bd = d; }
+                }
+            }
         }
-        sim[a2] = bs;
-        best[a2] = bd;
+        sim[grp * n_src + a2] = bs;
+        best[grp * n_src + a2] = bd;
     }
     __syncthreads();
-    // merged sources: the r largest similarities (ties: lower token index = lower entry index,
-    // since entries are in token order); kept entries get consecutive merged indices in token order
-    for (int k = threadIdx.x; k < nb; k += kMergeThreads) {
+    if (G > 1) {
+        // slot a2 (group 0) is read and then written by thread a2 alone
+        for (int a2 = tid; a2 < n_src; a2 += kMergeThreads) {
+            float bs = sim[a2];
+            int bd = best[a2];
+            for (int grp = 1; grp < G; ++grp)
+                if (sim[grp * n_src + a2] > bs) { bs = sim[grp * n_src + a2]; bd = best[grp * n_src + a2]; }
+            sim[a2] = bs;
+            best[a2] = bd;
+        }
+        __syncthreads();
+    }
+    // 4. merged sources: the r largest similarities (ties: lower token index = lower entry index,
+    //    since entries are in token order)
+    for (int k = tid; k < nb; k += kMergeThreads) {
         bool merged = false;
         if (k >= ws) {
             const int a2 = k - ws;
+            const float sa = sim[a2];
             long long ahead = 0;
-            for (int b2 = 0; b2 < n_src; ++b2)
-                if (sim[b2] > sim[a2] || (sim[b2] == sim[a2] && b2 < a2)) ++ahead;
+            for (int b2 = 0; b2 < n_src; ++b2) {
+                const float sb = sim[b2];
+                ahead += (sb > sa || (sb == sa && b2 < a2)) ? 1 : 0;
+            }
             merged = ahead < r;
         }
         rank[k] = merged ? -1 : 0;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {                                     // kept entries in token order
-        int m = 0;
-        for (int k = 0; k < nb; ++k)
-            if (rank[k] >= 0) rank[k] = m++;
-    }
-    __syncthreads();
-    // group means: a kept entry plus the sources merged into it (destinations only), summed in
-    // entry order, 16 dims at a time
-    for (int k = threadIdx.x; k < nb; k += kMergeThreads) {
-        const long long t = tok(k);
-        if (rank[k] < 0) {
-            map[t] = (int32_t)(base + rank[best[k - ws]]);
-            continue;
-        }
-        const long long mi = base + rank[k];
-        map[t] = (int32_t)mi;
-        int cnt = 1;
-        if (k < ws)
-            for (int a2 = 0; a2 < n_src; ++a2) cnt += (rank[ws + a2] < 0 && best[a2] == k) ? 1 : 0;
-        const float inv = 1.0f / (float)cnt;
-        for (int e0 = 0; e0 < 64; e0 += 16) {
-            float sx[16], sy[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                sx[e] = xs[k * 65 + e0 + e];
-                sy[e] = Y ? Elem<T>::to_f(Y[t * 64 + e0 + e]) : 0.f;
+    // 5. kept entries get consecutive merged indices in entry (= token) order: a block-wide
+    //    exclusive scan of the kept flags, 256 entries per round
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        int carry = 0;
+        for (int b0 = 0; b0 < nb; b0 += kMergeThreads) {
+            const int k = b0 + tid;
+            const bool kept = k < nb && rank[k] >= 0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, kept);
+            if (lane == 0) wtot[warp] = __popc(bal);
+            __syncthreads();
+            int before = carry, total = carry;
+            for (int q = 0; q < kMergeThreads / 32; ++q) {
+                before += q < warp ? wtot[q] : 0;
+                total += wtot[q];
             }
-            if (k < ws && cnt > 1) {
-                for (int a2 = 0; a2 < n_src; ++a2) {
-                    if (rank[ws + a2] >= 0 || best[a2] != k) continue;
-                    const long long ts = tok(ws + a2);
+            if (kept) rank[k] = before + __popc(bal & ((1u << lane) - 1u));
+            carry = total;
+            __syncthreads();
+        }
+    }
+    // 6. map: every token to its merged row (a merged source to its destination's)
+    for (int k = tid; k < nb; k += kMergeThreads)
+        map[tok(k)] = (int32_t)(base + (rank[k] >= 0 ? rank[k] : rank[best[k - ws]]));
+    // 7. group means of the kept entries (a destination plus the sources merged into it, summed
+    //    in entry order), 16 dimensions per work item, and ln of the group size
+    for (int it = tid; it < nb * 4; it += kMergeThreads) {
+        const int k = it >> 2, e0 = (it & 3) * 16;
+        if (rank[k] < 0) continue;
+        const long long mi = base + rank[k];
+        float sx[16], sy[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        sx[e] += xs[(ws + a2) * 65 + e0 + e];
-                        if (Y) sy[e] += Elem<T>::to_f(Y[ts * 64 + e0 + e]);
-                    }
+        for (int e = 0; e < 16; ++e) { sx[e] = xs[k * 65 + e0 + e]; sy[e] = 0.f; }
+        if (Y) load16<T>(y_smem ? ys + k * 64 + e0 : Y + tok(k) * 64 + e0, sy);
+        int cnt = 1;
+        if (k < ws) {
+            for (int a2 = 0; a2 < n_src; ++a2) {
+                if (rank[ws + a2] >= 0 || best[a2] != k) continue;
+                ++cnt;
+                const int ks = ws + a2;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sx[e] += xs[ks * 65 + e0 + e];
+                if (Y) {
+                    float ty[16];
+                    load16<T>(y_smem ? ys + ks * 64 + e0 : Y + tok(ks) * 64 + e0, ty);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sy[e] += ty[e];
                 }
             }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                Xm[mi * 64 + e0 + e] = Elem<T>::from_f(sx[e] * inv);
-                if (Ym) Ym[mi * 64 + e0 + e] = Elem<T>::from_f(sy[e] * inv);
-            }
         }
-        if (lg) lg[mi] = logf((float)cnt);
+        const float inv = 1.0f / (float)cnt;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) { sx[e] *= inv; sy[e] *= inv; }
+        store16<T>(Xm + mi * 64 + e0, sx);
+        if (Ym) store16<T>(Ym + mi * 64 + e0, sy);
+        if (lg && e0 == 0) lg[mi] = logf((float)cnt);
     }
 }
 

@@ -775,16 +775,22 @@ sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, 
     if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_INVALID_ARG;
     const int di = cfg->dtype == SGA_BF16 ? 0 : 1;
+    const int elem = di == 0 ? 2 : 4;
     const int nb_max = g.n_t * g.n_s;                   // entries of the largest block
-    const int smem = sga::merge_smem_bytes(nb_max);
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return SGA_ERR_CUDA;
+    // the values are staged in shared memory beside the keys when both fit
+    const bool y_smem = Y != nullptr && sga::merge_smem_bytes(nb_max, elem, true) <= optin;
+    const int smem = sga::merge_smem_bytes(nb_max, elem, y_smem);
+    if (smem > optin) return SGA_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         if (!g_merge_smem_set[dev][di]) {
-            const int most = sga::merge_smem_bytes(sga::kMergeMaxBlock);
             const cudaError_t e = di == 0 ? cudaFuncSetAttribute(sga::merge_kernel<__nv_bfloat16>,
-                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most)
+                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin)
                                           : cudaFuncSetAttribute(sga::merge_kernel<float>,
-                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
             if (e != cudaSuccess) return SGA_ERR_CUDA;
             g_merge_smem_set[dev][di] = true;
         }
@@ -797,12 +803,14 @@ sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, 
     a.Ym = Y_m;
     a.log_g = log_g;
     a.map = map;
+    a.nb_max = nb_max;
+    a.y_smem = y_smem ? 1 : 0;
     dim3 grid((unsigned)g.n_windows + 1, (unsigned)g.n_chunks, (unsigned)(cfg->B * cfg->H));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (di == 0)
-        sga::merge_kernel<__nv_bfloat16><<<grid, sga::kMergeThreads, smem, s>>>(a, nb_max);
+        sga::merge_kernel<__nv_bfloat16><<<grid, sga::kMergeThreads, smem, s>>>(a);
     else
-        sga::merge_kernel<float><<<grid, sga::kMergeThreads, smem, s>>>(a, nb_max);
+        sga::merge_kernel<float><<<grid, sga::kMergeThreads, smem, s>>>(a);
     return launch_status();
 }
 

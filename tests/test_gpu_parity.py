@@ -616,6 +616,19 @@ def test_merge_matches_oracle(dev, dtype, tdt, n_t, n_s, r):
             _merge_check(mc, k, v, Km, Vm, lg, mp, b, h)
 
 
+@pytest.mark.parametrize("dtype,tdt", [("bf16", torch.bfloat16), ("f32", torch.float32)])
+def test_merge_largest_block(dev, dtype, tdt):
+    # 8 frames x 64 patches = 512 entries per block, the largest supported; in fp32 the values
+    # no longer fit in shared memory beside the keys and are read from global memory
+    mc = sga.MergeConfig(B=1, H=2, N=9, grid_h=8, grid_w=8, n_t=8, n_s=64, r_permille=500, dtype=dtype)
+    _, k, v = correlated_qkv(1, 2, mc.N, mc.n_special + 64, 64, seed=130, dtype=tdt, device=dev)
+    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    for h in range(2):
+        _merge_check(mc, k, v, Km, Vm, lg, mp, 0, h)
+
+
 @pytest.mark.parametrize("merge_queries", [False, True])
 def test_merged_attention(dev, merge_queries):
     mc = sga.MergeConfig(B=1, H=2, N=8, grid_h=9, grid_w=10, n_t=4, n_s=10, r_permille=600)
