@@ -6,7 +6,8 @@
 // (the sums formed here; the division by the count happens in the attention kernel).
 //
 // HBM-bound.  Each 64-wide row is read with 16-byte vector loads by a group of lanes (8 lanes
-// for bf16, 16 for fp32); several rows per lane are in flight.  Kept rows go to the slot the
+// for bf16, 16 for fp32; half as many with the rotation, each lane then holding the two vectors
+// whose dims rotate together); several rows per lane are in flight.  Kept rows go to the slot the
 // plan assigned; dropped rows are accumulated in fp32 registers.  The per-block partial sums go
 // to a scratch buffer and a second kernel adds them in a fixed order, so the result does not
 // depend on scheduling.
@@ -59,88 +60,120 @@ template <> struct Vec16<float> {
 };
 
 template <typename T, bool kRope>
-__global__ void __launch_bounds__(kCompactThreads) compact_kernel(CompactArgs a) {
-    constexpr int kLanesPerRow = 64 * (int)sizeof(T) / 16;     // 8 (bf16) or 16 (fp32)
-    constexpr int kRowsPerPass = kCompactThreads / kLanesPerRow;
+__global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel(CompactArgs a) {
+    constexpr int kLanesPerRow = 64 * (int)sizeof(T) / 16;     // 16-byte vectors per row: 8 (bf16) or 16 (fp32)
     constexpr int kElemsPerVec = 16 / (int)sizeof(T);            // 8 or 4
-    __shared__ float red[kCompactThreads][2 * kElemsPerVec + 1];
+    // with the rotation a lane holds both vectors of its rotation pairs (dims j and j+16 of a
+    // 32-dim half), so a row takes half as many lanes and no shuffles
+    constexpr int kRowLanes = kRope ? kLanesPerRow / 2 : kLanesPerRow;
+    constexpr int kVecsPerLane = kRope ? 2 : 1;
+    constexpr int kRowsPerPass = kCompactThreads / kRowLanes;
+    constexpr int kSums = kVecsPerLane * kElemsPerVec;            // key (and value) sums per lane
+    // rows in flight per lane (a rotating lane moves two vectors of K and of V per row)
+    constexpr int kUnroll = kRope ? kCompactUnroll / 2 : kCompactUnroll;
+    __shared__ float red[kCompactThreads][2 * kSums + 1];
 
     const int chunk = blockIdx.x;
     const int bh = blockIdx.y;
-    const int vec = threadIdx.x % kLanesPerRow;
-    const int rsub = threadIdx.x / kLanesPerRow;
+    const int lane_r = threadIdx.x % kRowLanes;
+    const int rsub = threadIdx.x / kRowLanes;
+    // vectors of this lane: without the rotation one (lane_r); with it the pair (va, va + PO),
+    // PO = 16 dims in vectors, va running over the first 16 dims of each 32-dim half
+    constexpr int PO = 16 / kElemsPerVec;
+    const int va = kRope ? (lane_r % PO) + 2 * PO * (lane_r / PO) : lane_r;
 
     const uint4* K = reinterpret_cast<const uint4*>(a.K) + (long long)bh * a.T * kLanesPerRow;
     const uint4* V = reinterpret_cast<const uint4*>(a.V) + (long long)bh * a.T * kLanesPerRow;
     uint4* KS = reinterpret_cast<uint4*>(a.KS) + (long long)bh * a.S * kLanesPerRow;
     uint4* VS = reinterpret_cast<uint4*>(a.VS) + (long long)bh * a.S * kLanesPerRow;
 
-    float ks[kElemsPerVec], vs[kElemsPerVec];
+    float ks[kSums], vs[kSums];
 #pragma unroll
-    for (int e = 0; e < kElemsPerVec; ++e) { ks[e] = 0.f; vs[e] = 0.f; }
+    for (int e = 0; e < kSums; ++e) { ks[e] = 0.f; vs[e] = 0.f; }
 
     const long long r_begin = (long long)chunk * a.rows_per_chunk;
     const long long r_end = (r_begin + a.rows_per_chunk < a.T) ? r_begin + a.rows_per_chunk : a.T;
 
     if constexpr (kRope) {
-        // rotated keys: the (cos, sin) table in shared memory; every lane takes part in each
-        // row group's shuffles, rows past the chunk end with zeros
+        // rotated keys: the (cos, sin) table in shared memory
         extern __shared__ float2 rope_s[];
         for (int i = threadIdx.x; i < a.rope.P * 16; i += kCompactThreads) rope_s[i] = a.rope.tab[i];
         __syncthreads();
         using VT = Vec16<T>;
-        for (long long r0 = r_begin; r0 < r_end; r0 += (long long)kRowsPerPass * kCompactUnroll) {
-            uint4 kv[kCompactUnroll], vv[kCompactUnroll];
-            int sl[kCompactUnroll];
+        const int d0 = va * kElemsPerVec;                         // first dim of vector va
+        for (long long r0 = r_begin; r0 < r_end; r0 += (long long)kRowsPerPass * kUnroll) {
+            uint4 ka[kUnroll], kb[kUnroll], wa[kUnroll], wb[kUnroll];
+            int sl[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kCompactUnroll; ++u) {
+            for (int u = 0; u < kUnroll; ++u) {
                 const long long t = r0 + (long long)u * kRowsPerPass + rsub;
                 sl[u] = -2;
-                kv[u] = make_uint4(0u, 0u, 0u, 0u);
-                vv[u] = kv[u];
                 if (t < r_end) {
                     sl[u] = __ldg(a.slot + t);
-                    kv[u] = __ldcs(K + t * kLanesPerRow + vec);
-                    vv[u] = __ldcs(V + t * kLanesPerRow + vec);
+                    ka[u] = __ldcs(K + t * kLanesPerRow + va);
+                    kb[u] = __ldcs(K + t * kLanesPerRow + va + PO);
+                    wa[u] = __ldcs(V + t * kLanesPerRow + va);
+                    wb[u] = __ldcs(V + t * kLanesPerRow + va + PO);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kCompactUnroll; ++u) {
+            for (int u = 0; u < kUnroll; ++u) {
+                if (sl[u] == -2) continue;
                 const long long t = r0 + (long long)u * kRowsPerPass + rsub;
                 int pr, pc;
-                rope_pos(a.rope, t < r_end ? t : 0, pr, pc);
-                float xk[kElemsPerVec], xv[kElemsPerVec];
-                VT::unpack(kv[u], xk);
-                rope_lane<kElemsPerVec>(rope_s, pr, pc, vec * kElemsPerVec, xk);
-                if (sl[u] >= 0) {
-                    KS[(long long)sl[u] * kLanesPerRow + vec] = VT::pack(xk);
-                    VS[(long long)sl[u] * kLanesPerRow + vec] = vv[u];
-                } else if (sl[u] == -1) {
-                    VT::unpack(vv[u], xv);
+                rope_pos(a.rope, t, pr, pc);
+                const float2* tb = rope_s + ((d0 & 32) ? pc : pr) * 16 + (d0 & 15);
+                float x0[kElemsPerVec], x1[kElemsPerVec];
+                VT::unpack(ka[u], x0);
+                VT::unpack(kb[u], x1);
 #pragma unroll
-                    for (int e = 0; e < kElemsPerVec; ++e) { ks[e] += xk[e]; vs[e] += xv[e]; }
+                for (int e = 0; e < kElemsPerVec; ++e) {             // dims d0+e and d0+e+16
+                    const float2 cs = tb[e];
+                    const float y0 = fmaf(-x1[e], cs.y, x0[e] * cs.x);
+                    const float y1 = fmaf(x0[e], cs.y, x1[e] * cs.x);
+                    x0[e] = y0;
+                    x1[e] = y1;
+                }
+                if (sl[u] >= 0) {
+                    uint4* ksr = KS + (long long)sl[u] * kLanesPerRow;
+                    uint4* vsr = VS + (long long)sl[u] * kLanesPerRow;
+                    ksr[va] = VT::pack(x0);
+                    ksr[va + PO] = VT::pack(x1);
+                    vsr[va] = wa[u];
+                    vsr[va + PO] = wb[u];
+                } else {
+                    float v0[kElemsPerVec], v1[kElemsPerVec];
+                    VT::unpack(wa[u], v0);
+                    VT::unpack(wb[u], v1);
+#pragma unroll
+                    for (int e = 0; e < kElemsPerVec; ++e) {
+                        ks[e] += x0[e];
+                        ks[kElemsPerVec + e] += x1[e];
+                        vs[e] += v0[e];
+                        vs[kElemsPerVec + e] += v1[e];
+                    }
                 }
             }
         }
     } else {
-    for (long long r0 = r_begin; r0 < r_end; r0 += (long long)kRowsPerPass * kCompactUnroll) {
-        uint4 kv[kCompactUnroll], vv[kCompactUnroll];
-        int sl[kCompactUnroll];
+    for (long long r0 = r_begin; r0 < r_end; r0 += (long long)kRowsPerPass * kUnroll) {
+        uint4 kv[kUnroll], vv[kUnroll];
+        int sl[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kCompactUnroll; ++u) {
+        for (int u = 0; u < kUnroll; ++u) {
             const long long t = r0 + (long long)u * kRowsPerPass + rsub;
             sl[u] = -2;
             if (t < r_end) {
                 sl[u] = __ldg(a.slot + t);
-                kv[u] = __ldcs(K + t * kLanesPerRow + vec);
-                vv[u] = __ldcs(V + t * kLanesPerRow + vec);
+                kv[u] = __ldcs(K + t * kLanesPerRow + va);
+                vv[u] = __ldcs(V + t * kLanesPerRow + va);
             }
         }
 #pragma unroll
-        for (int u = 0; u < kCompactUnroll; ++u) {
+        for (int u = 0; u < kUnroll; ++u) {
             if (sl[u] >= 0) {
-                KS[(long long)sl[u] * kLanesPerRow + vec] = kv[u];
-                VS[(long long)sl[u] * kLanesPerRow + vec] = vv[u];
+                KS[(long long)sl[u] * kLanesPerRow + va] = kv[u];
+                VS[(long long)sl[u] * kLanesPerRow + va] = vv[u];
             } else if (sl[u] == -1) {
                 if constexpr (sizeof(T) == 2) {
                     const uint32_t kw[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
@@ -164,9 +197,9 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(CompactArgs a)
     }
 
 #pragma unroll
-    for (int e = 0; e < kElemsPerVec; ++e) {
+    for (int e = 0; e < kSums; ++e) {
         red[threadIdx.x][e] = ks[e];
-        red[threadIdx.x][kElemsPerVec + e] = vs[e];
+        red[threadIdx.x][kSums + e] = vs[e];
     }
     __syncthreads();
     // 128 outputs: dim j of the key sum (j < 64) or of the value sum (j >= 64); added over the
@@ -175,8 +208,16 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(CompactArgs a)
         const int which = threadIdx.x >> 6;          // 0: keys, 1: values
         const int dim = threadIdx.x & 63;
         const int v = dim / kElemsPerVec, e = dim % kElemsPerVec;
+        // the lane holding vector v, and which of its vectors it is
+        int lane_v = v, slot_v = 0;
+        if (kRope) {
+            const int h = v / (2 * PO), w = v % (2 * PO);
+            slot_v = w / PO;
+            lane_v = (w % PO) + PO * h;
+        }
         float s = 0.f;
-        for (int r = 0; r < kRowsPerPass; ++r) s += red[r * kLanesPerRow + v][which * kElemsPerVec + e];
+        for (int r = 0; r < kRowsPerPass; ++r)
+            s += red[r * kRowLanes + lane_v][which * kSums + slot_v * kElemsPerVec + e];
         a.partials[((long long)bh * a.n_chunks + chunk) * 128 + threadIdx.x] = s;
     }
 }

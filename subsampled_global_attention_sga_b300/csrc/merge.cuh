@@ -65,13 +65,15 @@ struct MergeArgs {
 };
 
 // Dynamic shared memory of one block, sized for nb_max entries:
-//   Y rows as stored (only when staged), X rows as fp32 with a padded stride of 65 (conflict-free
-//   per-thread rows), norms, similarity / destination partials (at least one per thread), kept
+//   Y rows as stored (only when staged), X rows as fp32 with a padded stride of 68 floats (rows
+//   16-byte aligned: a warp's per-thread float4 row reads are conflict-free and a destination
+//   row is broadcast four values per load), norms, similarity / destination partials (at least one per thread), kept
 //   ranks, and the per-warp totals of the rank scan.
+constexpr int kXS = 68;                // row stride of the fp32 X rows in shared memory
 __host__ __device__ constexpr int merge_partials(int nb_max) { return nb_max > kMergeThreads ? nb_max : kMergeThreads; }
 __host__ __device__ constexpr int merge_smem_bytes(int nb_max, int elem_bytes, bool y_smem) {
     return (y_smem ? nb_max * 64 * elem_bytes : 0) +
-           4 * (nb_max * 65 + nb_max + 2 * merge_partials(nb_max) + nb_max + kMergeThreads / 32);
+           4 * (nb_max * kXS + nb_max + 2 * merge_partials(nb_max) + nb_max + kMergeThreads / 32);
 }
 
 // 16 consecutive elements of a row (generic address: shared or global) to fp32
@@ -159,8 +161,8 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
 
     extern __shared__ __align__(16) uint8_t smem[];
     T* ys = reinterpret_cast<T*>(smem);                                     // [nb][64] when staged
-    float* xs = reinterpret_cast<float*>(smem + (a.y_smem ? nb_max * 64 * (int)sizeof(T) : 0));  // [nb][65]
-    float* nrm = xs + nb_max * 65;                                          // [nb]
+    float* xs = reinterpret_cast<float*>(smem + (a.y_smem ? nb_max * 64 * (int)sizeof(T) : 0));  // [nb][kXS]
+    float* nrm = xs + nb_max * kXS;                                         // [nb]
     float* sim = nrm + nb_max;                                              // partials, then [n_src]
     int* best = reinterpret_cast<int*>(sim + merge_partials(nb_max));      // partials, then [n_src]
     int* rank = best + merge_partials(nb_max);                              // [nb]: merged index in block, or -1
@@ -174,22 +176,29 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         const int k = i / VPR, v = i % VPR;
         const long long t = tok(k);
         const uint4 wv = __ldg(reinterpret_cast<const uint4*>(X + t * 64) + v);
-        float* dst = xs + k * 65 + v * EPV;
+        float4* dst = reinterpret_cast<float4*>(xs + k * kXS + v * EPV);
         if constexpr (sizeof(T) == 2) {
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) { dst[2 * q] = bf16_lo(ww[q]); dst[2 * q + 1] = bf16_hi(ww[q]); }
+            dst[0] = make_float4(bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y));
+            dst[1] = make_float4(bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w));
         } else {
-            dst[0] = __uint_as_float(wv.x); dst[1] = __uint_as_float(wv.y);
-            dst[2] = __uint_as_float(wv.z); dst[3] = __uint_as_float(wv.w);
+            dst[0] = make_float4(__uint_as_float(wv.x), __uint_as_float(wv.y), __uint_as_float(wv.z),
+                                 __uint_as_float(wv.w));
         }
         if (y_smem) reinterpret_cast<uint4*>(ys + k * 64)[v] = __ldg(reinterpret_cast<const uint4*>(Y + t * 64) + v);
     }
     __syncthreads();
     // 2. norms: sqrt_rn of the fma chain of squares, dimensions in order
     for (int k = tid; k < nb; k += kMergeThreads) {
+        const float4* row = reinterpret_cast<const float4*>(xs + k * kXS);
         float s = 0.f;
-        for (int e = 0; e < 64; ++e) s = __fmaf_rn(xs[k * 65 + e], xs[k * 65 + e], s);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 x = row[q];
+            s = __fmaf_rn(x.x, x.x, s);
+            s = __fmaf_rn(x.y, x.y, s);
+            s = __fmaf_rn(x.z, x.z, s);
+            s = __fmaf_rn(x.w, x.w, s);
+        }
         nrm[k] = __fsqrt_rn(s);
     }
     __syncthreads();
@@ -205,19 +214,31 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         const int d_beg = (grp * ws) / G, d_end = ((grp + 1) * ws) / G;
         float xk[64];                                            // the source row, in registers
 #pragma unroll
-        for (int e = 0; e < 64; ++e) xk[e] = xs[k * 65 + e];
+        for (int q = 0; q < 16; ++q) {
+            const float4 x = reinterpret_cast<const float4*>(xs + k * kXS)[q];
+            xk[4 * q] = x.x; xk[4 * q + 1] = x.y; xk[4 * q + 2] = x.z; xk[4 * q + 3] = x.w;
+        }
         const float nk = nrm[k];
         float bs = -INFINITY;
         int bd = -1;
         for (int d0 = d_beg; d0 < d_end; d0 += 4) {
             const int d1 = min(d0 + 1, d_end - 1), d2 = min(d0 + 2, d_end - 1), d3 = min(d0 + 3, d_end - 1);
             float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+            const float4* r0 = reinterpret_cast<const float4*>(xs + d0 * kXS);
+            const float4* r1 = reinterpret_cast<const float4*>(xs + d1 * kXS);
+            const float4* r2 = reinterpret_cast<const float4*>(xs + d2 * kXS);
+            const float4* r3 = reinterpret_cast<const float4*>(xs + d3 * kXS);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                p0 = __fmaf_rn(xk[e], xs[d0 * 65 + e], p0);
-                p1 = __fmaf_rn(xk[e], xs[d1 * 65 + e], p1);
-                p2 = __fmaf_rn(xk[e], xs[d2 * 65 + e], p2);
-                p3 = __fmaf_rn(xk[e], xs[d3 * 65 + e], p3);
+            for (int q = 0; q < 16; ++q) {                       // dimensions 4q .. 4q+3, in order
+                const float4 b0 = r0[q], b1 = r1[q], b2 = r2[q], b3 = r3[q];
+                p0 = __fmaf_rn(xk[4 * q], b0.x, p0); p0 = __fmaf_rn(xk[4 * q + 1], b0.y, p0);
+                p0 = __fmaf_rn(xk[4 * q + 2], b0.z, p0); p0 = __fmaf_rn(xk[4 * q + 3], b0.w, p0);
+                p1 = __fmaf_rn(xk[4 * q], b1.x, p1); p1 = __fmaf_rn(xk[4 * q + 1], b1.y, p1);
+                p1 = __fmaf_rn(xk[4 * q + 2], b1.z, p1); p1 = __fmaf_rn(xk[4 * q + 3], b1.w, p1);
+                p2 = __fmaf_rn(xk[4 * q], b2.x, p2); p2 = __fmaf_rn(xk[4 * q + 1], b2.y, p2);
+                p2 = __fmaf_rn(xk[4 * q + 2], b2.z, p2); p2 = __fmaf_rn(xk[4 * q + 3], b2.w, p2);
+                p3 = __fmaf_rn(xk[4 * q], b3.x, p3); p3 = __fmaf_rn(xk[4 * q + 1], b3.y, p3);
+                p3 = __fmaf_rn(xk[4 * q + 2], b3.z, p3); p3 = __fmaf_rn(xk[4 * q + 3], b3.w, p3);
             }
             const float dots[4] = {p0, p1, p2, p3};
 #pragma unroll
@@ -295,7 +316,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         const long long mi = base + rank[k];
         float sx[16], sy[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) { sx[e] = xs[k * 65 + e0 + e]; sy[e] = 0.f; }
+        for (int e = 0; e < 16; ++e) { sx[e] = xs[k * kXS + e0 + e]; sy[e] = 0.f; }
         if (Y) load16<T>(y_smem ? ys + k * 64 + e0 : Y + tok(k) * 64 + e0, sy);
         int cnt = 1;
         if (k < ws) {
@@ -304,7 +325,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
                 ++cnt;
                 const int ks = ws + a2;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) sx[e] += xs[ks * 65 + e0 + e];
+                for (int e = 0; e < 16; ++e) sx[e] += xs[ks * kXS + e0 + e];
                 if (Y) {
                     float ty[16];
                     load16<T>(y_smem ? ys + ks * 64 + e0 : Y + tok(ks) * 64 + e0, ty);

@@ -21,7 +21,7 @@ struct RopeArgs {
 
 // (row, column) position of token t (index within one (batch, head) sequence)
 __device__ __forceinline__ void rope_pos(const RopeArgs& a, long long t, int& pr, int& pc) {
-    const int p = (int)(t % a.L);
+    const int p = (int)t % a.L;             // token indices of a sequence are below 2^31
     if (p < a.n_special) {
         pr = 0;
         pc = 0;
@@ -46,24 +46,6 @@ __device__ __forceinline__ void rope_row64(const RopeArgs& a, long long t, float
             x[32 * h + j] = x0 * cs.x - x1 * cs.y;
             x[32 * h + j + 16] = x0 * cs.y + x1 * cs.x;
         }
-    }
-}
-
-// Rotate the E = 16/sizeof-dependent consecutive dims [e0, e0 + E) a lane holds of one row,
-// where the 64 dims of the row are spread over consecutive lanes (E dims each); the partner
-// dims (+-16) live in lane ^ (16 / E).  tab_s: the table in shared memory.  Every lane of the
-// warp must call this (it shuffles).
-template <int E>
-__device__ __forceinline__ void rope_lane(const float2* tab_s, int pr, int pc, int e0, float (&x)[E]) {
-    float y[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], 16 / E);
-    const int pos = (e0 & 32) ? pc : pr;
-    const bool second = (e0 & 16) != 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float2 cs = tab_s[pos * 16 + ((e0 + e) & 15)];
-        x[e] = second ? fmaf(y[e], cs.y, x[e] * cs.x) : fmaf(-y[e], cs.y, x[e] * cs.x);
     }
 }
 
