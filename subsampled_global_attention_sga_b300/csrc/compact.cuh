@@ -69,8 +69,9 @@ __global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel
     constexpr int kVecsPerLane = kRope ? 2 : 1;
     constexpr int kRowsPerPass = kCompactThreads / kRowLanes;
     constexpr int kSums = kVecsPerLane * kElemsPerVec;            // key (and value) sums per lane
-    // rows in flight per lane (a rotating lane moves two vectors of K and of V per row)
-    constexpr int kUnroll = kRope ? kCompactUnroll / 2 : kCompactUnroll;
+    // rows in flight per lane (a rotating lane moves two vectors of K and of V per row; three
+    // rows keep it within two blocks per SM)
+    constexpr int kUnroll = kRope ? 3 : kCompactUnroll;
     __shared__ float red[kCompactThreads][2 * kSums + 1];
 
     const int chunk = blockIdx.x;
