@@ -629,6 +629,32 @@ def test_merge_largest_block(dev, dtype, tdt):
         _merge_check(mc, k, v, Km, Vm, lg, mp, 0, h)
 
 
+@pytest.mark.parametrize("dtype,tdt", [("bf16", torch.bfloat16), ("f32", torch.float32)])
+def test_merge_nothing_is_identity(dev, dtype, tdt):
+    # r = 0: every token is its own group, so unmerging the merged rows restores X exactly and
+    # every group's ln g is 0
+    mc = sga.MergeConfig(B=1, H=2, N=7, grid_h=6, grid_w=7, n_t=3, n_s=10, r_permille=0, dtype=dtype)
+    _, k, v = correlated_qkv(1, 2, mc.N, mc.n_special + 42, 64, seed=140, dtype=tdt, device=dev)
+    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    assert Km.shape[2] == mc.T
+    assert torch.equal(sga.unmerge(mc, mp, Km), k) and torch.equal(sga.unmerge(mc, mp, Vm), v)
+    assert torch.count_nonzero(lg) == 0
+    for h in range(2):                                      # the map is a permutation per head
+        assert torch.equal(torch.sort(mp[0, h]).values, torch.arange(mc.T, device=dev, dtype=mp.dtype))
+
+
+def test_unmerge_gives_each_token_its_group_mean(dev):
+    mc = sga.MergeConfig(B=1, H=2, N=8, grid_h=6, grid_w=7, n_t=4, n_s=7, r_permille=700, dtype="f32")
+    _, k, _ = correlated_qkv(1, 2, mc.N, mc.n_special + 42, 64, seed=150, dtype=torch.float32, device=dev)
+    Km, _, lg, mp = sga.merge(mc, k)
+    back = sga.unmerge(mc, mp, Km)
+    torch.cuda.synchronize(dev)
+    for h in range(2):
+        kept, gid, sizes, _ = _merge_check(mc, k, None, Km, None, lg, mp, 0, h)
+        ref = oracle.merge_apply(_host(k[0, h]), gid, len(kept))[gid]      # every token's group mean
+        _compare(_host(back[0, h]), ref, "f32", "unmerged means")
+
+
 @pytest.mark.parametrize("merge_queries", [False, True])
 def test_merged_attention(dev, merge_queries):
     mc = sga.MergeConfig(B=1, H=2, N=8, grid_h=9, grid_w=10, n_t=4, n_s=10, r_permille=600)

@@ -43,6 +43,20 @@ def test_stream_equals_layer(dev, depth):
         assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
 
 
+def test_stream_with_rotation_equals_layer(dev):
+    cfg = sga.SGAConfig(B=1, H=2, N=5, grid_h=9, grid_w=9, sigma=4, rope=True)
+    plan = sga.Plan(cfg, dev)
+    batches = _batches(cfg, 3)
+    outs = [torch.empty((cfg.B, cfg.H, cfg.T, 64), dtype=torch.bfloat16, pin_memory=True) for _ in batches]
+    hs = sga.HostStream(plan)
+    for (q, k, v), o in zip(batches, outs):
+        hs.submit(q, k, v, o)
+    hs.synchronize()
+    for (q, k, v), o in zip(batches, outs):
+        ref = plan.layer(q.to(dev), k.to(dev), v.to(dev)).cpu()
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+
+
 def test_stream_matches_oracle(dev):
     cfg = sga.SGAConfig(B=1, H=2, N=4, grid_h=8, grid_w=8, sigma=4)
     plan = sga.Plan(cfg, dev)
