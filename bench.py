@@ -514,6 +514,9 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         _barrier(world)
         e_ms = _max_over_ranks(a.elapsed_time(b), world, dev) / args.steps
+        if job.kind == "sga":
+            hs.synchronize()
+            hs.close()
         e2e = {"value": world * job.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host_in),
                "d2h_bytes_per_step": oh.numel() * oh.element_size(), "mode": e2e_mode}

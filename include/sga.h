@@ -273,6 +273,33 @@ sga_status sga_unmerge(const sga_merge_config* cfg, const int32_t* map, const vo
 sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, const void* V, void* K_S,
                                void* V_S, float* k_sum, float* v_sum, void* stream);
 
+/* Streaming from host memory (no counterpart on the pages; the executor that feeds the layer
+ * from host buffers).  A stream object owns, for one plan, `depth` sets of device tensors (Q, K,
+ * V, O, K_S, V_S and the two sums) and three CUDA streams of its own: host-to-device copies,
+ * compute, device-to-host copies.  Every device allocation happens in sga_stream_create.
+ *
+ * sga_stream_submit queues one whole layer: copies K and V, then Q, from the HOST pointers
+ * into the next buffer set, runs sga_compact as soon as K and V have arrived and sga_forward
+ * once Q has, and copies O back to the host pointer.  It returns at once.  Consecutive submits
+ * overlap: layer i+1's inputs and layer i-1's output move while layer i computes.  Events order
+ * every reuse of a buffer set after the work that last read it, so each output equals
+ * sga_compact + sga_forward on the same inputs.  Host buffers are [B, H, T, 64] in the plan's
+ * dtype; they must stay valid and unchanged until sga_stream_synchronize returns, and they
+ * should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to overlap.
+ * `scale` <= 0 means 1/sqrt(64).  All calls need the plan's device current; the plan must
+ * outlive the stream object.  depth: 1 .. 8 buffer sets. */
+typedef struct sga_stream_s* sga_stream_t;
+sga_status sga_stream_create(sga_plan_t plan, int depth, sga_stream_t* out);
+sga_status sga_stream_submit(sga_stream_t s, const void* Q_host, const void* K_host, const void* V_host,
+                             void* O_host, float scale);
+/* Wait until every submitted layer's output is in its host buffer. */
+sga_status sga_stream_synchronize(sga_stream_t s);
+/* The object's CUDA streams (cudaStream_t), e.g. to record timing events around submits:
+ * h2d receives the first work of a submit, d2h the last. */
+sga_status sga_stream_handles(sga_stream_t s, void** h2d, void** compute, void** d2h);
+/* Waits for outstanding work, then frees everything the object owns.  NULL is a no-op. */
+void sga_stream_destroy(sga_stream_t s);
+
 /* Synchronise `stream`, then read and clear the device status word of the current device
  * (SGA_OK or SGA_ERR_TIMEOUT from a kernel's bounded wait).  Returns SGA_ERR_CUDA if the
  * synchronisation itself failed. */

@@ -23,6 +23,8 @@ EXPORTS = (
     "sga_status_string", "sga_build_info", "sga_compact_noalloc", "sga_bias_forward",
     "sga_plan_host_general", "sga_plan_create_from_index", "sga_rope2d",
     "sga_merge_size", "sga_merge", "sga_unmerge", "sga_selftest_timeout",
+    "sga_stream_create", "sga_stream_submit", "sga_stream_synchronize", "sga_stream_handles",
+    "sga_stream_destroy",
 )
 
 
@@ -91,6 +93,11 @@ def lib():
             "sga_device_status": (i32, [vp]),
             "sga_status_string": (ctypes.c_char_p, [i32]),
             "sga_build_info": (ctypes.c_char_p, []),
+            "sga_stream_create": (i32, [vp, i32, ctypes.POINTER(vp)]),
+            "sga_stream_submit": (i32, [vp, vp, vp, vp, vp, f32]),
+            "sga_stream_synchronize": (i32, [vp]),
+            "sga_stream_handles": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp)]),
+            "sga_stream_destroy": (None, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -410,66 +410,58 @@ def device_status(device=None) -> int:
 
 
 class HostStream:
-    """Streams SGA layers from pinned host memory through one plan, overlapping transfers with
-    compute.  Device inputs and outputs are double-buffered: while batch i is computed on the
-    compute stream, batch i+1's Q, K, V are copied in on a copy stream and batch i-1's output is
-    copied out on another.  Within a batch K and V are copied first, so the compaction starts
-    while Q is still in flight.  Events order every reuse of a device buffer after the work that
-    last read it, so results equal ``Plan.layer`` on the same inputs."""
+    """Streams SGA layers from pinned host memory through one plan (``sga_stream_*``): the
+    library double-buffers the device tensors and runs host-to-device copies, compute and
+    device-to-host copies on three CUDA streams of its own, so layer i+1's inputs and layer
+    i-1's output move while layer i computes (K and V first, so the compaction starts while Q is
+    in flight).  Each output equals ``Plan.layer`` on the same inputs.  ``h2d`` and ``d2h`` are
+    the library's first and last streams, for timing events."""
 
     def __init__(self, plan: Plan, depth: int = 2):
-        if depth < 1:
-            raise ValueError("depth must be >= 1")
-        cfg, dev = plan.cfg, plan.device
-        self.plan, self.device, self.depth = plan, dev, depth
-        shp = (cfg.B, cfg.H, plan.T, 64)
-        dt = cfg.torch_dtype
-        with torch.cuda.device(dev):
-            self._in = [tuple(torch.empty(shp, dtype=dt, device=dev) for _ in range(3)) for _ in range(depth)]
-            self._out = [torch.empty(shp, dtype=dt, device=dev) for _ in range(depth)]
-            self.h2d = torch.cuda.Stream(dev)
-            self.compute = torch.cuda.Stream(dev)
-            self.d2h = torch.cuda.Stream(dev)
-            ev = lambda: [torch.cuda.Event() for _ in range(depth)]
-            self._kv_in, self._q_in, self._done, self._out_read = ev(), ev(), ev(), ev()
-        self._used = [False] * depth
-        self._i = 0
+        self.plan, self.device = plan, plan.device
+        self._h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            check("sga_stream_create", lib().sga_stream_create(plan._h, int(depth), ctypes.byref(self._h)))
+            a, b, c = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+            check("sga_stream_handles", lib().sga_stream_handles(self._h, ctypes.byref(a), ctypes.byref(b),
+                                                                 ctypes.byref(c)))
+            self.h2d = torch.cuda.ExternalStream(a.value, device=self.device)
+            self.compute = torch.cuda.ExternalStream(b.value, device=self.device)
+            self.d2h = torch.cuda.ExternalStream(c.value, device=self.device)
+        self._keep = []          # host tensors of queued layers, held until synchronize
 
     def submit(self, Q_host, K_host, V_host, out_host, scale=None):
         """Queue one layer: out_host <- SGA(Q_host, K_host, V_host).  Returns immediately; the
-        host buffers (pinned) must stay untouched until ``synchronize``."""
-        k = self._i % self.depth
-        Qd, Kd, Vd = self._in[k]
-        Od = self._out[k]
-        used = self._used[k]
+        host tensors (CPU, contiguous, pinned for overlap) must stay untouched until
+        ``synchronize``."""
+        cfg = self.plan.cfg
+        shp = (cfg.B, cfg.H, self.plan.T, 64)
+        for n, t in (("Q", Q_host), ("K", K_host), ("V", V_host), ("out", out_host)):
+            _check_tensor(n, t, shp, cfg.torch_dtype, torch.device("cpu"))
         with torch.cuda.device(self.device):
-            if used:
-                self.h2d.wait_event(self._done[k])          # the layer that read these inputs is done
-            with torch.cuda.stream(self.h2d):
-                Kd.copy_(K_host, non_blocking=True)
-                Vd.copy_(V_host, non_blocking=True)
-                self._kv_in[k].record(self.h2d)
-                Qd.copy_(Q_host, non_blocking=True)
-                self._q_in[k].record(self.h2d)
-            self.compute.wait_event(self._kv_in[k])
-            if used:
-                self.compute.wait_event(self._out_read[k])  # the previous output left this buffer
-            with torch.cuda.stream(self.compute):
-                K_S, V_S, k_sum, v_sum = self.plan.compact(Kd, Vd)
-                self.compute.wait_event(self._q_in[k])
-                self.plan.forward(Qd, Kd, Vd, K_S, V_S, k_sum, v_sum, out=Od, scale=scale)
-                self._done[k].record(self.compute)
-            self.d2h.wait_event(self._done[k])
-            with torch.cuda.stream(self.d2h):
-                out_host.copy_(Od, non_blocking=True)
-                self._out_read[k].record(self.d2h)
-        self._used[k] = True
-        self._i += 1
+            check("sga_stream_submit", lib().sga_stream_submit(
+                self._h, _ptr(Q_host), _ptr(K_host), _ptr(V_host), _ptr(out_host),
+                ctypes.c_float(0.0 if scale is None else float(scale))))
+        self._keep.append((Q_host, K_host, V_host, out_host))
         return out_host
 
     def synchronize(self):
         """Wait until every submitted layer's output is in its host buffer."""
-        self.d2h.synchronize()
+        with torch.cuda.device(self.device):
+            check("sga_stream_synchronize", lib().sga_stream_synchronize(self._h))
+        self._keep.clear()
+
+    def close(self):
+        if self._h:
+            lib().sga_stream_destroy(self._h)
+            self._h = ctypes.c_void_p()
+            self._keep.clear()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def layer_from_host(plan: Plan, Q_host, K_host, V_host, out_host=None, scale=None):

@@ -864,6 +864,165 @@ sga_status sga_selftest_timeout(void* stream) {
     return st;
 }
 
+}  // extern "C"
+
+struct sga_stream_s {
+    uint32_t magic;
+    sga_plan_t plan;
+    int depth;
+    size_t in_bytes;                        // one of Q, K, V, O
+    std::vector<void*> q, k, v, o, ks, vs;  // per buffer set
+    std::vector<float*> ksum, vsum;
+    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    std::vector<cudaEvent_t> kv_in, q_in, done, out_read;
+    std::vector<char> used;
+    long long next = 0;
+};
+
+namespace {
+
+constexpr uint32_t kStreamMagic = 0x53474153u;   // "SGAS"
+
+void stream_free(sga_stream_s* s) {
+    if (s->h2d) cudaStreamSynchronize(s->h2d);
+    if (s->comp) cudaStreamSynchronize(s->comp);
+    if (s->d2h) cudaStreamSynchronize(s->d2h);
+    for (auto* vec : {&s->q, &s->k, &s->v, &s->o, &s->ks, &s->vs})
+        for (void* p : *vec) if (p) cudaFree(p);
+    for (auto* vec : {&s->ksum, &s->vsum})
+        for (float* p : *vec) if (p) cudaFree(p);
+    for (auto* vec : {&s->kv_in, &s->q_in, &s->done, &s->out_read})
+        for (cudaEvent_t e : *vec) if (e) cudaEventDestroy(e);
+    if (s->h2d) cudaStreamDestroy(s->h2d);
+    if (s->comp) cudaStreamDestroy(s->comp);
+    if (s->d2h) cudaStreamDestroy(s->d2h);
+    s->magic = 0;
+    delete s;
+}
+
+sga_status check_stream(sga_stream_t s) {
+    if (!s || s->magic != kStreamMagic) return SGA_ERR_INVALID_ARG;
+    return check_plan(s->plan);
+}
+
+}  // namespace
+
+extern "C" {
+
+sga_status sga_stream_create(sga_plan_t plan, int depth, sga_stream_t* out) {
+    if (!plan || !out || depth < 1 || depth > 8) return SGA_ERR_INVALID_ARG;
+    *out = nullptr;
+    sga_status st = check_plan(plan);
+    if (st != SGA_OK) return st;
+    sga_stream_s* s = new (std::nothrow) sga_stream_s();
+    if (!s) return SGA_ERR_CUDA;
+    s->magic = kStreamMagic;
+    s->plan = plan;
+    s->depth = depth;
+    const size_t elem = plan->cfg.dtype == SGA_BF16 ? 2 : 4;
+    const size_t bh = (size_t)plan->cfg.B * plan->cfg.H;
+    s->in_bytes = bh * (size_t)plan->T * 64 * elem;
+    const size_t ks_bytes = bh * (size_t)(plan->S > 0 ? plan->S : 1) * 64 * elem;
+    const size_t sum_bytes = bh * 64 * sizeof(float);
+    bool ok = true;
+    auto alloc = [&](size_t bytes) -> void* {
+        void* p = nullptr;
+        if (ok && cudaMalloc(&p, bytes) != cudaSuccess) { ok = false; p = nullptr; }
+        return p;
+    };
+    auto event = [&]() -> cudaEvent_t {
+        cudaEvent_t e = nullptr;
+        if (ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) { ok = false; e = nullptr; }
+        return e;
+    };
+    for (int i = 0; i < depth; ++i) {
+        s->q.push_back(alloc(s->in_bytes));
+        s->k.push_back(alloc(s->in_bytes));
+        s->v.push_back(alloc(s->in_bytes));
+        s->o.push_back(alloc(s->in_bytes));
+        s->ks.push_back(alloc(ks_bytes));
+        s->vs.push_back(alloc(ks_bytes));
+        s->ksum.push_back(static_cast<float*>(alloc(sum_bytes)));
+        s->vsum.push_back(static_cast<float*>(alloc(sum_bytes)));
+        s->kv_in.push_back(event());
+        s->q_in.push_back(event());
+        s->done.push_back(event());
+        s->out_read.push_back(event());
+        s->used.push_back(0);
+    }
+    if (ok && (cudaStreamCreateWithFlags(&s->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+               cudaStreamCreateWithFlags(&s->comp, cudaStreamNonBlocking) != cudaSuccess ||
+               cudaStreamCreateWithFlags(&s->d2h, cudaStreamNonBlocking) != cudaSuccess))
+        ok = false;
+    if (!ok) {
+        stream_free(s);
+        cudaGetLastError();
+        return SGA_ERR_CUDA;
+    }
+    *out = s;
+    return SGA_OK;
+}
+
+sga_status sga_stream_submit(sga_stream_t s, const void* Q_host, const void* K_host, const void* V_host,
+                             void* O_host, float scale) {
+    sga_status st = check_stream(s);
+    if (st != SGA_OK) return st;
+    if (!Q_host || !K_host || !V_host || !O_host) return SGA_ERR_INVALID_ARG;
+    if (!(scale > 0.f)) scale = 0.125f;
+    const int i = (int)(s->next % s->depth);
+    const size_t n = s->in_bytes;
+    auto cu = [](cudaError_t e) { return e == cudaSuccess; };
+    // inputs: the layer that last read this buffer set has finished; K and V first
+    if (s->used[i] && !cu(cudaStreamWaitEvent(s->h2d, s->done[i], 0))) return SGA_ERR_CUDA;
+    if (!cu(cudaMemcpyAsync(s->k[i], K_host, n, cudaMemcpyHostToDevice, s->h2d)) ||
+        !cu(cudaMemcpyAsync(s->v[i], V_host, n, cudaMemcpyHostToDevice, s->h2d)) ||
+        !cu(cudaEventRecord(s->kv_in[i], s->h2d)) ||
+        !cu(cudaMemcpyAsync(s->q[i], Q_host, n, cudaMemcpyHostToDevice, s->h2d)) ||
+        !cu(cudaEventRecord(s->q_in[i], s->h2d)))
+        return SGA_ERR_CUDA;
+    // compute: compaction once K and V are in, attention once Q is; O is free once the previous
+    // output of this set has been copied out
+    if (!cu(cudaStreamWaitEvent(s->comp, s->kv_in[i], 0))) return SGA_ERR_CUDA;
+    if (s->used[i] && !cu(cudaStreamWaitEvent(s->comp, s->out_read[i], 0))) return SGA_ERR_CUDA;
+    if ((st = sga_compact(s->plan, s->k[i], s->v[i], s->ks[i], s->vs[i], s->ksum[i], s->vsum[i], s->comp)) != SGA_OK)
+        return st;
+    if (!cu(cudaStreamWaitEvent(s->comp, s->q_in[i], 0))) return SGA_ERR_CUDA;
+    if ((st = sga_forward(s->plan, s->q[i], s->k[i], s->v[i], s->ks[i], s->vs[i], s->ksum[i], s->vsum[i], s->o[i],
+                          nullptr, scale, s->comp)) != SGA_OK)
+        return st;
+    if (!cu(cudaEventRecord(s->done[i], s->comp))) return SGA_ERR_CUDA;
+    // output
+    if (!cu(cudaStreamWaitEvent(s->d2h, s->done[i], 0)) ||
+        !cu(cudaMemcpyAsync(O_host, s->o[i], n, cudaMemcpyDeviceToHost, s->d2h)) ||
+        !cu(cudaEventRecord(s->out_read[i], s->d2h)))
+        return SGA_ERR_CUDA;
+    s->used[i] = 1;
+    ++s->next;
+    return SGA_OK;
+}
+
+sga_status sga_stream_synchronize(sga_stream_t s) {
+    sga_status st = check_stream(s);
+    if (st != SGA_OK) return st;
+    if (cudaStreamSynchronize(s->h2d) != cudaSuccess || cudaStreamSynchronize(s->comp) != cudaSuccess ||
+        cudaStreamSynchronize(s->d2h) != cudaSuccess)
+        return SGA_ERR_CUDA;
+    return SGA_OK;
+}
+
+sga_status sga_stream_handles(sga_stream_t s, void** h2d, void** compute, void** d2h) {
+    if (!s || s->magic != kStreamMagic) return SGA_ERR_INVALID_ARG;
+    if (h2d) *h2d = s->h2d;
+    if (compute) *compute = s->comp;
+    if (d2h) *d2h = s->d2h;
+    return SGA_OK;
+}
+
+void sga_stream_destroy(sga_stream_t s) {
+    if (!s || s->magic != kStreamMagic) return;
+    stream_free(s);
+}
+
 sga_status sga_device_status(void* stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SGA_ERR_CUDA;
     int v = 0;

@@ -118,6 +118,13 @@ def test_null_arguments_rejected_without_device():
     buf = (ctypes.c_char * 64)()
     p = ctypes.addressof(buf) + 1  # misaligned
     assert L.sga_dense_forward(1, 1, 4, 64, 0, 0, p, p, p, p, None, ctypes.c_float(0.125), None) == 3
+    # the host-streaming executor rejects a missing plan or object before any CUDA call
+    h = ctypes.c_void_p()
+    assert L.sga_stream_create(None, 2, ctypes.byref(h)) == 1 and not h.value
+    assert L.sga_stream_submit(None, p, p, p, p, ctypes.c_float(0.125)) == 1
+    assert L.sga_stream_synchronize(None) == 1
+    assert L.sga_stream_handles(None, None, None, None) == 1
+    L.sga_stream_destroy(None)
 
 
 GENERAL_CASES = [
