@@ -11,9 +11,10 @@
 // Work unit: two 128-row query tiles of one segment (a (batch, head) pair, or one frame of it)
 // against all key tiles of that segment.  Roles (384 threads):
 //   warp 0      TMA producer: the two Q tiles, then a STAGES-deep ring of K and V tiles
-//   warp 1      TMEM owner and MMA issuer (one elected lane issues):
-//                 S_t = Q_t K_j^T  (M=128, N=128, K=64; A, B from shared memory)
-//                 O_t += P_t V_j   (M=128, N=64,  K=128; P from TMEM, V from shared memory)
+//   warp 1      TMEM owner and MMA issuer of query tile 0 (one elected lane issues):
+//                 S_0 = Q_0 K_j^T  (M=128, N=128, K=64; A, B from shared memory)
+//                 O_0 += P_0 V_j   (M=128, N=64,  K=128; P from TMEM, V from shared memory)
+//   warp 2      MMA issuer of query tile 1 (S_1, O_1); the two issuers take turns
 //   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
 //   warps 8-11  softmax + epilogue of query tile 1
 // TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384) P_0 [384,448) P_1 [448,512).
@@ -44,9 +45,11 @@ __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * (uint32_t)t;
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 64u * (uint32_t)t; }   // O_t
 __host__ __device__ constexpr uint32_t col_p(int t) { return 384u + 64u * (uint32_t)t; }   // P_t
 constexpr float kRescaleThreshold = 8.0f;      // base-2: rescale when the max grows by > 2^8
+constexpr float kSumTrigger = 128.0f;          // a tile sum above this takes the exact max path
+constexpr int kLazyMinKeyTiles = 32;           // key ranges this long use the exponentials-first softmax
 
 // Register split (setmaxnreg): the kernel is launched with LAUNCH_REGS per thread; warpgroup 0
-// (TMA producer, MMA issuer, two idle warps) gives registers back, the two softmax warpgroups
+// (TMA producer, two MMA issuers, one idle warp) gives registers back, the two softmax warpgroups
 // take them.  The split must add up to the launch total, otherwise setmaxnreg.inc cannot be
 // satisfied; the host checks the compiled register count before every launch.
 constexpr uint32_t LAUNCH_REGS = 168;
@@ -66,9 +69,9 @@ constexpr int EXT_BYTES = 128 * 16 * 2;
 constexpr int OFF_QEXT = OFF_V + STAGES * TILE_BYTES;
 constexpr int OFF_KEXT = OFF_QEXT + EXT_BYTES;
 constexpr int OFF_BAR = OFF_KEXT + STAGES * EXT_BYTES;
-// barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
-//           p_ready[2], o_done[2], o_free[2], drain, q_rot, pv_done[2]
-constexpr int NUM_BARS = 2 + 4 * STAGES + 8 + 2 + 2;
+// barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_done[2],
+//           o_free[2], drain, q_rot, pv_done[2], turn[2]
+constexpr int NUM_BARS = 2 + 2 * STAGES + 8 + 2 + 2 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
 
@@ -103,19 +106,18 @@ struct Bars {
     uint32_t base;
     __device__ __forceinline__ uint32_t q_full() const { return base; }
     __device__ __forceinline__ uint32_t q_empty() const { return base + 8; }
-    __device__ __forceinline__ uint32_t k_full(int s) const { return base + 16 + 8 * s; }
-    __device__ __forceinline__ uint32_t k_empty(int s) const { return base + 16 + 8 * (STAGES + s); }
-    __device__ __forceinline__ uint32_t v_full(int s) const { return base + 16 + 8 * (2 * STAGES + s); }
-    __device__ __forceinline__ uint32_t v_empty(int s) const { return base + 16 + 8 * (3 * STAGES + s); }
-    __device__ __forceinline__ uint32_t s_full(int t) const { return base + 16 + 8 * (4 * STAGES + t); }
-    __device__ __forceinline__ uint32_t p_ready(int t) const { return base + 16 + 8 * (4 * STAGES + 2 + t); }
-    __device__ __forceinline__ uint32_t o_done(int t) const { return base + 16 + 8 * (4 * STAGES + 4 + t); }
-    __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (4 * STAGES + 6 + t); }
-    __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (4 * STAGES + 8); }
-    __device__ __forceinline__ uint32_t q_rot() const { return base + 16 + 8 * (4 * STAGES + 9); }
-    __device__ __forceinline__ uint32_t pv_done(int t) const { return base + 16 + 8 * (4 * STAGES + 10 + t); }
+    __device__ __forceinline__ uint32_t kv_full(int s) const { return base + 16 + 8 * s; }
+    __device__ __forceinline__ uint32_t kv_empty(int s) const { return base + 16 + 8 * (STAGES + s); }
+    __device__ __forceinline__ uint32_t s_full(int t) const { return base + 16 + 8 * (2 * STAGES + t); }
+    __device__ __forceinline__ uint32_t p_ready(int t) const { return base + 16 + 8 * (2 * STAGES + 2 + t); }
+    __device__ __forceinline__ uint32_t o_done(int t) const { return base + 16 + 8 * (2 * STAGES + 4 + t); }
+    __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (2 * STAGES + 6 + t); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (2 * STAGES + 8); }
+    __device__ __forceinline__ uint32_t q_rot() const { return base + 16 + 8 * (2 * STAGES + 9); }
+    __device__ __forceinline__ uint32_t pv_done(int t) const { return base + 16 + 8 * (2 * STAGES + 10 + t); }
+    __device__ __forceinline__ uint32_t turn(int t) const { return base + 16 + 8 * (2 * STAGES + 12 + t); }
 };
-static_assert(16 + 8 * (4 * STAGES + 12) == NUM_BARS * 8, "barrier block size");
+static_assert(16 + 8 * (2 * STAGES + 14) == NUM_BARS * 8, "barrier block size");
 
 // Key tile processed at step j of a CTA's u_local-th unit.  All CTAs work on units of the same
 // head at the same time and sweep its key tiles; consecutive rounds sweep in opposite
@@ -152,7 +154,71 @@ __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&s)[128]) {
     }
 }
 
-template <bool kBias, bool kRope>
+// The max-first step of the online softmax for one query row and one key tile (logits s[128],
+// masked columns already -inf): the row maximum decides whether the reference max m moves (by
+// more than 2^kRescaleThreshold).  When it moves, l (and O in TMEM, when o_live) is rescaled; P
+// is (re)computed and stored whenever the reference moved or store_always is set, and tsum is
+// then this tile's sum of p.  The tile's previous PV must have completed.
+__device__ __forceinline__ void exact_tile(const float (&s)[128], uint32_t tP, uint32_t tO, float sl2,
+                                           bool o_live, bool store_always, float& m, float& l, float& tsum) {
+    // row maximum: eight independent 16-column chains, then a small tree
+    float mx8[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
+#pragma unroll
+        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
+        mx8[g] = fmaxf(a, s[16 * g + 15]);
+    }
+    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+    const float m_cand = mx * sl2;
+    const bool need = m_cand > m + kRescaleThreshold;
+    const bool rescale = __any_sync(0xffffffffu, need);
+    float alpha = 1.0f;
+    if (rescale) {
+        const float m_new = fmaxf(m, m_cand);
+        alpha = ex2_approx(m - m_new);                       // 0 when m = -inf
+        l *= alpha;
+        m = m_new;
+    }
+    if (rescale || store_always) {
+        const uint64_t sc2 = f2_pack(sl2, sl2);
+        const uint64_t nm2 = f2_pack(-m, -m);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
+                const float p0 = ex2_approx(x0);
+                const float p1 = ex2_approx(x1);
+                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tP + 16 * c, pk);
+        }
+        float a0, a1;
+        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+        tsum = a0 + a1;
+    }
+    // O *= alpha when the reference moved; the tile's next PV waits for p_ready, so it sees
+    // both updates
+    if (rescale && o_live) {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            tmem_ld32(tO + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + 32 * c, r);
+        }
+    }
+}
+
+template <bool kBias, bool kRope, bool kLazy>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcArgs p) {
@@ -168,23 +234,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         mbar_init(bars.q_full(), 1);
-        mbar_init(bars.q_empty(), 1);
+        mbar_init(bars.q_empty(), 2);                   // one commit per MMA issuer
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bars.k_full(s), 1);
-            mbar_init(bars.k_empty(s), 1);
-            mbar_init(bars.v_full(s), 1);
-            mbar_init(bars.v_empty(s), 1);
+            mbar_init(bars.kv_full(s), 1);
+            mbar_init(bars.kv_empty(s), 2);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bars.s_full(t), 1);
             mbar_init(bars.p_ready(t), 128);
             mbar_init(bars.o_done(t), 1);
             mbar_init(bars.o_free(t), 128);
+            mbar_init(bars.pv_done(t), 1);
+            mbar_init(bars.turn(t), 1);
         }
-        mbar_init(bars.drain(), 1);
+        mbar_init(bars.drain(), 2);
         mbar_init(bars.q_rot(), 256);
-        mbar_init(bars.pv_done(0), 1);
-        mbar_init(bars.pv_done(1), 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
@@ -219,7 +283,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         // The whole warp runs the loop (warp-uniform state); one elected lane issues.
-        uint32_t kv_it = 0, k_issued = 0, v_issued = 0, q_issued = 0, u_local = 0;
+        uint32_t kv_it = 0, kv_issued = 0, q_issued = 0, u_local = 0;
         bool ok = true;
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
             const int seg = (int)(u / p.n_pairs);
@@ -236,7 +300,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const int st = kv_it % STAGES;
                 const uint32_t ph = (kv_it / STAGES) & 1;
                 const int jt = key_tile(j, n_kv, u_local);
-                if (!warp_wait(bars.k_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.kv_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
                 if (kBias) {
                     // columns 0-1 of key row r: bias/scale as bf16 high + low parts
                     uint8_t* blk = base + OFF_KEXT + st * EXT_BYTES;
@@ -253,112 +317,118 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                 }
+                // K and V of one key tile arrive on one barrier; the self-test loads nothing for
+                // tile drop_kv, so that barrier never completes
                 if ((long long)kv_it != p.drop_kv) {
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(bars.k_full(st), TILE_BYTES);
-                        tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.k_full(st), 0, jt * BN, seg);
+                        mbar_arrive_expect_tx(bars.kv_full(st), 2 * TILE_BYTES);
+                        tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.kv_full(st), 0, jt * BN, seg);
+                        tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.kv_full(st), 0, jt * BN, seg);
                     }
                     __syncwarp();
-                    k_issued = kv_it + 1;            // key tiles [0, k_issued) are issued (but drop_kv)
                 }
-                if (!warp_wait(bars.v_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
-                if (elect_one()) {
-                    mbar_arrive_expect_tx(bars.v_full(st), TILE_BYTES);
-                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.v_full(st), 0, jt * BN, seg);
-                }
-                __syncwarp();
-                ++v_issued;
+                kv_issued = kv_it + 1;               // key tiles [0, kv_issued) are issued (but drop_kv)
             }
         }
         if (!ok) {
             // let the copies already issued land before the CTA leaves
-            for (uint32_t i = (k_issued > STAGES ? k_issued - STAGES : 0); i < k_issued; ++i)
-                if ((long long)i != p.drop_kv) drain_wait(bars.k_full(i % STAGES), (i / STAGES) & 1);
-            for (uint32_t i = (v_issued > STAGES ? v_issued - STAGES : 0); i < v_issued; ++i)
-                drain_wait(bars.v_full(i % STAGES), (i / STAGES) & 1);
+            for (uint32_t i = (kv_issued > STAGES ? kv_issued - STAGES : 0); i < kv_issued; ++i)
+                if ((long long)i != p.drop_kv) drain_wait(bars.kv_full(i % STAGES), (i / STAGES) & 1);
             if (q_issued > 0) drain_wait(bars.q_full(), (q_issued - 1) & 1);
         }
-      } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        // The whole warp runs the loop so descriptors and TMEM addresses stay warp-uniform;
-        // one elected lane (always the same, the lowest) issues every MMA and commit.
-        // Descriptors advance by adding (byte offset >> 4) to their start-address field.
-        const uint64_t dQ = smem_desc_sw128(sbase + OFF_Q, 16);
+      } else if (warp <= 2) {
+        // ------------------------------------------------------------------ MMA issuers
+        // Warp 1 issues the products of query tile 0, warp 2 those of tile 1.  They take turns
+        // (a token passed through the turn barriers), so the tensor pipe still receives the
+        // batches in the order tile 0, tile 1, tile 0, ... and the two tiles' softmax phases
+        // alternate; each issuer does its barrier bookkeeping while the other's batch runs
+        // (the pipe only queues a few instructions ahead).  The whole warp runs the loop so
+        // descriptors and TMEM addresses stay warp-uniform; one elected lane (always the
+        // lowest) issues every MMA, commit and token arrive.  A K/V stage is released when
+        // both issuers have committed it (the barrier counts two arrivals).  Descriptors
+        // advance by adding (byte offset >> 4) to their start-address field.
+        const int t = warp - 1;
+        const uint64_t dq = smem_desc_sw128(sbase + OFF_Q + t * TILE_BYTES, 16);
         const uint64_t dK = smem_desc_sw128(sbase + OFF_K, 16);
         const uint64_t dV = smem_desc_sw128(sbase + OFF_V, TILE_BYTES);
         const uint64_t dQe = smem_desc_noswz(sbase + OFF_QEXT, 128, 256);
         const uint64_t dKe = smem_desc_noswz(sbase + OFF_KEXT, 128, 256);
         constexpr uint64_t kTileStep = TILE_BYTES >> 4;
         constexpr uint64_t kExtStep = EXT_BYTES >> 4;
-        uint32_t kv_it = 0, g_it = 0, u_local = 0;
+        const uint32_t ts = tmem + col_s(t), to = tmem + col_o(t), tp = tmem + col_p(t);
+        // turns taken: issuer 0 holds the token first (its first wait is on the preceding,
+        // already complete phase)
+        uint32_t kv_it = 0, g_it = 0, u_local = 0, turns = 0;
         bool ok = true;
-        auto issue_qk = [&](int t, int st) {
-            const uint64_t dq = dQ + (uint64_t)t * kTileStep;
+        auto issue_qk = [&](int st) {
             const uint64_t dk = dK + (uint64_t)st * kTileStep;
-            const uint32_t ts = tmem + col_s(t);
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)                  // 16 columns = 32 bytes
                 mma_ss(ts, dq + 2 * kk, dk + 2 * kk, IDESC_QK, kk > 0 ? 1u : 0u);
             if (kBias) mma_ss(ts, dQe, dKe + (uint64_t)st * kExtStep, IDESC_QK, 1u);
         };
-        auto issue_pv = [&](int t, int st, uint32_t acc) {
+        auto issue_pv = [&](int st, uint32_t acc) {
             const uint64_t dv = dV + (uint64_t)st * kTileStep;
-            const uint32_t to = tmem + col_o(t), tp = tmem + col_p(t);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)                  // 16 rows = 2048 bytes
                 mma_ts(to, tp + 8 * kk, dv + 128 * kk, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        };
+        auto take_turn = [&]() -> bool {
+            const bool got = warp_wait(bars.turn(t), (turns & 1) ^ (t == 0 ? 1u : 0u), abort_flag);
+            ++turns;
+            return got;
+        };
+        auto pass_turn = [&]() {
+            if (elect_one()) mbar_arrive(bars.turn(t ^ 1));
+            __syncwarp();
         };
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
             // Q tiles loaded (and, with the rotary embedding, rotated by the softmax warps)
             if (!warp_wait(kRope ? bars.q_rot() : bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
             {
                 const int st = kv_it % STAGES;
-                if (!warp_wait(bars.k_full(st), (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.kv_full(st), (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
+                if (!take_turn()) { ok = false; break; }
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_qk(0, st);
-                    mma_commit(bars.s_full(0));
-                    issue_qk(1, st);
-                    mma_commit(bars.s_full(1));
+                    issue_qk(st);
+                    mma_commit(bars.s_full(t));
                 }
                 __syncwarp();
+                pass_turn();
             }
             for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_it) {
                 const int st = kv_it % STAGES;
-                const uint32_t ph = (kv_it / STAGES) & 1;
                 const bool has_next = (j + 1 < n_kv);
                 const int stn = (kv_it + 1) % STAGES;
                 const uint32_t phn = ((kv_it + 1) / STAGES) & 1;
+                if (has_next && !warp_wait(bars.kv_full(stn), phn, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.p_ready(t), g_it & 1, abort_flag)) { ok = false; break; }
+                if (j == 0 && !warp_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!take_turn()) { ok = false; break; }
+                tc_fence_after();
                 if (elect_one()) {
-                    mma_commit(bars.k_empty(st));                   // both QK_j issued
-                    // on the unit's last key tile every QK of the unit has been issued: the Q
-                    // tiles are free once they complete, so the next unit's Q loads during
-                    // this tile's softmax and PV
-                    if (!has_next) mma_commit(bars.q_empty());
+                    // the next S of this tile first (its softmax warps have read S_t), then this
+                    // tile's PV: the tensor pipe is in order, so S_t(j+1) is ready a PV earlier;
+                    // the softmax warps wait for pv_done before they touch P_t or O_t
+                    if (has_next) {
+                        issue_qk(stn);
+                        mma_commit(bars.s_full(t));
+                    } else {
+                        // every QK of the unit has been issued: the Q tiles are free once they
+                        // complete, so the next unit's Q loads during the last softmax and PV
+                        mma_commit(bars.q_empty());
+                    }
+                    issue_pv(st, j > 0 ? 1u : 0u);
                 }
                 __syncwarp();
-                if (has_next && !warp_wait(bars.k_full(stn), phn, abort_flag)) { ok = false; break; }
-                if (!warp_wait(bars.v_full(st), ph, abort_flag)) { ok = false; break; }
-                for (int t = 0; t < 2; ++t) {
-                    if (!warp_wait(bars.p_ready(t), g_it & 1, abort_flag)) { ok = false; break; }
-                    if (j == 0 && !warp_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        // the next S of this tile first (its softmax warps have read S_t), then
-                        // this tile's PV: the tensor pipe is in order, so S_t(j+1) is ready a PV
-                        // earlier; the softmax warps wait for pv_done before they touch P_t or O_t
-                        if (has_next) {
-                            issue_qk(t, stn);
-                            mma_commit(bars.s_full(t));
-                        }
-                        issue_pv(t, st, j > 0 ? 1u : 0u);
-                        mma_commit(bars.pv_done(t));
-                        if (t == 1) mma_commit(bars.v_empty(st));
-                        if (!has_next) mma_commit(bars.o_done(t));
-                    }
-                    __syncwarp();
+                pass_turn();
+                if (elect_one()) {
+                    mma_commit(bars.pv_done(t));
+                    mma_commit(bars.kv_empty(st));                  // QK_j and PV_j of this tile
+                    if (!has_next) mma_commit(bars.o_done(t));
                 }
-                if (!ok) break;
+                __syncwarp();
             }
             if (!ok) break;
         }
@@ -366,7 +436,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (elect_one()) mma_commit(bars.drain());
         __syncwarp();
         drain_wait(bars.drain(), 0);
-      }                                                 // warps 2-3: idle
+      }                                                 // warp 3: idle
     } else {
         regs_inc<REGS_SOFTMAX>();
         // ------------------------------------------------------------------ softmax + epilogue
@@ -423,88 +493,193 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         (xr.s_mean == -INFINITY ? 0.f : exp2f(xr.s_mean - m));
             }
 
-            for (int j = 0; j < n_kv; ++j, ++g_it) {
-                if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                float s[128];
-                ld_row128(tS, s);
-                tmem_wait_ld();
-                if (key_tile(j, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (c >= last_valid) s[c] = -INFINITY;
-                }
-                // row maximum: eight independent 16-column chains, then a small tree
-                float mx8[8];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
-#pragma unroll
-                    for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
-                    mx8[g] = fmaxf(a, s[16 * g + 15]);
-                }
-                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
-                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-                const float m_cand = mx * sl2;
-                const bool need = m_cand > m + kRescaleThreshold;
-                const bool rescale = __any_sync(0xffffffffu, need);
-                float alpha = 1.0f;
-                if (rescale) {
-                    const float m_new = fmaxf(m, m_cand);
-                    alpha = ex2_approx(m - m_new);               // 0 when m = -inf
-                    l *= alpha;
-                    m = m_new;
-                }
-                // P_t and O_t are free once this tile's previous PV has completed (it was issued
-                // after the QK that produced this S, so it is usually done already)
-                if (j > 0) {
-                    if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
+            // Long key ranges: exponentials against the current reference first (kLazy).  Short
+            // ones (a frame's dozen key tiles) keep the max-first step, which costs no extra pass
+            // over a unit's first key tile.
+            if constexpr (kLazy) {
+                // A row without the extra components has no reference max yet: the unit's first key
+                // tile sets it (to that tile's row maximum, as a max-first softmax would), so that
+                // the loop below can exponentiate against it right away.
+                if (__any_sync(0xffffffffu, m == -INFINITY)) {
+                    if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                }
-                // p = 2^(s * scale_log2 - m), two columns per packed FMA; P goes back to TMEM
-                // as bf16 pairs one 32-column chunk at a time
-                const uint64_t sc2 = f2_pack(sl2, sl2);
-                const uint64_t nm2 = f2_pack(-m, -m);
-                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                    float s[128];
+                    ld_row128(tS, s);
+                    tmem_wait_ld();
+                    if (key_tile(0, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
-                        const float p0 = ex2_approx(x0);
-                        const float p1 = ex2_approx(x1);
-                        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                        pk[i] = pack_bf16x2(p0, p1);
+                        for (int c = 0; c < 128; ++c)
+                            if (c >= last_valid) s[c] = -INFINITY;
                     }
-                    tmem_st16(tP + 16 * c, pk);
-                }
-                {
-                    float a0, a1;
-                    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
-                    l += a0 + a1;
-                }
-                // O *= alpha when the reference max moved (the logits are dead by now; the
-                // previous PV has completed); this tile's next PV waits for p_ready, so it sees
-                // both updates
-                if (rescale && j > 0) {
-                    uint32_t r[32];
+                    float mx8[8];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        tmem_ld32(tO + 32 * c, r);
-                        tmem_wait_ld();
+                    for (int g = 0; g < 8; ++g) {
+                        float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tO + 32 * c, r);
+                        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
+                        mx8[g] = fmaxf(a, s[16 * g + 15]);
                     }
+                    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                           max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                    if (m == -INFINITY) m = mx * sl2;
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bars.p_ready(t));
-            }
-            if (!ok) break;
 
+                for (int j = 0; j < n_kv; ++j, ++g_it) {
+                    if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    float s[128];
+                    ld_row128(tS, s);
+                    tmem_wait_ld();
+                    const bool ragged = key_tile(j, n_kv, u_local) == n_kv - 1 && last_valid < BN;   // warp-uniform
+                    if (ragged) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (c >= last_valid) s[c] = -INFINITY;
+                    }
+                    // p = 2^(s * scale_log2 - m) against the row's current reference max m, two
+                    // columns per packed FMA; P goes back to TMEM as bf16 pairs one 32-column chunk
+                    // at a time.  P_t and O_t are free once this tile's previous PV has completed;
+                    // that wait comes after the first chunk's exponentials (the PV was issued right
+                    // behind the QK that produced this S).  A row whose reference is not set yet
+                    // (m = -inf: the first key tile without the extra components) takes the exact
+                    // path at once.
+                    float tsum = 0.f;
+                    {
+                        const uint64_t sc2 = f2_pack(sl2, sl2);
+                        const uint64_t nm2 = f2_pack(-m, -m);
+                        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                float x0, x1;
+                                f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
+                                const float p0 = ex2_approx(x0);
+                                const float p1 = ex2_approx(x1);
+                                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                                pk[i] = pack_bf16x2(p0, p1);
+                            }
+                            if (c == 0 && j > 0) {
+                                if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
+                                tc_fence_after();
+                            }
+                            tmem_st16(tP + 16 * c, pk);
+                        }
+                        if (!ok) break;
+                        float a0, a1;
+                        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                        tsum = a0 + a1;
+                        // The reference max moves (and O is rescaled) only when a row's logits exceed
+                        // it by more than 2^kRescaleThreshold.  A row whose tile sum is at most
+                        // kSumTrigger = 2^7 has every p <= 2^7: its logits stay at least 1 below that
+                        // bound, a margin far above the rounding of the two computations, so the P
+                        // just stored is final.  Otherwise (rare: many large p) the decision is taken
+                        // exactly as a max-first softmax takes it, and P is recomputed when the
+                        // reference moves.
+                        if (__any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
+                            // the logits again from TMEM (S_t(j) stays intact until p_ready)
+                            float s2[128];
+                            ld_row128(tS, s2);
+                            tmem_wait_ld();
+                            if (ragged) {
+#pragma unroll
+                                for (int c = 0; c < 128; ++c)
+                                    if (c >= last_valid) s2[c] = -INFINITY;
+                            }
+                            tmem_wait_st();                              // the P stores above are done
+                            exact_tile(s2, tP, tO, sl2, j > 0, false, m, l, tsum);
+                        }
+                    }
+                    l += tsum;
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bars.p_ready(t));
+                }
+                if (!ok) break;
+            } else {
+                for (int j = 0; j < n_kv; ++j, ++g_it) {
+                    if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    float s[128];
+                    ld_row128(tS, s);
+                    tmem_wait_ld();
+                    if (key_tile(j, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (c >= last_valid) s[c] = -INFINITY;
+                    }
+                    // row maximum: eight independent 16-column chains, then a small tree
+                    float mx8[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
+#pragma unroll
+                        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
+                        mx8[g] = fmaxf(a, s[16 * g + 15]);
+                    }
+                    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                           max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                    const float m_cand = mx * sl2;
+                    const bool need = m_cand > m + kRescaleThreshold;
+                    const bool rescale = __any_sync(0xffffffffu, need);
+                    float alpha = 1.0f;
+                    if (rescale) {
+                        const float m_new = fmaxf(m, m_cand);
+                        alpha = ex2_approx(m - m_new);               // 0 when m = -inf
+                        l *= alpha;
+                        m = m_new;
+                    }
+                    // P_t and O_t are free once this tile's previous PV has completed (it was issued
+                    // after the QK that produced this S, so it is usually done already)
+                    if (j > 0) {
+                        if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    // p = 2^(s * scale_log2 - m), two columns per packed FMA; P goes back to TMEM
+                    // as bf16 pairs one 32-column chunk at a time
+                    const uint64_t sc2 = f2_pack(sl2, sl2);
+                    const uint64_t nm2 = f2_pack(-m, -m);
+                    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
+                            const float p0 = ex2_approx(x0);
+                            const float p1 = ex2_approx(x1);
+                            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                            pk[i] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tP + 16 * c, pk);
+                    }
+                    {
+                        float a0, a1;
+                        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                        l += a0 + a1;
+                    }
+                    // O *= alpha when the reference max moved (the logits are dead by now; the
+                    // previous PV has completed); this tile's next PV waits for p_ready, so it sees
+                    // both updates
+                    if (rescale && j > 0) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            tmem_ld32(tO + 32 * c, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(tO + 32 * c, r);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bars.p_ready(t));
+                }
+                if (!ok) break;
+            }
             // epilogue: O from TMEM, extra components, normalisation, store
             if (!warp_wait(bars.o_done(t), u_local & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();

@@ -25,7 +25,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool init = false;
     int sm_count = 0;
-    bool tc_ready[2][2] = {{false, false}, {false, false}};   // attn_tc_kernel<bias, rope> ready
+    bool tc_ready[2][2][2] = {};                               // attn_tc_kernel<bias, rope, lazy> ready
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -125,19 +125,30 @@ struct AttnProblem {
 // The tensor-core kernel instantiation for a bias setting, checked once per device: its
 // setmaxnreg split assumes exactly LAUNCH_REGS registers per thread at launch (any other count
 // would leave setmaxnreg.inc unsatisfiable), and it needs the large dynamic shared memory.
-template <bool kBias, bool kRope>
+template <bool kBias, bool kRope, bool kLazy>
 sga_status prepare_tc(DeviceInfo* di) {
     namespace T = sga::tc;
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (di->tc_ready[kBias][kRope]) return SGA_OK;
+    if (di->tc_ready[kBias][kRope][kLazy]) return SGA_OK;
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias, kRope>) != cudaSuccess) return SGA_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias, kRope, kLazy>) != cudaSuccess) return SGA_ERR_CUDA;
     if (fa.numRegs != (int)T::LAUNCH_REGS) return SGA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias, kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias, kRope, kLazy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_BYTES) != cudaSuccess)
         return SGA_ERR_CUDA;
-    di->tc_ready[kBias][kRope] = true;
+    di->tc_ready[kBias][kRope][kLazy] = true;
     return SGA_OK;
+}
+
+// Launch one instantiation of the tensor-core kernel.
+template <bool kBias, bool kRope, bool kLazy>
+sga_status launch_tc(DeviceInfo* di, long long grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                     const CUtensorMap& mv, const sga::tc::TcArgs& a, cudaStream_t stream) {
+    namespace T = sga::tc;
+    sga_status st = prepare_tc<kBias, kRope, kLazy>(di);
+    if (st != SGA_OK) return st;
+    T::attn_tc_kernel<kBias, kRope, kLazy><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+    return launch_status();
 }
 
 sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
@@ -154,9 +165,6 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         if (pb.seg_rows > 0x7FFFFFFFLL || pb.kv_rows > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
         namespace T = sga::tc;
         if (pb.bias && pb.rope) return SGA_ERR_UNSUPPORTED;
-        if ((st = pb.bias ? prepare_tc<true, false>(di) : pb.rope ? prepare_tc<false, true>(di)
-                                                               : prepare_tc<false, false>(di)) != SGA_OK)
-            return st;
         CUtensorMap mq, mk, mv;
         if ((st = make_map(&mq, pb.Q, pb.seg_rows, pb.n_seg)) != SGA_OK) return st;
         if ((st = make_map(&mk, pb.Kt, pb.kv_rows, pb.n_seg)) != SGA_OK) return st;
@@ -178,13 +186,17 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.inv_scale = 1.0f / pb.scale;
         a.drop_kv = pb.drop_kv;
         const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
+        // the exponentials-first softmax pays off over long key ranges; short ones (frame-local
+        // attention: 11 key tiles per frame) keep the max-first step
+        const bool lazy = a.n_kv_tiles >= T::kLazyMinKeyTiles;
         if (pb.bias)
-            T::attn_tc_kernel<true, false><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
-        else if (pb.rope)
-            T::attn_tc_kernel<false, true><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
-        else
-            T::attn_tc_kernel<false, false><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
-        return launch_status();
+            return lazy ? launch_tc<true, false, true>(di, grid, mq, mk, mv, a, stream)
+                        : launch_tc<true, false, false>(di, grid, mq, mk, mv, a, stream);
+        if (pb.rope)
+            return lazy ? launch_tc<false, true, true>(di, grid, mq, mk, mv, a, stream)
+                        : launch_tc<false, true, false>(di, grid, mq, mk, mv, a, stream);
+        return lazy ? launch_tc<false, false, true>(di, grid, mq, mk, mv, a, stream)
+                    : launch_tc<false, false, false>(di, grid, mq, mk, mv, a, stream);
     }
     if (kern != SGA_KERNEL_SIMT) return SGA_ERR_INVALID_ARG;
     sga::SimtArgs a;
