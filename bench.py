@@ -1,6 +1,6 @@
 """Benchmark of one SGA layer (compaction + attention) on B300: prints one JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload headline|vggt|long|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME | --workload sweep]
                     [--impl ours|reference] [--no-e2e] [--no-cpu]
 
 A step is one pass of the whole hot path over one layer of synthetic input: the compaction of
@@ -40,6 +40,10 @@ WORKLOADS = {
                           "bf16, sigma=4 (2,2), frame 0 and special tokens dense, diagonal + mean "
                           "(leave-one-out, ln count bias)",
                      cfg=dict(B=1, H=16, N=800, sigma=4)),
+    "headline_phase": dict(kind="sga",
+                           desc="SGA layer with the per-frame phase-shifted grid: N=800 frames x 1374 tokens, "
+                                "H=16, d=64, bf16, sigma=4 (2,2), frame 0 and special tokens dense, diagonal + mean",
+                           cfg=dict(B=1, H=16, N=800, sigma=4, phase_shift=True)),
     "vggt": dict(kind="sga", desc="SGA layer: N=32 frames x 1374 tokens, H=16, d=64, bf16, sigma=4, diag+mean",
                  cfg=dict(B=1, H=16, N=32, sigma=4)),
     "long": dict(kind="sga", desc="SGA layer: N=200 frames x 1374 tokens, H=16, d=64, bf16, sigma=9 (3,3), diag+mean",
@@ -188,6 +192,13 @@ def _max_over_ranks(x: float, world: int, dev) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def _percentiles(xs):
+    """p10 / p50 / p90 (linear interpolation) and the mean of a list of times."""
+    a = np.sort(np.asarray(xs, dtype=np.float64))
+    q = lambda f: float(np.interp(f * (len(a) - 1), np.arange(len(a)), a))
+    return {"p10": q(0.1), "p50": q(0.5), "p90": q(0.9), "mean": float(a.mean()), "n": int(len(a))}
 
 
 def layer_flops(cfg, S: int) -> float:
@@ -453,6 +464,11 @@ def run_ours(args):
     total_ms = _max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     stage_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
                 for i, (name, _) in enumerate(job.stages)}
+    # spread of the per-step device times (every step bracketed by its own events)
+    step_times = [e[0].elapsed_time(e[n_st]) for e in evs]
+    spread = {"step": _percentiles(step_times)}
+    for i, (name, _) in enumerate(job.stages):
+        spread[name] = _percentiles([e[i].elapsed_time(e[i + 1]) for e in evs])
     clocks = clk.summary()
 
     ms_step = total_ms / args.steps
@@ -471,7 +487,7 @@ def run_ours(args):
                 "frac_of_burst": achieved / peaks["bf16"], "burst_peak": peaks["bf16"],
                 "traffic": traffic * 1e9 if traffic is not None else None,
                 "traffic_unit": "bytes per launch (dram read + write, ncu)", "kernel_fingerprint": fp,
-                "kernel_ms": d_ms}
+                "kernel_ms": d_ms, "kernel_ms_p50": spread[d_name]["p50"]}
     secondary = None
     if "merge" in stage_ms:
         secondary = {"kernel": "sga::merge_kernel<bf16>", "ms": stage_ms["merge"]}
@@ -487,20 +503,32 @@ def run_ours(args):
         host_in = [x.cpu().pin_memory() for x in job.inputs]
         oh = torch.empty(job.out.shape, dtype=job.out.dtype, pin_memory=True)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if job.kind == "sga":
+        if job.kind in ("sga", "dense", "frame", "bias"):
             # streamed: batch i+1's inputs are copied in and batch i-1's output copied out while
-            # batch i is computed (HostStream); every step still moves all its bytes
-            hs = job.sga.HostStream(job.plan)
+            # batch i is computed (the library's host-streaming executor); every step still moves
+            # all its bytes
+            if job.kind == "sga":
+                hs = job.sga.HostStream(job.plan)
+                submit = lambda: hs.submit(*host_in, oh)
+            else:
+                sh = job.wl["shape"]
+                if job.kind == "bias":
+                    hs = job.sga.PlainHostStream("bias", 1, sh["H"], sh["Tq"], Tk=sh["Tk"])
+                    submit = lambda: hs.submit(*host_in[:3], oh, bias_host=host_in[3])
+                else:
+                    T = sh["N"] * sh["L"]
+                    hs = job.sga.PlainHostStream(job.kind, 1, sh["H"], T, N=sh["N"], L=sh["L"])
+                    submit = lambda: hs.submit(*host_in, oh)
             for _ in range(2):
-                hs.submit(*host_in, oh)
+                submit()
             hs.synchronize()
             torch.cuda.synchronize(dev)
             _barrier(world)
             a.record(hs.h2d)
             for _ in range(args.steps):
-                hs.submit(*host_in, oh)
+                submit()
             b.record(hs.d2h)
-            e2e_mode = "streamed (HostStream: copies overlap the previous/next step's compute)"
+            e2e_mode = "streamed (host-streaming executor: copies overlap the previous/next step's compute)"
         else:
             for _ in range(2):
                 job.e2e_call(host_in, oh)
@@ -514,12 +542,17 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         _barrier(world)
         e_ms = _max_over_ranks(a.elapsed_time(b), world, dev) / args.steps
-        if job.kind == "sga":
+        if job.kind in ("sga", "dense", "frame", "bias"):
             hs.synchronize()
             hs.close()
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = oh.numel() * oh.element_size()
+        # with copies overlapping compute a step costs max(copy-in time, compute, copy-out time):
+        # when the step takes well over the device time, the host link is what binds
+        bound = "copies (host link)" if e_ms > 1.25 * ms_step else "compute"
         e2e = {"value": world * job.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host_in),
-               "d2h_bytes_per_step": oh.numel() * oh.element_size(), "mode": e2e_mode}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode, "bound": bound,
+               "h2d_gbs": h2d / (e_ms * 1e-3) / 1e9, "device_ms_per_step": ms_step}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -532,7 +565,8 @@ def run_ours(args):
     config = {"workload": wl["desc"], **job.config,
               "l2": "inputs larger than L2 (Q %.2f GB); no flush" % (q.numel() * q.element_size() / 1e9)
               if q.numel() * q.element_size() > 126e6 else "inputs smaller than L2: steady-state, L2-warm",
-              "parallelism": f"dp{world} (independent layers per rank)", "stage_ms": stage_ms}
+              "parallelism": f"dp{world} (independent layers per rank)", "stage_ms": stage_ms,
+              "ms_spread": spread}
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -544,6 +578,97 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def _time_stages(stages, warmup, steps, dev):
+    """Per-step CUDA-event times (ms) of each stage, on the current stream, after `warmup` steps."""
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        for _, fn in stages:
+            fn()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(steps)]
+    torch.cuda._sleep(int(2e6 * (2 + steps)))
+    for e in evs:
+        for i, (_, fn) in enumerate(stages):
+            e[i].record(stream)
+            fn()
+        e[len(stages)].record(stream)
+    torch.cuda.synchronize(dev)
+    return {name: [e[i].elapsed_time(e[i + 1]) for e in evs] for i, (name, _) in enumerate(stages)}
+
+
+SWEEP_N, SWEEP_H, SWEEP_SIGMAS = 100, 16, (1, 2, 4, 6, 9)
+
+
+def run_sweep(args):
+    """The 100-frame sweep: sigma in {1, 2, 4, 6, 9} x fixed / phase-shifted grid x diagonal and
+    mean terms on / off, plus frame-local attention as the dense-per-frame baseline.  One JSON
+    line per configuration (median of the per-step device times), then a summary line with the
+    measured dense / SGA time ratios beside the FLOP ratios that bound them."""
+    import subsampled_global_attention_sga_b300 as sga
+    from subsampled_global_attention_sga_b300.inputs import correlated_qkv
+    rank, world, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    N, H = SWEEP_N, SWEEP_H
+    L = sga.SGAConfig(B=1, H=H, N=N).L
+    q, k, v = correlated_qkv(1, H, N, L, 64, seed=3 * rank, dtype=torch.bfloat16, device=dev)
+    cases = [(s_, ph, terms) for s_ in SWEEP_SIGMAS for ph in (False, True) for terms in (True, False)
+             if not (s_ == 1 and ph)]
+    lines, att_ms = [], {}
+    with Clocks(dev.index) as clk:
+        for sigma, ph, terms in cases:
+            cfg = sga.SGAConfig(B=1, H=H, N=N, sigma=sigma, phase_shift=ph, diag=terms, mean=terms)
+            plan = sga.Plan(cfg, dev)
+            bufs = plan.compact(k, v)
+            out = torch.empty_like(q)
+            t = _time_stages([("compaction", lambda: plan.compact(k, v, *bufs)),
+                              ("attention", lambda: plan.forward(q, k, v, *bufs, out=out))],
+                             args.warmup, args.steps, dev)
+            if sga.device_status(dev) != 0:
+                raise RuntimeError("device status not OK")
+            flops = layer_flops(cfg, plan.S)
+            a50, c50 = _percentiles(t["attention"])["p50"], _percentiles(t["compaction"])["p50"]
+            att_ms[(sigma, ph, terms)] = a50
+            lines.append({
+                "metric": f"sweep N={N}: SGA ms/layer and effective TFLOP/s", "sigma": sigma, "phase_shift": ph,
+                "diag_mean": terms, "T": cfg.T, "S": plan.S, "flops_per_layer": flops,
+                "ms_per_layer": a50 + c50, "attention_ms": _percentiles(t["attention"]),
+                "compaction_ms": _percentiles(t["compaction"]), "tflops": flops / ((a50 + c50) * 1e-3) / 1e12,
+                "attention_tflops": flops / (a50 * 1e-3) / 1e12,
+                "frac_of_burst": flops / (a50 * 1e-3) / 1e12 / peaks["bf16"],
+                "frac_of_sustained": flops / (a50 * 1e-3) / 1e12 / peaks["bf16_sus"],
+                "compaction_gbs": compaction_bytes(cfg, plan.S) / (c50 * 1e-3) / 1e9})
+            plan.close()
+            del bufs, out
+        out = torch.empty_like(q)
+        t = _time_stages([("attention", lambda: sga.frame_forward(q, k, v, N, L, out=out))], args.warmup,
+                         args.steps, dev)
+        f50 = _percentiles(t["attention"])["p50"]
+        fflops = 4.0 * N * L * L * 64 * H
+        lines.append({"metric": f"sweep N={N}: frame-local attention ms/layer and TFLOP/s", "kind": "frame-local",
+                      "T": N * L, "flops_per_layer": fflops, "ms_per_layer": f50,
+                      "attention_ms": _percentiles(t["attention"]), "tflops": fflops / (f50 * 1e-3) / 1e12,
+                      "frac_of_burst": fflops / (f50 * 1e-3) / 1e12 / peaks["bf16"]})
+    if rank != 0:
+        return
+    for ln in lines:
+        print(json.dumps(ln), flush=True)
+    dense = att_ms[(1, False, True)]
+    ratios = {}
+    for sigma in SWEEP_SIGMAS[1:]:
+        for ph in (False, True):
+            key = (sigma, ph, True)
+            row = next(x for x in lines if x.get("sigma") == sigma and x.get("phase_shift") == ph and x.get("diag_mean"))
+            dense_row = next(x for x in lines if x.get("sigma") == 1)
+            ratios[f"sigma{sigma}{'_phase' if ph else ''}"] = {
+                "measured_dense_over_sga": dense / att_ms[key],
+                "flop_bound": dense_row["flops_per_layer"] / row["flops_per_layer"]}
+    print(json.dumps({"metric": f"sweep N={N}: dense / SGA attention time", "ratios": ratios,
+                      "frame_local_over_dense": f50 / dense, "clocks": clk.summary(), "steps": args.steps,
+                      "warmup": args.warmup, "peaks": peaks}), flush=True)
+
+
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, on a bounded sample of the workload (rank 0 only)."""
     rank, world, _ = (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0)
@@ -552,7 +677,7 @@ def run_reference(args):
     import oracle
     import subsampled_global_attention_sga_b300 as sga
     from subsampled_global_attention_sga_b300.inputs import correlated_qkv
-    wl = WORKLOADS[args.workload]
+    wl = WORKLOADS.get(args.workload, {"kind": "sweep"})
     if wl["kind"] != "sga":
         print(json.dumps({"impl": "reference", "unavailable": "the CPU reference arm covers the SGA workloads"}))
         return
@@ -594,7 +719,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="headline")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["sweep"], default="headline")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -603,6 +728,8 @@ def main(argv=None):
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "sweep":
+        run_sweep(args)
     else:
         run_ours(args)
     if torch.distributed.is_available() and torch.distributed.is_initialized():

@@ -56,7 +56,8 @@ typedef enum {
     SGA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (launch, memcpy, ...) */
     SGA_ERR_TIMEOUT = 5,        /* a kernel's bounded wait expired (reported by device status) */
     SGA_ERR_PLAN_MISMATCH = 6,  /* plan used with another device or a destroyed plan */
-    SGA_ERR_SCRATCH_LIMIT = 7   /* problem larger than sga_compact_noalloc's fixed scratch */
+    SGA_ERR_SCRATCH_LIMIT = 7,  /* problem larger than sga_compact_noalloc's fixed scratch */
+    SGA_ERR_DEBUG_CHECK = 8     /* debug builds only: a kernel's index check failed (access skipped) */
 } sga_status;
 
 typedef enum { SGA_BF16 = 0, SGA_F32 = 1 } sga_dtype;
@@ -252,10 +253,11 @@ sga_status sga_unmerge(const sga_merge_config* cfg, const int32_t* map, const vo
  * dropped rows -- in a fixed array inside the library.
  *
  * Results are those of sga_compact with a plan for `cfg`: K_S, V_S [B, H, |S|, 64] get the
- * kept rows of K, V [B, H, T, 64] in ascending token order (|S| from sga_plan_host or
- * sga_plan_info), and k_sum, v_sum (fp32 [B, H, 64]) get the sums of the dropped rows.  All
- * pointers are caller-owned device memory, 16-byte aligned.  No cudaMalloc, cudaFree or other
- * allocating call is made.
+ * kept rows of K, V [B, H, T, 64] in ascending token order, and k_sum, v_sum (fp32 [B, H, 64])
+ * get the sums of the dropped rows.  |S| comes from sga_kept_count (or sga_plan_host /
+ * sga_plan_info); the call receives no buffer sizes, so the caller must size K_S and V_S by
+ * it (the Python binding checks this before the call).  All pointers are caller-owned device
+ * memory, 16-byte aligned.  No cudaMalloc, cudaFree or other allocating call is made.
  *
  * No rotary embedding: a configuration with rope = 1 returns SGA_ERR_UNSUPPORTED.
  *
@@ -265,13 +267,23 @@ sga_status sga_unmerge(const sga_merge_config* cfg, const int32_t* map, const vo
  * with 16 heads (T = 1,099,200) needs 8592.
  *
  * The first call on a device looks up the scratch array's device address (once per device,
- * with that device current); make that first call before any stream capture.  Every call on a
- * device shares the one scratch array, so calls that may overlap on the GPU (other streams,
- * other host threads) race and must be serialised by the caller.  The array keeps the last
+ * with that device current); make that first call before any stream capture.  The address is
+ * cached with the id of the context it belongs to: after a device reset (a new primary context)
+ * the next call looks it up again.  Every call on a device shares the one scratch array, so
+ * calls that may overlap on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller.  The array keeps the last
  * call's contents; nothing in it needs to start at zero because each call overwrites every
  * partial it reads. */
 sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, const void* V, void* K_S,
                                void* V_S, float* k_sum, float* v_sum, void* stream);
+
+/* |S| of `cfg` in closed form (host only, allocates nothing): per frame, L tokens when the frame
+ * is kept whole, else n_special + ceil((grid_h - phi_r) / s_h) * ceil((grid_w - phi_c) / s_w)
+ * with the frame's phase (phi_r, phi_c).  Equals sga_plan_info's S for a plan of `cfg`.  The
+ * buffers K_S and V_S given to sga_compact_noalloc must hold exactly this many rows per (b, h):
+ * the call receives no sizes and cannot check them itself.  SGA_ERR_INVALID_ARG for a bad
+ * configuration or a NULL S. */
+sga_status sga_kept_count(const sga_config* cfg, int64_t* S);
 
 /* Streaming from host memory (no counterpart on the pages; the executor that feeds the layer
  * from host buffers).  A stream object owns, for one plan, `depth` sets of device tensors (Q, K,
@@ -292,6 +304,26 @@ typedef struct sga_stream_s* sga_stream_t;
 sga_status sga_stream_create(sga_plan_t plan, int depth, sga_stream_t* out);
 sga_status sga_stream_submit(sga_stream_t s, const void* Q_host, const void* K_host, const void* V_host,
                              void* O_host, float scale);
+/* The same executor for the plain attention calls: dense global attention (sga_dense_forward),
+ * frame-local attention (sga_frame_forward) and size-aware attention (sga_bias_forward).
+ * spec->kind picks the call; B, H, head_dim, dtype and kernel are its arguments; Tq is the query
+ * (and output) rows per (b, h); Tk the key rows (SGA_PLAIN_BIAS only, else Tq is used); N and L
+ * the frames and tokens per frame (SGA_PLAIN_FRAME only, N*L = Tq).  A stream object made here
+ * takes sga_stream_submit_plain (sga_stream_submit refuses it, and the other way round); it
+ * uses the device current at creation.  sga_stream_submit_plain copies K, V, the bias (host fp32
+ * [B, H, Tk]; SGA_PLAIN_BIAS only, else NULL) and Q in, runs the call once they have arrived and
+ * copies O [B, H, Tq, 64] back, overlapping consecutive submits like sga_stream_submit. */
+typedef enum { SGA_PLAIN_DENSE = 1, SGA_PLAIN_FRAME = 2, SGA_PLAIN_BIAS = 3 } sga_plain_kind;
+typedef struct {
+    int kind;                /* sga_plain_kind */
+    int B, H;
+    int64_t Tq, Tk;
+    int N, L;
+    int head_dim, dtype, kernel;
+} sga_plain_spec;
+sga_status sga_stream_create_plain(const sga_plain_spec* spec, int depth, sga_stream_t* out);
+sga_status sga_stream_submit_plain(sga_stream_t s, const void* Q_host, const void* K_host, const void* V_host,
+                                   const float* bias_host, void* O_host, float scale);
 /* Wait until every submitted layer's output is in its host buffer. */
 sga_status sga_stream_synchronize(sga_stream_t s);
 /* The object's CUDA streams (cudaStream_t), e.g. to record timing events around submits:
@@ -305,6 +337,12 @@ void sga_stream_destroy(sga_stream_t s);
  * synchronisation itself failed. */
 sga_status sga_device_status(void* stream);
 
+/* The same read for the device of `plan` (which must be current): SGA_ERR_PLAN_MISMATCH for an
+ * invalid plan or another current device, else the result of sga_device_status(stream).  The
+ * status word is per device, not per plan: it reports every library kernel that ran on the
+ * device since the last read. */
+sga_status sga_last_device_status(sga_plan_t plan, void* stream);
+
 /* Failure-detection self-test of the bounded waits (no counterpart on the pages; it checks
  * the error path of this library).  Runs the tensor-core attention kernel on a small dense
  * problem (buffers of its own, allocated and freed here) in which the TMA producer never loads
@@ -314,6 +352,16 @@ sga_status sga_device_status(void* stream);
  * -- and the kernel records SGA_ERR_TIMEOUT.  Synchronises `stream` and returns the status it
  * read (and cleared): SGA_ERR_TIMEOUT when the mechanism works.  The context stays usable. */
 sga_status sga_selftest_timeout(void* stream);
+
+/* Debug builds of the library (compiled with -DSGA_DEBUG; sga_build_info then contains "debug")
+ * check every indexed store of the compaction, attention, merge and unmerge kernels, and the
+ * index reads that steer them, against the buffer's bound; a failed check skips the access,
+ * sets the device status word to SGA_ERR_DEBUG_CHECK and records the first failure.  This call
+ * copies that record to the host and clears it: `site` (the check that failed: 1-2 compaction,
+ * 10-12 attention, 20-23 merging), the offending `index`, its `bound`, and `count`, the number of
+ * failed checks.  Any output pointer may be NULL.  Synchronous.  A normal build returns
+ * SGA_ERR_UNSUPPORTED. */
+sga_status sga_debug_report(int64_t* site, int64_t* index, int64_t* bound, int64_t* count);
 
 /* Static description of a status code. */
 const char* sga_status_string(sga_status s);

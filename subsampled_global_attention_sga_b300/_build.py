@@ -1,4 +1,5 @@
-"""Build libsga.so in-tree with nvcc for sm_103a (one translation unit, static cudart)."""
+"""Build libsga.so in-tree with nvcc for sm_103a (one translation unit, static cudart), and its
+debug twin libsga_debug.so (-DSGA_DEBUG: every kernel checks its indexed stores)."""
 from __future__ import annotations
 
 import glob
@@ -10,6 +11,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libsga.so")
+LIB_DEBUG = os.path.join(PKG, "libsga_debug.so")
 HEADER = os.path.join(ROOT, "include", "sga.h")
 
 NVCC_FLAGS = [
@@ -35,27 +37,31 @@ def source_hash(csrc: str = CSRC, header: str = HEADER) -> str:
     return h.hexdigest()[:16]
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(debug: bool = False) -> bool:
+    lib = LIB_DEBUG if debug else LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(s) > t for s in _sources())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    lib = LIB_DEBUG if debug else LIB
+    if not force and not needs_build(debug):
+        return lib
     nvcc = os.environ.get("NVCC", "nvcc")
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, *NVCC_FLAGS, f'-DSGA_SOURCE_HASH="{source_hash()}"', "-o", tmp, os.path.join(CSRC, "sga.cu")]
+    tmp = lib + ".tmp"
+    cmd = [nvcc, *NVCC_FLAGS, f'-DSGA_SOURCE_HASH="{source_hash()}"', *(["-DSGA_DEBUG"] if debug else []),
+           "-o", tmp, os.path.join(CSRC, "sga.cu")]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
     if verbose:
         print(res.stdout + res.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     build(force=True, verbose=True)
+    build(force=True, verbose=True, debug=True)

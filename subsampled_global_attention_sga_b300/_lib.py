@@ -5,12 +5,14 @@ import ctypes
 import os
 
 from . import _build
-from ._build import LIB
+from ._build import LIB, LIB_DEBUG
 
 SGA_OK = 0
+SGA_ERR_CUDA, SGA_ERR_TIMEOUT, SGA_ERR_PLAN_MISMATCH = 4, 5, 6
 STATUS_NAMES = {
     0: "SGA_OK", 1: "SGA_ERR_INVALID_ARG", 2: "SGA_ERR_UNSUPPORTED", 3: "SGA_ERR_ALIGNMENT",
     4: "SGA_ERR_CUDA", 5: "SGA_ERR_TIMEOUT", 6: "SGA_ERR_PLAN_MISMATCH", 7: "SGA_ERR_SCRATCH_LIMIT",
+    8: "SGA_ERR_DEBUG_CHECK",
 }
 SGA_BF16, SGA_F32 = 0, 1
 SGA_MEAN_LOO, SGA_MEAN_GLOBAL = 0, 1
@@ -24,7 +26,8 @@ EXPORTS = (
     "sga_plan_host_general", "sga_plan_create_from_index", "sga_rope2d",
     "sga_merge_size", "sga_merge", "sga_unmerge", "sga_selftest_timeout",
     "sga_stream_create", "sga_stream_submit", "sga_stream_synchronize", "sga_stream_handles",
-    "sga_stream_destroy",
+    "sga_stream_destroy", "sga_kept_count", "sga_last_device_status",
+    "sga_stream_create_plain", "sga_stream_submit_plain", "sga_debug_report",
 )
 
 
@@ -46,6 +49,15 @@ class SgaMergeConfig(ctypes.Structure):
         "B", "H", "N", "grid_h", "grid_w", "n_special", "head_dim", "n_t", "n_s", "r_permille", "dtype")]
 
 
+class SgaPlainSpec(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("B", ctypes.c_int), ("H", ctypes.c_int), ("Tq", ctypes.c_int64),
+                ("Tk", ctypes.c_int64), ("N", ctypes.c_int), ("L", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("kernel", ctypes.c_int)]
+
+
+SGA_PLAIN_DENSE, SGA_PLAIN_FRAME, SGA_PLAIN_BIAS = 1, 2, 3
+
+
 class SgaError(RuntimeError):
     def __init__(self, call: str, status: int):
         self.status = status
@@ -62,13 +74,20 @@ def _describe(status: int) -> str:
         return "?"
 
 
+def library_path() -> str:
+    """The library this process loads: libsga.so, or its debug build (every kernel checks its
+    indexed stores) when the environment sets SGA_LIBRARY=debug."""
+    return LIB_DEBUG if os.environ.get("SGA_LIBRARY", "") == "debug" else LIB
+
+
 def lib():
     """Load libsga.so (built in-tree by ``__graft_entry__.build()``); raise if it is missing."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB):
-            raise RuntimeError(f"libsga.so is not built ({LIB}); run __graft_entry__.build()")
-        L = ctypes.CDLL(LIB)
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
         vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
         cfgp = ctypes.POINTER(SgaConfig)
         sig = {
@@ -91,6 +110,8 @@ def lib():
             "sga_merge": (i32, [ctypes.POINTER(SgaMergeConfig), vp, vp, vp, vp, vp, vp, vp]),
             "sga_unmerge": (i32, [ctypes.POINTER(SgaMergeConfig), vp, vp, vp, vp]),
             "sga_device_status": (i32, [vp]),
+            "sga_last_device_status": (i32, [vp, vp]),
+            "sga_kept_count": (i32, [cfgp, ctypes.POINTER(i64)]),
             "sga_status_string": (ctypes.c_char_p, [i32]),
             "sga_build_info": (ctypes.c_char_p, []),
             "sga_stream_create": (i32, [vp, i32, ctypes.POINTER(vp)]),
@@ -98,6 +119,9 @@ def lib():
             "sga_stream_synchronize": (i32, [vp]),
             "sga_stream_handles": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp)]),
             "sga_stream_destroy": (None, [vp]),
+            "sga_debug_report": (i32, [ctypes.POINTER(i64)] * 4),
+            "sga_stream_create_plain": (i32, [ctypes.POINTER(SgaPlainSpec), i32, ctypes.POINTER(vp)]),
+            "sga_stream_submit_plain": (i32, [vp, vp, vp, vp, vp, vp, f32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -235,15 +235,27 @@ class Plan:
         return self.forward(Q, K, V, K_S, V_S, k_sum, v_sum, out=out, lse=lse, scale=scale)
 
 
+def kept_count(cfg: SGAConfig) -> int:
+    """|S| of a layer configuration, from the library's closed form (host only)."""
+    c = cfg.to_c()
+    n = ctypes.c_int64(0)
+    check("sga_kept_count", lib().sga_kept_count(ctypes.byref(c), ctypes.byref(n)))
+    return n.value
+
+
 def compact_noalloc(cfg: SGAConfig, K, V, K_S, V_S, k_sum, v_sum):
     """Compaction through ``sga_compact_noalloc``: no plan and no device allocation inside the
-    library (its scratch is a fixed array in the library; see include/sga.h).  Every output is
-    passed in by the caller; K_S/V_S are [B, H, |S|, 64] with |S| from ``plan_host``."""
+    library (its scratch is a fixed array in the library).  Every output is passed in by the
+    caller on the inputs' CUDA device; K_S/V_S must be [B, H, |S|, 64] with |S| =
+    ``kept_count(cfg)``: the C call receives no buffer sizes, so a wrong shape is refused here,
+    before anything is launched."""
     dev = K.device
+    if dev.type != "cuda":
+        raise ValueError(f"K: on {dev}, expected a CUDA device")
     shp = (cfg.B, cfg.H, cfg.T, 64)
     _check_tensor("K", K, shp, cfg.torch_dtype, dev)
     _check_tensor("V", V, shp, cfg.torch_dtype, dev)
-    S = K_S.shape[2]
+    S = kept_count(cfg)
     for n, t in (("K_S", K_S), ("V_S", V_S)):
         _check_tensor(n, t, (cfg.B, cfg.H, S, 64), cfg.torch_dtype, dev)
     for n, t in (("k_sum", k_sum), ("v_sum", v_sum)):
@@ -402,6 +414,16 @@ def merged_attention(mcfg: MergeConfig, Q, K, V, *, merge_queries=False, scale=N
     return unmerge(mcfg, mq, Om)
 
 
+def last_device_status(plan: "Plan") -> int:
+    """``sga_last_device_status``: synchronise the current stream of the plan's device and
+    return (and clear) that device's kernel status word; raises for an invalid plan."""
+    with torch.cuda.device(plan.device):
+        st = int(lib().sga_last_device_status(plan._h, _stream(plan.device)))
+    if st in (_lib.SGA_ERR_PLAN_MISMATCH, _lib.SGA_ERR_CUDA):
+        check("sga_last_device_status", st)
+    return st
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device's kernel status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
@@ -409,19 +431,15 @@ def device_status(device=None) -> int:
         return int(lib().sga_device_status(_stream(dev)))
 
 
-class HostStream:
-    """Streams SGA layers from pinned host memory through one plan (``sga_stream_*``): the
-    library double-buffers the device tensors and runs host-to-device copies, compute and
-    device-to-host copies on three CUDA streams of its own, so layer i+1's inputs and layer
-    i-1's output move while layer i computes (K and V first, so the compaction starts while Q is
-    in flight).  Each output equals ``Plan.layer`` on the same inputs.  ``h2d`` and ``d2h`` are
-    the library's first and last streams, for timing events."""
+class _Streamer:
+    """Common part of the host-streaming executors (``sga_stream_*``): the library owns the
+    device buffer sets and three CUDA streams (copies in, compute, copies out); ``h2d`` and
+    ``d2h`` are its first and last streams, for timing events."""
 
-    def __init__(self, plan: Plan, depth: int = 2):
-        self.plan, self.device = plan, plan.device
+    def _attach(self, create):
         self._h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
-            check("sga_stream_create", lib().sga_stream_create(plan._h, int(depth), ctypes.byref(self._h)))
+            create(ctypes.byref(self._h))
             a, b, c = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
             check("sga_stream_handles", lib().sga_stream_handles(self._h, ctypes.byref(a), ctypes.byref(b),
                                                                  ctypes.byref(c)))
@@ -429,21 +447,6 @@ class HostStream:
             self.compute = torch.cuda.ExternalStream(b.value, device=self.device)
             self.d2h = torch.cuda.ExternalStream(c.value, device=self.device)
         self._keep = []          # host tensors of queued layers, held until synchronize
-
-    def submit(self, Q_host, K_host, V_host, out_host, scale=None):
-        """Queue one layer: out_host <- SGA(Q_host, K_host, V_host).  Returns immediately; the
-        host tensors (CPU, contiguous, pinned for overlap) must stay untouched until
-        ``synchronize``."""
-        cfg = self.plan.cfg
-        shp = (cfg.B, cfg.H, self.plan.T, 64)
-        for n, t in (("Q", Q_host), ("K", K_host), ("V", V_host), ("out", out_host)):
-            _check_tensor(n, t, shp, cfg.torch_dtype, torch.device("cpu"))
-        with torch.cuda.device(self.device):
-            check("sga_stream_submit", lib().sga_stream_submit(
-                self._h, _ptr(Q_host), _ptr(K_host), _ptr(V_host), _ptr(out_host),
-                ctypes.c_float(0.0 if scale is None else float(scale))))
-        self._keep.append((Q_host, K_host, V_host, out_host))
-        return out_host
 
     def synchronize(self):
         """Wait until every submitted layer's output is in its host buffer."""
@@ -462,6 +465,77 @@ class HostStream:
             self.close()
         except Exception:
             pass
+
+
+class HostStream(_Streamer):
+    """Streams SGA layers from pinned host memory through one plan (``sga_stream_*``): the
+    library double-buffers the device tensors and runs host-to-device copies, compute and
+    device-to-host copies on three CUDA streams of its own, so layer i+1's inputs and layer
+    i-1's output move while layer i computes (K and V first, so the compaction starts while Q is
+    in flight).  Each output equals ``Plan.layer`` on the same inputs."""
+
+    def __init__(self, plan: Plan, depth: int = 2):
+        self.plan, self.device = plan, plan.device
+        self._attach(lambda h: check("sga_stream_create", lib().sga_stream_create(plan._h, int(depth), h)))
+
+    def submit(self, Q_host, K_host, V_host, out_host, scale=None):
+        """Queue one layer: out_host <- SGA(Q_host, K_host, V_host).  Returns immediately; the
+        host tensors (CPU, contiguous, pinned for overlap) must stay untouched until
+        ``synchronize``."""
+        cfg = self.plan.cfg
+        shp = (cfg.B, cfg.H, self.plan.T, 64)
+        for n, t in (("Q", Q_host), ("K", K_host), ("V", V_host), ("out", out_host)):
+            _check_tensor(n, t, shp, cfg.torch_dtype, torch.device("cpu"))
+        with torch.cuda.device(self.device):
+            check("sga_stream_submit", lib().sga_stream_submit(
+                self._h, _ptr(Q_host), _ptr(K_host), _ptr(V_host), _ptr(out_host),
+                ctypes.c_float(0.0 if scale is None else float(scale))))
+        self._keep.append((Q_host, K_host, V_host, out_host))
+        return out_host
+
+
+_PLAIN_KINDS = {"dense": _lib.SGA_PLAIN_DENSE, "frame": _lib.SGA_PLAIN_FRAME, "bias": _lib.SGA_PLAIN_BIAS}
+
+
+class PlainHostStream(_Streamer):
+    """The host-streaming executor for the plain attention calls (``sga_stream_create_plain``):
+    kind "dense" (``dense_forward``), "frame" (``frame_forward``, N frames of L tokens) or
+    "bias" (``bias_forward``, Tk keys with an fp32 bias).  Each output equals the device call
+    on the same inputs."""
+
+    def __init__(self, kind: str, B: int, H: int, Tq: int, *, Tk: int | None = None, N: int = 0, L: int = 0,
+                 dtype: str = "bf16", kernel: str = "auto", depth: int = 2, device=None):
+        if kind not in _PLAIN_KINDS:
+            raise ValueError(f"kind must be one of {sorted(_PLAIN_KINDS)}")
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.kind, self.B, self.H, self.Tq = kind, B, H, Tq
+        self.Tk = Tk if (kind == "bias" and Tk is not None) else Tq
+        self.dtype = dtype
+        spec = _lib.SgaPlainSpec()
+        spec.kind, spec.B, spec.H, spec.Tq, spec.Tk = _PLAIN_KINDS[kind], B, H, Tq, self.Tk
+        spec.N, spec.L, spec.head_dim = N, L, 64
+        spec.dtype, spec.kernel = _DTYPES[dtype][0], _KERNELS[kernel]
+        self._attach(lambda h: check("sga_stream_create_plain",
+                                     lib().sga_stream_create_plain(ctypes.byref(spec), int(depth), h)))
+
+    def submit(self, Q_host, K_host, V_host, out_host, bias_host=None, scale=None):
+        """Queue one call: out_host <- attention(Q_host, K_host, V_host[, bias_host]).  Host
+        tensors (CPU, contiguous, pinned for overlap) must stay untouched until ``synchronize``."""
+        tdt, cpu = _DTYPES[self.dtype][1], torch.device("cpu")
+        _check_tensor("Q", Q_host, (self.B, self.H, self.Tq, 64), tdt, cpu)
+        _check_tensor("out", out_host, (self.B, self.H, self.Tq, 64), tdt, cpu)
+        for n, t in (("K", K_host), ("V", V_host)):
+            _check_tensor(n, t, (self.B, self.H, self.Tk, 64), tdt, cpu)
+        if (self.kind == "bias") != (bias_host is not None):
+            raise ValueError("bias_host is required for kind 'bias' and only for it")
+        if bias_host is not None:
+            _check_tensor("bias", bias_host, (self.B, self.H, self.Tk), torch.float32, cpu)
+        with torch.cuda.device(self.device):
+            check("sga_stream_submit_plain", lib().sga_stream_submit_plain(
+                self._h, _ptr(Q_host), _ptr(K_host), _ptr(V_host), _ptr(bias_host), _ptr(out_host),
+                ctypes.c_float(0.0 if scale is None else float(scale))))
+        self._keep.append((Q_host, K_host, V_host, bias_host, out_host))
+        return out_host
 
 
 def layer_from_host(plan: Plan, Q_host, K_host, V_host, out_host=None, scale=None):

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kSimtRows) attn_simt_kernel(SimtArgs p) {
     }
 
     if (!valid) return;
+    if (!SGA_CHECK_INDEX((long long)seg * p.seg_rows + row, (long long)gridDim.y * p.seg_rows, 12)) return;
     if (p.ex.on) extra_values<T, 64>(p.ex, seg, row, xr, m, 0, o);
     const float inv_l = 1.0f / l;
     T* Ob = reinterpret_cast<T*>(p.O) + ((long long)seg * p.seg_rows + row) * 64;

@@ -697,7 +697,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
             tc_fence_before();
             mbar_arrive(bars.o_free(t));
-            if (valid) {
+            if (valid && SGA_CHECK_INDEX((long long)seg * p.seg_rows + row, (long long)p.n_seg * p.seg_rows, 10)) {
                 if (p.ex.on) extra_values<__nv_bfloat16, 64>(p.ex, seg, row, xr, m, 0, o);
                 const float inv_l = 1.0f / l;
                 const long long grow = (long long)seg * p.seg_rows + row;

@@ -15,6 +15,28 @@ namespace sga {
 // bounded wait expires; sga_device_status() reads and clears it.
 __device__ int g_status;
 
+// Debug builds (-DSGA_DEBUG): before each indexed store (and the index reads that steer one) a
+// kernel checks the index against its buffer's bound.  An index out of range is recorded -- the
+// first one's site, index and bound, plus a count -- the status word is set to
+// SGA_ERR_DEBUG_CHECK, and the access is skipped; nothing traps.  sga_debug_report reads the
+// record.  In normal builds SGA_CHECK_INDEX is the constant true and costs nothing.
+#ifdef SGA_DEBUG
+__device__ unsigned long long g_debug_word[4];        // site, index, bound, count
+__device__ __noinline__ bool dbg_index_ok(long long idx, long long bound, int site) {
+    if (idx >= 0 && idx < bound) return true;
+    if (atomicAdd(&g_debug_word[3], 1ull) == 0ull) {
+        g_debug_word[0] = (unsigned long long)site;
+        g_debug_word[1] = (unsigned long long)idx;
+        g_debug_word[2] = (unsigned long long)bound;
+    }
+    atomicExch(&g_status, (int)SGA_ERR_DEBUG_CHECK);
+    return false;
+}
+#define SGA_CHECK_INDEX(idx, bound, site) (::sga::dbg_index_ok((long long)(idx), (long long)(bound), (site)))
+#else
+#define SGA_CHECK_INDEX(idx, bound, site) (true)
+#endif
+
 // Waits give up after this many SM clock cycles (about 2 s at 2 GHz).
 constexpr long long kTimeoutCycles = 4000000000LL;
 

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel
                     x1[e] = y1;
                 }
                 if (sl[u] >= 0) {
+                    if (!SGA_CHECK_INDEX(sl[u], a.S, 1)) continue;
                     uint4* ksr = KS + (long long)sl[u] * kLanesPerRow;
                     uint4* vsr = VS + (long long)sl[u] * kLanesPerRow;
                     ksr[va] = VT::pack(x0);
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             if (sl[u] >= 0) {
+                if (!SGA_CHECK_INDEX(sl[u], a.S, 1)) continue;
                 KS[(long long)sl[u] * kLanesPerRow + va] = kv[u];
                 VS[(long long)sl[u] * kLanesPerRow + va] = vv[u];
             } else if (sl[u] == -1) {

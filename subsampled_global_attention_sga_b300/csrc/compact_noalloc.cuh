@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_noalloc_kernel(Noallo
 #pragma unroll
         for (int u = 0; u < kCompactUnroll; ++u) {
             if (sl[u] >= 0) {
-                if (sl[u] < a.S) {          // always true for a consistent configuration
+                if (SGA_CHECK_INDEX(sl[u], a.S, 2) && sl[u] < a.S) {   // true for a consistent configuration
                     KS[sl[u] * kLanesPerRow + vec] = kv[u];
                     VS[sl[u] * kLanesPerRow + vec] = vv[u];
                 }

@@ -45,6 +45,7 @@ __device__ __forceinline__ ExtraRow extra_logits(const ExtraArgs& a, int bh, lon
     r.s_mean = -INFINITY;
     r.loo = 0;
     r.inv_c = 0.f;
+    if (!SGA_CHECK_INDEX(i, a.T, 11)) return r;
     const bool dropped_row = a.slot[i] < 0;
     const T* krow = reinterpret_cast<const T*>(a.K) + ((long long)bh * a.T + i) * 64;
     if (a.diag && dropped_row) {

@@ -139,11 +139,13 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         for (int i = tid; i < n * VPR; i += kMergeThreads) {
             const int k = i / VPR, v = i % VPR;
             const long long t = (long long)(f0 + k / g.n_special) * g.L + k % g.n_special;
+            if (!SGA_CHECK_INDEX(base + k, g.M, 22)) continue;
             reinterpret_cast<uint4*>(Xm + (base + k) * 64)[v] = __ldg(reinterpret_cast<const uint4*>(X + t * 64) + v);
             if (Ym) reinterpret_cast<uint4*>(Ym + (base + k) * 64)[v] = __ldg(reinterpret_cast<const uint4*>(Y + t * 64) + v);
         }
         for (int k = tid; k < n; k += kMergeThreads) {
             const long long t = (long long)(f0 + k / g.n_special) * g.L + k % g.n_special;
+            if (!SGA_CHECK_INDEX(t, g.T, 20) || !SGA_CHECK_INDEX(base + k, g.M, 22)) continue;
             map[t] = (int32_t)(base + k);
             if (lg) lg[base + k] = 0.f;
         }
@@ -306,14 +308,17 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         }
     }
     // 6. map: every token to its merged row (a merged source to its destination's)
-    for (int k = tid; k < nb; k += kMergeThreads)
-        map[tok(k)] = (int32_t)(base + (rank[k] >= 0 ? rank[k] : rank[best[k - ws]]));
+    for (int k = tid; k < nb; k += kMergeThreads) {
+        const long long mi = base + (rank[k] >= 0 ? rank[k] : rank[best[k - ws]]);
+        if (SGA_CHECK_INDEX(tok(k), g.T, 20) && SGA_CHECK_INDEX(mi, g.M, 21)) map[tok(k)] = (int32_t)mi;
+    }
     // 7. group means of the kept entries (a destination plus the sources merged into it, summed
     //    in entry order), 16 dimensions per work item, and ln of the group size
     for (int it = tid; it < nb * 4; it += kMergeThreads) {
         const int k = it >> 2, e0 = (it & 3) * 16;
         if (rank[k] < 0) continue;
         const long long mi = base + rank[k];
+        if (!SGA_CHECK_INDEX(mi, g.M, 21)) continue;
         float sx[16], sy[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) { sx[e] = xs[k * kXS + e0 + e]; sy[e] = 0.f; }
@@ -354,7 +359,9 @@ __global__ void __launch_bounds__(256) unmerge_kernel(const int32_t* map, const 
     const long long row = i / kVec;
     const int v = (int)(i % kVec);
     const long long bh = row / T_seq;
-    const long long src = bh * M + __ldg(map + row);
+    const int32_t mi = __ldg(map + row);
+    if (!SGA_CHECK_INDEX(mi, M, 23)) return;
+    const long long src = bh * M + mi;
     reinterpret_cast<uint4*>(Y)[row * kVec + v] = __ldg(reinterpret_cast<const uint4*>(Ym) + src * kVec + v);
 }
 

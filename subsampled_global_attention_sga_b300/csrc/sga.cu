@@ -325,6 +325,7 @@ const char* sga_status_string(sga_status s) {
         case SGA_ERR_TIMEOUT: return "kernel wait timed out";
         case SGA_ERR_PLAN_MISMATCH: return "plan invalid or created for another device";
         case SGA_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch of sga_compact_noalloc";
+        case SGA_ERR_DEBUG_CHECK: return "a kernel's index check failed (debug build; see sga_debug_report)";
     }
     return "unknown status";
 }
@@ -332,8 +333,31 @@ const char* sga_status_string(sga_status s) {
 #ifndef SGA_SOURCE_HASH
 #define SGA_SOURCE_HASH "unknown"
 #endif
+#ifdef SGA_DEBUG
+#define SGA_BUILD_KIND "debug (index checks) "
+#else
+#define SGA_BUILD_KIND ""
+#endif
 const char* sga_build_info(void) {
-    return "libsga sm_103a (tcgen05/TMEM/TMA attention, CUDA-core fp32 path) v1 src=" SGA_SOURCE_HASH;
+    return "libsga sm_103a (tcgen05/TMEM/TMA attention, CUDA-core fp32 path) v2 " SGA_BUILD_KIND "src=" SGA_SOURCE_HASH;
+}
+
+sga_status sga_debug_report(int64_t* site, int64_t* index, int64_t* bound, int64_t* count) {
+#ifdef SGA_DEBUG
+    if (cudaDeviceSynchronize() != cudaSuccess) return SGA_ERR_CUDA;
+    unsigned long long w[4] = {0, 0, 0, 0};
+    if (cudaMemcpyFromSymbol(w, sga::g_debug_word, sizeof(w)) != cudaSuccess) return SGA_ERR_CUDA;
+    const unsigned long long zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(sga::g_debug_word, zero, sizeof(zero)) != cudaSuccess) return SGA_ERR_CUDA;
+    if (site) *site = (int64_t)w[0];
+    if (index) *index = (int64_t)w[1];
+    if (bound) *bound = (int64_t)w[2];
+    if (count) *count = (int64_t)w[3];
+    return SGA_OK;
+#else
+    (void)site; (void)index; (void)bound; (void)count;
+    return SGA_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"
@@ -880,10 +904,13 @@ sga_status sga_selftest_timeout(void* stream) {
 
 struct sga_stream_s {
     uint32_t magic;
-    sga_plan_t plan;
+    sga_plan_t plan;                        // SGA layers; null for the plain kinds
+    sga_plain_spec spec;                    // dense / frame-local / size-aware layers
+    int device;
     int depth;
-    size_t in_bytes;                        // one of Q, K, V, O
-    std::vector<void*> q, k, v, o, ks, vs;  // per buffer set
+    size_t in_bytes;                        // one of Q, K, V, O (SGA layers)
+    size_t q_bytes, kv_bytes, bias_bytes;   // plain layers: Q and O, K and V, the bias
+    std::vector<void*> q, k, v, o, ks, vs, bias;   // per buffer set
     std::vector<float*> ksum, vsum;
     cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
     std::vector<cudaEvent_t> kv_in, q_in, done, out_read;
@@ -899,7 +926,7 @@ void stream_free(sga_stream_s* s) {
     if (s->h2d) cudaStreamSynchronize(s->h2d);
     if (s->comp) cudaStreamSynchronize(s->comp);
     if (s->d2h) cudaStreamSynchronize(s->d2h);
-    for (auto* vec : {&s->q, &s->k, &s->v, &s->o, &s->ks, &s->vs})
+    for (auto* vec : {&s->q, &s->k, &s->v, &s->o, &s->ks, &s->vs, &s->bias})
         for (void* p : *vec) if (p) cudaFree(p);
     for (auto* vec : {&s->ksum, &s->vsum})
         for (float* p : *vec) if (p) cudaFree(p);
@@ -914,7 +941,24 @@ void stream_free(sga_stream_s* s) {
 
 sga_status check_stream(sga_stream_t s) {
     if (!s || s->magic != kStreamMagic) return SGA_ERR_INVALID_ARG;
-    return check_plan(s->plan);
+    if (s->plan) return check_plan(s->plan);
+    int dev;
+    if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
+    return dev == s->device ? SGA_OK : SGA_ERR_PLAN_MISMATCH;
+}
+
+sga_status check_plain_spec(const sga_plain_spec* p) {
+    if (!p) return SGA_ERR_INVALID_ARG;
+    if (p->kind != SGA_PLAIN_DENSE && p->kind != SGA_PLAIN_FRAME && p->kind != SGA_PLAIN_BIAS)
+        return SGA_ERR_INVALID_ARG;
+    if (p->B <= 0 || p->H <= 0 || p->Tq <= 0) return SGA_ERR_INVALID_ARG;
+    if (p->kind == SGA_PLAIN_BIAS && p->Tk <= 0) return SGA_ERR_INVALID_ARG;
+    if (p->kind == SGA_PLAIN_FRAME && (p->N <= 0 || p->L <= 0 || (int64_t)p->N * p->L != p->Tq))
+        return SGA_ERR_INVALID_ARG;
+    sga_status st = check_common(p->dtype, p->head_dim, p->kernel);
+    if (st != SGA_OK) return st;
+    if ((long long)p->B * p->H > 0x7FFFFFFFLL || p->Tq > 0x7FFFFFFFLL || p->Tk > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
+    return SGA_OK;
 }
 
 }  // namespace
@@ -930,6 +974,8 @@ sga_status sga_stream_create(sga_plan_t plan, int depth, sga_stream_t* out) {
     if (!s) return SGA_ERR_CUDA;
     s->magic = kStreamMagic;
     s->plan = plan;
+    std::memset(&s->spec, 0, sizeof(s->spec));
+    s->device = plan->device;
     s->depth = depth;
     const size_t elem = plan->cfg.dtype == SGA_BF16 ? 2 : 4;
     const size_t bh = (size_t)plan->cfg.B * plan->cfg.H;
@@ -979,6 +1025,7 @@ sga_status sga_stream_submit(sga_stream_t s, const void* Q_host, const void* K_h
                              void* O_host, float scale) {
     sga_status st = check_stream(s);
     if (st != SGA_OK) return st;
+    if (!s->plan) return SGA_ERR_INVALID_ARG;                // a plain stream takes sga_stream_submit_plain
     if (!Q_host || !K_host || !V_host || !O_host) return SGA_ERR_INVALID_ARG;
     if (!(scale > 0.f)) scale = 0.125f;
     const int i = (int)(s->next % s->depth);
@@ -1013,6 +1060,104 @@ sga_status sga_stream_submit(sga_stream_t s, const void* Q_host, const void* K_h
     return SGA_OK;
 }
 
+sga_status sga_stream_create_plain(const sga_plain_spec* spec, int depth, sga_stream_t* out) {
+    if (!out || depth < 1 || depth > 8) return SGA_ERR_INVALID_ARG;
+    *out = nullptr;
+    sga_status st = check_plain_spec(spec);
+    if (st != SGA_OK) return st;
+    int dev;
+    if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
+    sga_stream_s* s = new (std::nothrow) sga_stream_s();
+    if (!s) return SGA_ERR_CUDA;
+    s->magic = kStreamMagic;
+    s->plan = nullptr;
+    s->spec = *spec;
+    if (spec->kind != SGA_PLAIN_BIAS) s->spec.Tk = spec->Tq;
+    s->device = dev;
+    s->depth = depth;
+    const size_t elem = spec->dtype == SGA_BF16 ? 2 : 4;
+    const size_t bh = (size_t)spec->B * spec->H;
+    s->q_bytes = bh * (size_t)spec->Tq * 64 * elem;
+    s->kv_bytes = bh * (size_t)s->spec.Tk * 64 * elem;
+    s->bias_bytes = spec->kind == SGA_PLAIN_BIAS ? bh * (size_t)spec->Tk * sizeof(float) : 0;
+    bool ok = true;
+    auto alloc = [&](size_t bytes) -> void* {
+        void* p = nullptr;
+        if (ok && bytes > 0 && cudaMalloc(&p, bytes) != cudaSuccess) { ok = false; p = nullptr; }
+        return p;
+    };
+    auto event = [&]() -> cudaEvent_t {
+        cudaEvent_t e = nullptr;
+        if (ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) { ok = false; e = nullptr; }
+        return e;
+    };
+    for (int i = 0; i < depth; ++i) {
+        s->q.push_back(alloc(s->q_bytes));
+        s->k.push_back(alloc(s->kv_bytes));
+        s->v.push_back(alloc(s->kv_bytes));
+        s->o.push_back(alloc(s->q_bytes));
+        s->bias.push_back(alloc(s->bias_bytes));
+        s->kv_in.push_back(event());
+        s->q_in.push_back(event());
+        s->done.push_back(event());
+        s->out_read.push_back(event());
+        s->used.push_back(0);
+    }
+    if (ok && (cudaStreamCreateWithFlags(&s->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+               cudaStreamCreateWithFlags(&s->comp, cudaStreamNonBlocking) != cudaSuccess ||
+               cudaStreamCreateWithFlags(&s->d2h, cudaStreamNonBlocking) != cudaSuccess))
+        ok = false;
+    if (!ok) {
+        stream_free(s);
+        cudaGetLastError();
+        return SGA_ERR_CUDA;
+    }
+    *out = s;
+    return SGA_OK;
+}
+
+sga_status sga_stream_submit_plain(sga_stream_t s, const void* Q_host, const void* K_host, const void* V_host,
+                                   const float* bias_host, void* O_host, float scale) {
+    sga_status st = check_stream(s);
+    if (st != SGA_OK) return st;
+    if (s->plan) return SGA_ERR_INVALID_ARG;                 // an SGA stream takes sga_stream_submit
+    const sga_plain_spec& p = s->spec;
+    if (!Q_host || !K_host || !V_host || !O_host || ((p.kind == SGA_PLAIN_BIAS) != (bias_host != nullptr)))
+        return SGA_ERR_INVALID_ARG;
+    if (!(scale > 0.f)) scale = 0.125f;
+    const int i = (int)(s->next % s->depth);
+    auto cu = [](cudaError_t e) { return e == cudaSuccess; };
+    // inputs: the layer that last read this buffer set has finished; K, V (and the bias) first
+    if (s->used[i] && !cu(cudaStreamWaitEvent(s->h2d, s->done[i], 0))) return SGA_ERR_CUDA;
+    if (!cu(cudaMemcpyAsync(s->k[i], K_host, s->kv_bytes, cudaMemcpyHostToDevice, s->h2d)) ||
+        !cu(cudaMemcpyAsync(s->v[i], V_host, s->kv_bytes, cudaMemcpyHostToDevice, s->h2d)) ||
+        (bias_host && !cu(cudaMemcpyAsync(s->bias[i], bias_host, s->bias_bytes, cudaMemcpyHostToDevice, s->h2d))) ||
+        !cu(cudaMemcpyAsync(s->q[i], Q_host, s->q_bytes, cudaMemcpyHostToDevice, s->h2d)) ||
+        !cu(cudaEventRecord(s->q_in[i], s->h2d)))
+        return SGA_ERR_CUDA;
+    // compute once every input is in and the previous output of this set has been copied out
+    if (!cu(cudaStreamWaitEvent(s->comp, s->q_in[i], 0))) return SGA_ERR_CUDA;
+    if (s->used[i] && !cu(cudaStreamWaitEvent(s->comp, s->out_read[i], 0))) return SGA_ERR_CUDA;
+    if (p.kind == SGA_PLAIN_DENSE)
+        st = sga_dense_forward(p.B, p.H, p.Tq, p.head_dim, p.dtype, p.kernel, s->q[i], s->k[i], s->v[i], s->o[i],
+                               nullptr, scale, s->comp);
+    else if (p.kind == SGA_PLAIN_FRAME)
+        st = sga_frame_forward(p.B, p.H, p.N, p.L, p.head_dim, p.dtype, p.kernel, s->q[i], s->k[i], s->v[i],
+                               s->o[i], nullptr, scale, s->comp);
+    else
+        st = sga_bias_forward(p.B, p.H, p.Tq, p.Tk, p.head_dim, p.dtype, p.kernel, s->q[i], s->k[i], s->v[i],
+                              static_cast<const float*>(s->bias[i]), s->o[i], nullptr, scale, s->comp);
+    if (st != SGA_OK) return st;
+    if (!cu(cudaEventRecord(s->done[i], s->comp))) return SGA_ERR_CUDA;
+    if (!cu(cudaStreamWaitEvent(s->d2h, s->done[i], 0)) ||
+        !cu(cudaMemcpyAsync(O_host, s->o[i], s->q_bytes, cudaMemcpyDeviceToHost, s->d2h)) ||
+        !cu(cudaEventRecord(s->out_read[i], s->d2h)))
+        return SGA_ERR_CUDA;
+    s->used[i] = 1;
+    ++s->next;
+    return SGA_OK;
+}
+
 sga_status sga_stream_synchronize(sga_stream_t s) {
     sga_status st = check_stream(s);
     if (st != SGA_OK) return st;
@@ -1033,6 +1178,12 @@ sga_status sga_stream_handles(sga_stream_t s, void** h2d, void** compute, void**
 void sga_stream_destroy(sga_stream_t s) {
     if (!s || s->magic != kStreamMagic) return;
     stream_free(s);
+}
+
+sga_status sga_last_device_status(sga_plan_t plan, void* stream) {
+    sga_status st = check_plan(plan);
+    if (st != SGA_OK) return st;
+    return sga_device_status(stream);
 }
 
 sga_status sga_device_status(void* stream) {
@@ -1061,17 +1212,50 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchFloats];
 namespace {
 
 float* g_noalloc_ptr[kMaxDevices];
+unsigned long long g_noalloc_ctx[kMaxDevices];   // id of the context the address belongs to
 bool g_noalloc_ready[kMaxDevices];
 std::mutex g_noalloc_mu;
 
+// Unique id of the calling thread's current CUDA context (ids are never reused within a
+// process, unlike context handles), or 0 when it cannot be read.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array on `dev` (current).  It is looked up with the device
+// current and cached per device together with the id of the context it was looked up in: after
+// a device reset (or any new primary context) the library's module is loaded again at another
+// address, so a changed context id triggers a fresh lookup.  No allocation is made.
 sga_status noalloc_scratch(int dev, float** out) {
     if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ready[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_noalloc_ready[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         float* p = nullptr;
         if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch) != cudaSuccess || !p)
             return SGA_ERR_CUDA;
         g_noalloc_ptr[dev] = p;
+        // the lookup made the primary context current if it was not: read its id now
+        g_noalloc_ctx[dev] = ctx != 0 ? ctx : current_context_id();
         g_noalloc_ready[dev] = true;
     }
     *out = g_noalloc_ptr[dev];
@@ -1098,6 +1282,14 @@ long long kept_count_closed_form(const sga_config& c) {
 }
 
 }  // namespace
+
+extern "C" sga_status sga_kept_count(const sga_config* cfg, int64_t* S) {
+    if (!S) return SGA_ERR_INVALID_ARG;
+    sga_status st = check_config(cfg);
+    if (st != SGA_OK) return st;
+    *S = kept_count_closed_form(*cfg);
+    return SGA_OK;
+}
 
 extern "C" sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, const void* V, void* K_S,
                                           void* V_S, float* k_sum, float* v_sum, void* stream) {

@@ -1,0 +1,117 @@
+"""The debug build of the library (libsga_debug.so, compiled with -DSGA_DEBUG): every kernel checks
+its indexed stores -- and the index reads that steer them -- against the buffer's bound, records a
+failure in a device word and skips the access instead of trapping.  The small parity cases run
+through it in a process of their own (the environment picks the library at load time): results
+must match the oracle as with the normal build, the device status must stay SGA_OK and no check
+may have failed."""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = r'''
+import ctypes, sys
+import numpy as np
+import torch
+sys.path.insert(0, ROOT)
+import oracle
+import subsampled_global_attention_sga_b300 as sga
+from subsampled_global_attention_sga_b300.inputs import correlated_qkv
+
+assert b"debug" in sga.lib().sga_build_info(), sga.lib().sga_build_info()
+dev = torch.device("cuda", 0)
+
+def host(x):
+    return x.float().cpu().numpy()
+
+def compare(got, ref, f32, what):
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    if f32:
+        assert err.max() <= 1e-5, (what, err.max())
+    else:
+        rel = np.linalg.norm(np.asarray(got, dtype=np.float64) - ref) / np.linalg.norm(ref)
+        assert err.max() <= 2e-2 and rel <= 5e-3, (what, err.max(), rel)
+
+def sga_case(cfg, seed):
+    tdt = cfg.torch_dtype
+    q, k, v = correlated_qkv(cfg.B, cfg.H, cfg.N, cfg.L, 64, seed=seed, dtype=tdt, device=dev)
+    out = sga.Plan(cfg, dev).layer(q, k, v)
+    torch.cuda.synchronize(dev)
+    s_h, s_w = cfg.s_hw
+    op = oracle.plan(cfg.N, cfg.grid_h, cfg.grid_w, cfg.n_special, s_h, s_w, cfg.phase_shift, cfg.ref_frame_dense)
+    for h in range(cfg.H):
+        ref, _ = oracle.sga_full(op, host(q[0, h]), host(k[0, h]), host(v[0, h]))
+        compare(host(out[0, h]), ref, cfg.dtype == "f32", "sga")
+
+sga_case(sga.SGAConfig(B=1, H=2, N=4, grid_h=8, grid_w=8, sigma=4, dtype="f32"), 0)
+for kern in ("tc", "simt"):
+    sga_case(sga.SGAConfig(B=1, H=2, N=4, grid_h=8, grid_w=8, sigma=4, kernel=kern), 0)
+sga_case(sga.SGAConfig(B=1, H=2, N=8, sigma=4, phase_shift=True), 1)
+
+# dense, frame-local and size-aware attention
+N, L, H = 3, 300, 2
+q, k, v = correlated_qkv(1, H, N, L, 64, seed=5, dtype=torch.bfloat16, device=dev)
+od = sga.dense_forward(q, k, v)
+of = sga.frame_forward(q, k, v, N, L)
+bias = torch.log(torch.randint(1, 5, (1, H, N * L), device=dev).float()).contiguous()
+ob = sga.bias_forward(q, k, v, bias)
+torch.cuda.synchronize(dev)
+rows = np.arange(N * L)
+for h in range(H):
+    ref, _ = oracle.attention_rows(host(q[0, h]), host(k[0, h]), host(v[0, h]), rows)
+    compare(host(od[0, h]), ref, False, "dense")
+    ref, _ = oracle.attention_rows(host(q[0, h]), host(k[0, h]), host(v[0, h]), rows, frame_len=L)
+    compare(host(of[0, h]), ref, False, "frame")
+    ref, _ = oracle.biased_attention_rows(host(q[0, h]), host(k[0, h]), host(v[0, h]),
+                                          bias[0, h].double().cpu().numpy())
+    compare(host(ob[0, h]), ref, False, "bias")
+
+# merging, unmerging and the allocation-free compaction
+mc = sga.MergeConfig(B=1, H=2, N=8, grid_h=6, grid_w=7, n_t=4, n_s=7, r_permille=600)
+_, k, v = correlated_qkv(1, 2, mc.N, mc.n_special + 42, 64, seed=6, dtype=torch.bfloat16, device=dev)
+Km, Vm, lg, mp = sga.merge(mc, k, v)
+back = sga.unmerge(mc, mp, Vm)
+cfg = sga.SGAConfig(B=1, H=2, N=5, grid_h=9, grid_w=7, sigma=9, phase_shift=True)
+_, k2, v2 = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=7, dtype=torch.bfloat16, device=dev)
+S = sga.kept_count(cfg)
+outs = [torch.empty((1, 2, S, 64), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+sums = [torch.empty((1, 2, 64), dtype=torch.float32, device=dev) for _ in range(2)]
+sga.compact_noalloc(cfg, k2, v2, *outs, *sums)
+torch.cuda.synchronize(dev)
+for h in range(2):
+    m_or = oracle.merge_match(host(k[0, h]), mc.N, mc.grid_h, mc.grid_w, mc.n_special, mc.n_t, mc.n_s,
+                              mc.r_permille)
+    kept, gid, sizes = oracle.merge_groups(m_or)
+    assert Km.shape[2] == len(kept)
+    g = mp[0, h].cpu().numpy()
+    assert len(set(zip(gid.tolist(), g.tolist()))) == len(kept)
+    assert torch.equal(back[0, h], Vm[0, h][mp[0, h].long()])
+op = oracle.plan(cfg.N, cfg.grid_h, cfg.grid_w, cfg.n_special, 3, 3, True, True)
+idx = torch.as_tensor(op.kv_index.astype(np.int64), device=dev)
+assert torch.equal(outs[0], k2[:, :, idx]) and torch.equal(outs[1], v2[:, :, idx])
+
+assert sga.device_status(dev) == 0
+w = [ctypes.c_int64(-1) for _ in range(4)]
+assert sga.lib().sga_debug_report(*[ctypes.byref(x) for x in w]) == 0
+assert w[3].value == 0, ("index checks failed", [x.value for x in w])
+print("DEBUG-OK")
+'''
+
+
+def test_parity_cases_under_the_debug_build():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = os.path.join(ROOT, "subsampled_global_attention_sga_b300", "libsga_debug.so")
+    if not os.path.exists(lib):
+        from subsampled_global_attention_sga_b300 import _build
+        _build.build(debug=True)
+    env = dict(os.environ, SGA_LIBRARY="debug")
+    res = subprocess.run([sys.executable, "-c", f"ROOT = {ROOT!r}\n" + SCRIPT], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0 and "DEBUG-OK" in res.stdout, res.stdout[-3000:] + res.stderr[-3000:]

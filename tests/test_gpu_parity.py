@@ -8,6 +8,7 @@ import torch
 
 import oracle
 import subsampled_global_attention_sga_b300 as sga
+from _guard import check_all, guarded
 from subsampled_global_attention_sga_b300.inputs import correlated_qkv, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -43,14 +44,26 @@ def _compare(got, ref, dtype, what=""):
         assert err <= BF16_MAX_ABS and rel <= BF16_REL_L2, f"{what}: max-abs {err:.3e} rel-L2 {rel:.3e}"
 
 
-def _run(cfg, q, k, v, dev, lse=False):
-    plan = sga.Plan(cfg, dev)
-    L = torch.empty(q.shape[:3], dtype=torch.float32, device=dev) if lse else None
-    K_S, V_S, ks, vs = plan.compact(k, v)
-    out = plan.forward(q, k, v, K_S, V_S, ks, vs, lse=L)
+def _layer_guarded(plan, cfg, q, k, v, dev, lse=False):
+    """Compaction and attention with every output between NaN guards, checked after the call."""
+    ks_shape = (cfg.B, cfg.H, plan.S, 64)
+    gs = [guarded(ks_shape, cfg.torch_dtype, dev), guarded(ks_shape, cfg.torch_dtype, dev),
+          guarded((cfg.B, cfg.H, 64), torch.float32, dev), guarded((cfg.B, cfg.H, 64), torch.float32, dev),
+          guarded(q.shape, q.dtype, dev)]
+    if lse:
+        gs.append(guarded(q.shape[:3], torch.float32, dev))
+    K_S, V_S, ks, vs = plan.compact(k, v, *[g.t for g in gs[:4]])
+    out = plan.forward(q, k, v, K_S, V_S, ks, vs, out=gs[4].t, lse=gs[5].t if lse else None)
     torch.cuda.synchronize(dev)
     assert sga.device_status(dev) == 0
-    return plan, out, L, (K_S, V_S, ks, vs)
+    check_all(gs, "layer")
+    return out, (gs[5].t if lse else None), (K_S, V_S, ks, vs)
+
+
+def _run(cfg, q, k, v, dev, lse=False):
+    plan = sga.Plan(cfg, dev)
+    out, L, bufs = _layer_guarded(plan, cfg, q, k, v, dev, lse)
+    return plan, out, L, bufs
 
 
 def _check_full(cfg, q, k, v, out, lse=None, **okw):
@@ -151,10 +164,12 @@ def test_compaction_exact(dev):
 def test_dense_and_frame_variants(dev, kernel):
     N, L, H = 3, 300, 2
     q, k, v = correlated_qkv(1, H, N, L, 64, seed=5, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((1, H, N * L), dtype=torch.float32, device=dev)
-    od = sga.dense_forward(q, k, v, kernel=kernel, lse=lse)
-    of = sga.frame_forward(q, k, v, N, L, kernel=kernel)
+    gs = [guarded((1, H, N * L), torch.float32, dev), guarded(q.shape, q.dtype, dev), guarded(q.shape, q.dtype, dev)]
+    lse = gs[0].t
+    od = sga.dense_forward(q, k, v, kernel=kernel, lse=lse, out=gs[1].t)
+    of = sga.frame_forward(q, k, v, N, L, kernel=kernel, out=gs[2].t)
     torch.cuda.synchronize(dev)
+    check_all(gs, "dense/frame")
     qf, kf, vf = _host(q), _host(k), _host(v)
     rows = np.arange(N * L)
     for h in range(H):
@@ -168,9 +183,11 @@ def test_dense_and_frame_variants(dev, kernel):
 def test_dense_frame_f32(dev):
     N, L, H = 2, 70, 2
     q, k, v = correlated_qkv(1, H, N, L, 64, seed=6, dtype=torch.float32, device=dev)
-    od = sga.dense_forward(q, k, v, dtype="f32")
-    of = sga.frame_forward(q, k, v, N, L, dtype="f32")
+    gs = [guarded(q.shape, q.dtype, dev), guarded(q.shape, q.dtype, dev)]
+    od = sga.dense_forward(q, k, v, dtype="f32", out=gs[0].t)
+    of = sga.frame_forward(q, k, v, N, L, dtype="f32", out=gs[1].t)
     torch.cuda.synchronize(dev)
+    check_all(gs, "dense/frame f32")
     rows = np.arange(N * L)
     for h in range(H):
         ref, _ = oracle.attention_rows(_host(q)[0, h], _host(k)[0, h], _host(v)[0, h], rows)
@@ -250,9 +267,7 @@ def test_bad_arguments_raise(dev):
 def _sampled(cfg, dev, n_rows=4096, seed=0):
     q, k, v = correlated_qkv(cfg.B, cfg.H, cfg.N, cfg.L, 64, seed=seed, dtype=torch.bfloat16, device=dev)
     plan = sga.Plan(cfg, dev)
-    out = plan.layer(q, k, v)
-    torch.cuda.synchronize(dev)
-    assert sga.device_status(dev) == 0
+    out, _, _ = _layer_guarded(plan, cfg, q, k, v, dev)
     op = _oracle_plan(cfg)
     assert op.S == plan.S
     per_head = max(1, n_rows // (cfg.B * cfg.H))
@@ -295,8 +310,10 @@ def test_sweep_sampled(dev, sigma, phase, terms):
 def test_sweep_frame_local_sampled(dev):
     N, L, H = 100, 1374, 16
     q, k, v = correlated_qkv(1, H, N, L, 64, seed=20, dtype=torch.bfloat16, device=dev)
-    out = sga.frame_forward(q, k, v, N, L)
+    g = guarded(q.shape, q.dtype, dev)
+    out = sga.frame_forward(q, k, v, N, L, out=g.t)
     torch.cuda.synchronize(dev)
+    g.check("frame sweep")
     gots, refs = [], []
     for h in range(H):
         rows = sample_rows(N * L, L, 64, seed=h).numpy()
@@ -337,17 +354,21 @@ def _check_bias(q, k, v, bias, out, dtype, lse=None, rows=None):
 @pytest.mark.parametrize("Tq,Tk,real", [(700, 450, False), (256, 1000, True), (130, 129, False), (1, 5, True)])
 def test_bias_forward(dev, kernel, Tq, Tk, real):
     q, k, v, bias = _bias_case(dev, Tq, Tk, 2, seed=40 + Tq, real=real)
-    lse = torch.empty((1, 2, Tq), dtype=torch.float32, device=dev)
-    out = sga.bias_forward(q, k, v, bias, kernel=kernel, lse=lse)
+    gs = [guarded((1, 2, Tq), torch.float32, dev), guarded(q.shape, q.dtype, dev)]
+    lse = gs[0].t
+    out = sga.bias_forward(q, k, v, bias, kernel=kernel, lse=lse, out=gs[1].t)
     torch.cuda.synchronize(dev)
     assert sga.device_status(dev) == 0
+    check_all(gs, "bias")
     _check_bias(q, k, v, bias, out, "bf16", lse)
 
 
 def test_bias_forward_f32(dev):
     q, k, v, bias = _bias_case(dev, 300, 333, 2, seed=50, dtype=torch.float32, real=True)
-    out = sga.bias_forward(q, k, v, bias, dtype="f32")
+    g = guarded(q.shape, q.dtype, dev)
+    out = sga.bias_forward(q, k, v, bias, dtype="f32", out=g.t)
     torch.cuda.synchronize(dev)
+    g.check("bias f32")
     _check_bias(q, k, v, bias, out, "f32")
 
 
@@ -396,8 +417,10 @@ def test_bias_merged_keys_sampled(dev):
     # stand for 1-8 tokens each, 16 heads; 2048 sampled query rows against the oracle
     H, Tq, Tk = 16, 43968, 12000
     q, k, v, bias = _bias_case(dev, Tq, Tk, H, seed=70)
-    out = sga.bias_forward(q, k, v, bias)
+    g = guarded(q.shape, q.dtype, dev)
+    out = sga.bias_forward(q, k, v, bias, out=g.t)
     torch.cuda.synchronize(dev)
+    g.check("merged keys")
     gots, refs = [], []
     for h in range(H):
         rows = sample_rows(Tq, 1374, 128, seed=300 + h).numpy()
@@ -421,9 +444,7 @@ def _general_case(dev, cfg, sh, sw, phase, n_prot, seed, dtype=torch.bfloat16):
     q, k, v = correlated_qkv(cfg.B, cfg.H, cfg.N, cfg.L, 64, seed=seed, dtype=dtype, device=dev)
     plan = sga.Plan(cfg, dev, kv_index=kv)
     assert plan.S == op.S
-    out = plan.layer(q, k, v)
-    torch.cuda.synchronize(dev)
-    assert sga.device_status(dev) == 0
+    out, _, _ = _layer_guarded(plan, cfg, q, k, v, dev)
     return op, q, k, v, out
 
 
@@ -443,8 +464,7 @@ def test_arbitrary_kept_set_f32(dev):
     kv = np.sort(rng.choice(cfg.T, size=cfg.T // 3, replace=False)).astype(np.int32)
     q, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=81, dtype=torch.float32, device=dev)
     plan = sga.Plan(cfg, dev, kv_index=kv)
-    out = plan.layer(q, k, v)
-    torch.cuda.synchronize(dev)
+    out, _, _ = _layer_guarded(plan, cfg, q, k, v, dev)
     kept = np.zeros(cfg.T, dtype=np.uint8)
     kept[kv] = 1
     off = np.searchsorted(kv, np.arange(cfg.N + 1) * cfg.L).astype(np.int32)
@@ -491,8 +511,11 @@ def test_rope_compaction(dev, dtype, tdt):
                         rope_base=100.0, rope_pos_offset=1)
     _, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=90, dtype=tdt, device=dev)
     plan = sga.Plan(cfg, dev)
-    K_S, V_S, ks, vs = plan.compact(k, v)
+    gs = [guarded((1, 2, plan.S, 64), tdt, dev), guarded((1, 2, plan.S, 64), tdt, dev),
+          guarded((1, 2, 64), torch.float32, dev), guarded((1, 2, 64), torch.float32, dev)]
+    K_S, V_S, ks, vs = plan.compact(k, v, *[g.t for g in gs])
     torch.cuda.synchronize(dev)
+    check_all(gs, "rope compaction")
     op = _oracle_plan(cfg)
     idx = torch.as_tensor(op.kv_index.astype(np.int64), device=dev)
     assert torch.equal(V_S, v[:, :, idx])                       # values are never rotated
@@ -538,9 +561,11 @@ def test_rope_standalone_dense_and_frame(dev, kernel):
     plan = sga.Plan(cfg, dev)
     plan.rope2d(qr)
     plan.rope2d(kr)
-    od = sga.dense_forward(qr, kr, v, kernel=kernel)
-    of = sga.frame_forward(qr, kr, v, cfg.N, cfg.L, kernel=kernel)
+    gs = [guarded(q.shape, q.dtype, dev), guarded(q.shape, q.dtype, dev)]
+    od = sga.dense_forward(qr, kr, v, kernel=kernel, out=gs[0].t)
+    of = sga.frame_forward(qr, kr, v, cfg.N, cfg.L, kernel=kernel, out=gs[1].t)
     torch.cuda.synchronize(dev)
+    check_all(gs, "rope dense/frame")
     rows = np.arange(cfg.T)
     for h in range(2):
         qo, ko = _rope_ref(q[0, h], cfg), _rope_ref(k[0, h], cfg)
@@ -567,9 +592,7 @@ def test_rope_vggt_sampled(dev):
     cfg = sga.SGAConfig(B=1, H=16, N=32, sigma=4, rope=True, rope_base=100.0, rope_pos_offset=1)
     q, k, v = correlated_qkv(1, cfg.H, cfg.N, cfg.L, 64, seed=94, dtype=torch.bfloat16, device=dev)
     plan = sga.Plan(cfg, dev)
-    out = plan.layer(q, k, v)
-    torch.cuda.synchronize(dev)
-    assert sga.device_status(dev) == 0
+    out, _, _ = _layer_guarded(plan, cfg, q, k, v, dev)
     op = _oracle_plan(cfg)
     gots, refs = [], []
     for h in range(cfg.H):
@@ -602,13 +625,33 @@ def _merge_check(mc, X, Y, Xm, Ym, lg, mp, b, h):
     return kept, gid, sizes, perm
 
 
+def _merge_guarded(mc, X, Y=None):
+    """sga.merge with every output between guards, checked after the call."""
+    M = sga.merge_size(mc)
+    dev, tdt = X.device, X.dtype
+    gs = [guarded((mc.B, mc.H, M, 64), tdt, dev), guarded((mc.B, mc.H, M, 64), tdt, dev) if Y is not None else None,
+          guarded((mc.B, mc.H, M), torch.float32, dev), guarded((mc.B, mc.H, mc.T), torch.int32, dev)]
+    out = sga.merge(mc, X, Y, out=tuple(g.t if g is not None else None for g in gs))
+    torch.cuda.synchronize(dev)
+    check_all([g for g in gs if g is not None], "merge")
+    return out
+
+
+def _unmerge_guarded(mc, mp, Ym):
+    g = guarded((mc.B, mc.H, mc.T, 64), Ym.dtype, Ym.device)
+    out = sga.unmerge(mc, mp, Ym, out=g.t)
+    torch.cuda.synchronize(Ym.device)
+    g.check("unmerge")
+    return out
+
+
 @pytest.mark.parametrize("dtype,tdt", [("bf16", torch.bfloat16), ("f32", torch.float32)])
 @pytest.mark.parametrize("n_t,n_s,r", [(4, 8, 500), (3, 13, 1000), (2, 64, 250)])
 def test_merge_matches_oracle(dev, dtype, tdt, n_t, n_s, r):
     mc = sga.MergeConfig(B=2, H=2, N=9, grid_h=6, grid_w=7, n_t=n_t, n_s=n_s, r_permille=r, dtype=dtype)
     _, k, v = correlated_qkv(2, 2, mc.N, mc.n_special + mc.grid_h * mc.grid_w, 64, seed=100 + n_s, dtype=tdt,
                              device=dev)
-    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    Km, Vm, lg, mp = _merge_guarded(mc, k, v)
     torch.cuda.synchronize(dev)
     assert sga.device_status(dev) == 0
     for b in range(2):
@@ -622,7 +665,7 @@ def test_merge_largest_block(dev, dtype, tdt):
     # no longer fit in shared memory beside the keys and are read from global memory
     mc = sga.MergeConfig(B=1, H=2, N=9, grid_h=8, grid_w=8, n_t=8, n_s=64, r_permille=500, dtype=dtype)
     _, k, v = correlated_qkv(1, 2, mc.N, mc.n_special + 64, 64, seed=130, dtype=tdt, device=dev)
-    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    Km, Vm, lg, mp = _merge_guarded(mc, k, v)
     torch.cuda.synchronize(dev)
     assert sga.device_status(dev) == 0
     for h in range(2):
@@ -635,9 +678,9 @@ def test_merge_nothing_is_identity(dev, dtype, tdt):
     # every group's ln g is 0
     mc = sga.MergeConfig(B=1, H=2, N=7, grid_h=6, grid_w=7, n_t=3, n_s=10, r_permille=0, dtype=dtype)
     _, k, v = correlated_qkv(1, 2, mc.N, mc.n_special + 42, 64, seed=140, dtype=tdt, device=dev)
-    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    Km, Vm, lg, mp = _merge_guarded(mc, k, v)
     assert Km.shape[2] == mc.T
-    assert torch.equal(sga.unmerge(mc, mp, Km), k) and torch.equal(sga.unmerge(mc, mp, Vm), v)
+    assert torch.equal(_unmerge_guarded(mc, mp, Km), k) and torch.equal(_unmerge_guarded(mc, mp, Vm), v)
     assert torch.count_nonzero(lg) == 0
     for h in range(2):                                      # the map is a permutation per head
         assert torch.equal(torch.sort(mp[0, h]).values, torch.arange(mc.T, device=dev, dtype=mp.dtype))
@@ -646,8 +689,8 @@ def test_merge_nothing_is_identity(dev, dtype, tdt):
 def test_unmerge_gives_each_token_its_group_mean(dev):
     mc = sga.MergeConfig(B=1, H=2, N=8, grid_h=6, grid_w=7, n_t=4, n_s=7, r_permille=700, dtype="f32")
     _, k, _ = correlated_qkv(1, 2, mc.N, mc.n_special + 42, 64, seed=150, dtype=torch.float32, device=dev)
-    Km, _, lg, mp = sga.merge(mc, k)
-    back = sga.unmerge(mc, mp, Km)
+    Km, _, lg, mp = _merge_guarded(mc, k)
+    back = _unmerge_guarded(mc, mp, Km)
     torch.cuda.synchronize(dev)
     for h in range(2):
         kept, gid, sizes, _ = _merge_check(mc, k, None, Km, None, lg, mp, 0, h)
@@ -661,7 +704,7 @@ def test_merged_attention(dev, merge_queries):
     L = mc.n_special + mc.grid_h * mc.grid_w
     q, k, v = correlated_qkv(1, 2, mc.N, L, 64, seed=110, dtype=torch.bfloat16, device=dev)
     out = sga.merged_attention(mc, q, k, v, merge_queries=merge_queries)
-    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    Km, Vm, lg, mp = _merge_guarded(mc, k, v)
     torch.cuda.synchronize(dev)
     for h in range(2):
         kept, gid, sizes, _ = _merge_check(mc, k, v, Km, Vm, lg, mp, 0, h)
@@ -684,7 +727,7 @@ def test_merge_vggt_sampled(dev):
     mc = sga.MergeConfig(B=1, H=16, N=32, n_t=4, n_s=37, r_permille=500)
     L = 1374
     q, k, v = correlated_qkv(1, mc.H, mc.N, L, 64, seed=120, dtype=torch.bfloat16, device=dev)
-    Km, Vm, lg, mp = sga.merge(mc, k, v)
+    Km, Vm, lg, mp = _merge_guarded(mc, k, v)
     out = sga.bias_forward(q, Km, Vm, lg)
     torch.cuda.synchronize(dev)
     assert sga.device_status(dev) == 0
@@ -698,3 +741,111 @@ def test_merge_vggt_sampled(dev):
         gots.append(_host(out[0, h])[rows])
         refs.append(ref)
     _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "merged sampled")
+
+
+# ------------------------------------------------------------------------------ the benchmarked shapes
+# Every workload the benchmark times, at its own shape and in its launch configuration, against
+# the oracle on sampled rows (outputs between guards).
+def test_dense_benched_shape_sampled(dev):
+    # dense global attention over 32 VGGT frames: 43,968 tokens, 16 heads
+    N, L, H = 32, 1374, 16
+    q, k, v = correlated_qkv(1, H, N, L, 64, seed=160, dtype=torch.bfloat16, device=dev)
+    g = guarded(q.shape, q.dtype, dev)
+    out = sga.dense_forward(q, k, v, out=g.t)
+    torch.cuda.synchronize(dev)
+    g.check("dense")
+    gots, refs = [], []
+    for h in range(H):
+        rows = sample_rows(N * L, L, 128, seed=700 + h).numpy()
+        ref, _ = oracle.attention_rows(_host(q[0, h])[rows], _host(k[0, h]), _host(v[0, h]), rows)
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "dense benched shape")
+
+
+def test_size_aware_benched_shape_sampled(dev):
+    # 274,800 queries (200 frames) against 137,400 merged keys standing for 1-3 tokens (ln g)
+    H, Tq, Tk = 16, 274800, 137400
+    q, _, _ = correlated_qkv(1, H, 1, Tq, 64, seed=170, dtype=torch.bfloat16, device=dev)
+    _, k, v = correlated_qkv(1, H, 1, Tk, 64, seed=171, dtype=torch.bfloat16, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(172)
+    bias = torch.log(torch.randint(1, 4, (1, H, Tk), generator=gen, device=dev).float()).contiguous()
+    g = guarded(q.shape, q.dtype, dev)
+    out = sga.bias_forward(q, k, v, bias, out=g.t)
+    torch.cuda.synchronize(dev)
+    g.check("size-aware")
+    gots, refs = [], []
+    for h in range(H):
+        rows = sample_rows(Tq, 1374, 48, seed=800 + h).numpy()
+        ref, _ = oracle.biased_attention_rows(_host(q[0, h])[rows], _host(k[0, h]), _host(v[0, h]),
+                                              bias[0, h].double().cpu().numpy())
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "size-aware benched shape")
+
+
+@pytest.mark.parametrize("N,sigma", [(800, 4), (200, 9)])
+def test_rope_benched_shapes_sampled(dev, N, sigma):
+    # the SGA layer with the fused rotation (base 100, position offset 1)
+    cfg = sga.SGAConfig(B=1, H=16, N=N, sigma=sigma, rope=True, rope_base=100.0, rope_pos_offset=1)
+    q, k, v = correlated_qkv(1, cfg.H, cfg.N, cfg.L, 64, seed=180 + N, dtype=torch.bfloat16, device=dev)
+    plan = sga.Plan(cfg, dev)
+    out, _, _ = _layer_guarded(plan, cfg, q, k, v, dev)
+    op = _oracle_plan(cfg)
+    gots, refs = [], []
+    for h in range(cfg.H):
+        rows = sample_rows(cfg.T, cfg.L, 96, seed=900 + h, kept=op.kept).numpy()
+        qr, kr = _rope_ref(q[0, h], cfg), _rope_ref(k[0, h], cfg)
+        ref, _ = oracle.sga_rows(op, qr[rows], kr, _host(v[0, h]), rows)
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", f"rope N={N}")
+
+
+def test_general_plan_benched_shape_sampled(dev):
+    # 200 frames, per-axis sigma_b = 1.3 with phase shift, 10 % of the tokens protected
+    cfg = sga.SGAConfig(B=1, H=16, N=200)
+    op, q, k, v, out = _general_case(dev, cfg, (13, 10), (13, 10), True, n_prot=cfg.T // 10, seed=190)
+    gots, refs = [], []
+    for h in range(cfg.H):
+        rows = sample_rows(cfg.T, cfg.L, 96, seed=1000 + h, kept=op.kept).numpy()
+        ref, _ = oracle.sga_rows(op, _host(q[0, h])[rows], _host(k[0, h]), _host(v[0, h]), rows)
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "general benched shape")
+
+
+def test_merge_benched_shape(dev):
+    # head-wise temporal merging at 200 frames (chunks of 4 frames, 37-patch runs, half of the
+    # sources merged), then size-aware attention of all queries over the merged keys: the
+    # partition bit for bit on three heads, and sampled attention rows there
+    mc = sga.MergeConfig(B=1, H=16, N=200, n_t=4, n_s=37, r_permille=500)
+    L = 1374
+    q, k, v = correlated_qkv(1, mc.H, mc.N, L, 64, seed=200, dtype=torch.bfloat16, device=dev)
+    Km, Vm, lg, mp = _merge_guarded(mc, k, v)
+    g = guarded(q.shape, q.dtype, dev)
+    out = sga.bias_forward(q, Km, Vm, lg, out=g.t)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    g.check("merged attention")
+    gots, refs = [], []
+    for h in (0, 7, 15):
+        kept, gid, sizes, _ = _merge_check(mc, k, v, Km, Vm, lg, mp, 0, h)
+        km = oracle.merge_apply(_host(k[0, h]), gid, len(kept))
+        vm = oracle.merge_apply(_host(v[0, h]), gid, len(kept))
+        rows = sample_rows(mc.T, L, 96, seed=1100 + h).numpy()
+        ref, _ = oracle.biased_attention_rows(_host(q[0, h])[rows], km, vm, np.log(sizes))
+        gots.append(_host(out[0, h])[rows])
+        refs.append(ref)
+    _compare(np.concatenate(gots), np.concatenate(refs), "bf16", "merge benched shape")
+
+
+def test_last_device_status_reads_the_plan_device(dev):
+    cfg = sga.SGAConfig(B=1, H=2, N=4, grid_h=8, grid_w=8, sigma=4)
+    q, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=210, dtype=torch.bfloat16, device=dev)
+    plan = sga.Plan(cfg, dev)
+    plan.layer(q, k, v)
+    assert sga.last_device_status(plan) == 0
+    plan.close()
+    with pytest.raises(sga.SgaError):
+        sga.last_device_status(plan)        # the handle is gone: refused on the host

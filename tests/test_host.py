@@ -44,6 +44,20 @@ def test_library_carries_its_source_fingerprint(monkeypatch):
         _lib.lib()
 
 
+def test_debug_report_only_in_debug_builds():
+    # the normal build has no index checks to report; its debug twin carries the same sources
+    import ctypes as C
+    w = [C.c_int64(0) for _ in range(4)]
+    assert sga.lib().sga_debug_report(*[C.byref(x) for x in w]) == 2
+    assert b"debug" not in sga.lib().sga_build_info()
+    from subsampled_global_attention_sga_b300 import _build
+    if os.path.exists(_build.LIB_DEBUG):
+        L = C.CDLL(_build.LIB_DEBUG)
+        L.sga_build_info.restype = C.c_char_p
+        info = L.sga_build_info().decode()
+        assert "debug" in info and info.endswith("src=" + _build.source_hash())
+
+
 def test_status_strings():
     L = sga.lib()
     for s in range(7):
@@ -125,6 +139,51 @@ def test_null_arguments_rejected_without_device():
     assert L.sga_stream_synchronize(None) == 1
     assert L.sga_stream_handles(None, None, None, None) == 1
     L.sga_stream_destroy(None)
+    # the plain executor validates its description before any CUDA call
+    spec = sga._lib.SgaPlainSpec()
+    spec.kind, spec.B, spec.H, spec.Tq, spec.head_dim = 7, 1, 1, 128, 64
+    assert L.sga_stream_create_plain(ctypes.byref(spec), 2, ctypes.byref(h)) == 1 and not h.value
+    spec.kind, spec.N, spec.L = 2, 3, 40                      # frame-local with N*L != Tq
+    assert L.sga_stream_create_plain(ctypes.byref(spec), 2, ctypes.byref(h)) == 1
+    spec.kind, spec.head_dim = 1, 32
+    assert L.sga_stream_create_plain(ctypes.byref(spec), 2, ctypes.byref(h)) == 2
+    assert L.sga_stream_create_plain(None, 2, ctypes.byref(h)) == 1
+    assert L.sga_stream_submit_plain(None, p, p, p, None, p, ctypes.c_float(0.125)) == 1
+
+
+KEPT_COUNT_CASES = [
+    # N, grid_h, grid_w, n_special, window, phase, ref_dense
+    (4, 8, 8, 5, (2, 2), False, True),
+    (13, 37, 28, 5, (2, 3), True, False),
+    (9, 37, 37, 5, (3, 3), True, True),
+    (6, 13, 11, 0, (1, 2), True, True),
+    (1, 5, 7, 3, (3, 3), False, False),
+    (5, 2, 2, 5, (3, 3), True, False),       # grid smaller than the window
+    (3, 9, 7, 5, (1, 1), False, True),       # sigma = 1 keeps every token
+    (800, 37, 37, 5, (2, 2), False, True),
+    (800, 37, 37, 5, (2, 2), True, True),
+]
+
+
+@pytest.mark.parametrize("case", KEPT_COUNT_CASES)
+def test_kept_count_matches_oracle(case):
+    """sga_kept_count (the closed form that sizes sga_compact_noalloc's outputs) equals |S| of
+    the oracle's plan, which enumerates the kept set token by token."""
+    N, gh, gw, nsp, win, ph, ref = case
+    cfg = sga.SGAConfig(B=1, H=2, N=N, grid_h=gh, grid_w=gw, n_special=nsp, window=win, phase_shift=ph,
+                        ref_frame_dense=ref)
+    op = oracle.plan(N, gh, gw, nsp, win[0], win[1], ph, ref)
+    assert sga.kept_count(cfg) == op.S
+
+
+def test_kept_count_rejects_bad_arguments():
+    with pytest.raises(sga.SgaError):
+        sga.kept_count(sga.SGAConfig(B=1, H=1, N=0, grid_h=4, grid_w=4))
+    c = sga.SGAConfig(B=1, H=1, N=2, grid_h=4, grid_w=4).to_c()
+    assert sga.lib().sga_kept_count(ctypes.byref(c), None) == 1
+    assert sga.lib().sga_kept_count(None, None) == 1
+    # the plan-based status read refuses a missing plan before any CUDA call
+    assert sga.lib().sga_last_device_status(None, None) == 6
 
 
 GENERAL_CASES = [

@@ -18,6 +18,7 @@ import pytest
 import torch
 
 import subsampled_global_attention_sga_b300 as sga
+from _guard import check_all, guarded
 from subsampled_global_attention_sga_b300.inputs import correlated_qkv
 
 pytestmark = pytest.mark.gpu
@@ -32,12 +33,15 @@ def dev():
     return torch.device("cuda", 0)
 
 
-def _outputs(cfg, S, dev):
+def _guarded_outputs(cfg, S, dev):
+    """NaN-filled outputs, each between NaN guard regions that must survive the call."""
     ks_shape = (cfg.B, cfg.H, S, 64)
-    return (torch.full(ks_shape, float("nan"), dtype=cfg.torch_dtype, device=dev),
-            torch.full(ks_shape, float("nan"), dtype=cfg.torch_dtype, device=dev),
-            torch.full((cfg.B, cfg.H, 64), float("nan"), dtype=torch.float32, device=dev),
-            torch.full((cfg.B, cfg.H, 64), float("nan"), dtype=torch.float32, device=dev))
+    return [guarded(ks_shape, cfg.torch_dtype, dev), guarded(ks_shape, cfg.torch_dtype, dev),
+            guarded((cfg.B, cfg.H, 64), torch.float32, dev), guarded((cfg.B, cfg.H, 64), torch.float32, dev)]
+
+
+def _outputs(cfg, S, dev):
+    return tuple(g.t for g in _guarded_outputs(cfg, S, dev))
 
 
 def _check_against_plan(cfg, seed, dev):
@@ -45,9 +49,11 @@ def _check_against_plan(cfg, seed, dev):
     del q
     plan = sga.Plan(cfg, dev)
     want = plan.compact(k, v)
-    got = sga.compact_noalloc(cfg, k, v, *_outputs(cfg, plan.S, dev))
+    gs = _guarded_outputs(cfg, plan.S, dev)
+    got = sga.compact_noalloc(cfg, k, v, *[g.t for g in gs])
     torch.cuda.synchronize(dev)
     assert sga.device_status(dev) == 0
+    check_all(gs, "noalloc")
     assert torch.equal(got[0], want[0]) and torch.equal(got[1], want[1])
     for g, w in zip(got[2:], want[2:]):
         w64 = w.double()
@@ -72,6 +78,21 @@ def test_noalloc_matches_plan_compaction_twice(dev, kw):
     # two calls in a row on different inputs: the second must not see the first one's scratch
     _check_against_plan(cfg, seed=31, dev=dev)
     _check_against_plan(cfg, seed=32, dev=dev)
+
+
+def test_noalloc_refuses_buffers_of_the_wrong_kept_count(dev):
+    # the C call receives no buffer sizes: the binding sizes K_S/V_S by sga_kept_count and refuses
+    # any other row count before anything is launched, so nothing is written
+    cfg = sga.SGAConfig(B=1, H=2, N=6, grid_h=9, grid_w=7, sigma=4, phase_shift=True)
+    _, k, v = correlated_qkv(cfg.B, cfg.H, cfg.N, cfg.L, 64, seed=33, dtype=cfg.torch_dtype, device=dev)
+    S = sga.kept_count(cfg)
+    for wrong in (S - 1, S + 1):
+        outs = _outputs(cfg, wrong, dev)
+        with pytest.raises(ValueError):
+            sga.compact_noalloc(cfg, k, v, *outs)
+        torch.cuda.synchronize(dev)
+        assert all(torch.isnan(t).all() for t in outs)
+    assert sga.device_status(dev) == 0
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(dev):
