@@ -9,24 +9,29 @@
 // and mean components share the softmax); "RegimeVGGT ...", Key design 2 (ln g logit bias).
 //
 // Work unit: two 128-row query tiles of one segment (a (batch, head) pair, or one frame of it)
-// against all key tiles of that segment.  Roles (384 threads):
-//   warp 0      TMA producer: the two Q tiles, then a STAGES-deep ring of K and V tiles
-//   warp 1      TMEM owner and MMA issuer of query tile 0 (one elected lane issues):
-//                 S_0 = Q_0 K_j^T  (M=128, N=128, K=64; A, B from shared memory)
-//                 O_0 += P_0 V_j   (M=128, N=64,  K=128; P from TMEM, V from shared memory)
-//   warp 2      MMA issuer of query tile 1 (S_1, O_1); the two issuers take turns
+// against all key tiles of that segment.  A unit is a sequence of slots n = 2j + t (query tile t,
+// key tile j).  Roles (384 threads):
+//   warp 0      TMA producer: the two Q tiles, then a STAGES-deep ring of K and V tiles (one
+//               barrier pair per stage)
+//   warps 1, 2  MMA issuers (one elected lane each), taking turns:
+//                 S(n)  = Q_t K_j^T  (M=128, N=128, K=64; A, B from shared memory)
+//                 O_t  += P(n) V_j   (M=128, N=64,  K=128; P from TMEM, V from shared memory)
+//               batch G_n = PV(n), then QK(n + 3); issuer n mod 2 issues it once P(n) is ready
 //   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
 //   warps 8-11  softmax + epilogue of query tile 1
-// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384) P_0 [384,448) P_1 [448,512).
+// TMEM columns: O_0 [0,64) O_1 [64,128), and three S buffers [128,256) [256,384) [384,512).  The
+// S of global slot n goes to buffer n mod 3 and its P (bf16 pairs) is written over the first 64
+// columns of that S.  PV(n) frees the buffer that QK(n + 3) then fills, so each softmax
+// warpgroup finds its next S computed while it works: the tensor pipe and the softmax warps no
+// longer wait on each other tile by tile.
 // With a per-key bias (size-aware attention, "RegimeVGGT ..." Key design 2: a key standing
 // for g tokens carries the logit bias ln g), QK^T gets a fifth K = 16 step: the Q side is a
 // constant block with ones in columns 0-1, the K side holds bias/scale split into a bf16 high
 // and low part in columns 0-1 (written by the producer warp from the fp32 bias), so the
 // accumulator already contains q.k + bias/scale and the softmax is unchanged.
-// The two tiles ping-pong: while one tile's rows are exponentiated the tensor core runs the
-// other tile's products.  A running max is only moved (and O rescaled in TMEM) when a row's
-// maximum grows by more than 2^8; the final normalisation uses the same reference, so the
-// result is exact either way.
+// A row's reference max is only moved (and O rescaled in TMEM) when its logits exceed it by
+// more than 2^8; the final normalisation uses the same reference, so the result is exact either
+// way.
 #pragma once
 
 #include "extras.cuh"
@@ -41,12 +46,10 @@ constexpr int STAGES = 4;
 constexpr int TILE_BYTES = BM * HD * 2;        // one 128 x 64 bf16 tile = 16 KB
 constexpr int NUM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
-__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * (uint32_t)t; }         // S_t
-__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 64u * (uint32_t)t; }   // O_t
-__host__ __device__ constexpr uint32_t col_p(int t) { return 384u + 64u * (uint32_t)t; }   // P_t
+__host__ __device__ constexpr uint32_t col_o(int t) { return 64u * (uint32_t)t; }            // O_t
+__host__ __device__ constexpr uint32_t col_buf(uint32_t b) { return 128u + 128u * b; }     // S (then P) buffer b
+constexpr uint32_t NUM_SBUF = 3;
 constexpr float kRescaleThreshold = 8.0f;      // base-2: rescale when the max grows by > 2^8
-constexpr float kSumTrigger = 128.0f;          // a tile sum above this takes the exact max path
-constexpr int kLazyMinKeyTiles = 32;           // key ranges this long use the exponentials-first softmax
 
 // Register split (setmaxnreg): the kernel is launched with LAUNCH_REGS per thread; warpgroup 0
 // (TMA producer, two MMA issuers, one idle warp) gives registers back, the two softmax warpgroups
@@ -69,9 +72,9 @@ constexpr int EXT_BYTES = 128 * 16 * 2;
 constexpr int OFF_QEXT = OFF_V + STAGES * TILE_BYTES;
 constexpr int OFF_KEXT = OFF_QEXT + EXT_BYTES;
 constexpr int OFF_BAR = OFF_KEXT + STAGES * EXT_BYTES;
-// barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_done[2],
+// barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[3], p_ready[3], o_done[2],
 //           o_free[2], drain, q_rot, pv_done[2], turn[2]
-constexpr int NUM_BARS = 2 + 2 * STAGES + 8 + 2 + 2 + 2;
+constexpr int NUM_BARS = 2 + 2 * STAGES + 6 + 4 + 2 + 2 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
 
@@ -108,16 +111,18 @@ struct Bars {
     __device__ __forceinline__ uint32_t q_empty() const { return base + 8; }
     __device__ __forceinline__ uint32_t kv_full(int s) const { return base + 16 + 8 * s; }
     __device__ __forceinline__ uint32_t kv_empty(int s) const { return base + 16 + 8 * (STAGES + s); }
-    __device__ __forceinline__ uint32_t s_full(int t) const { return base + 16 + 8 * (2 * STAGES + t); }
-    __device__ __forceinline__ uint32_t p_ready(int t) const { return base + 16 + 8 * (2 * STAGES + 2 + t); }
-    __device__ __forceinline__ uint32_t o_done(int t) const { return base + 16 + 8 * (2 * STAGES + 4 + t); }
-    __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (2 * STAGES + 6 + t); }
-    __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (2 * STAGES + 8); }
-    __device__ __forceinline__ uint32_t q_rot() const { return base + 16 + 8 * (2 * STAGES + 9); }
-    __device__ __forceinline__ uint32_t pv_done(int t) const { return base + 16 + 8 * (2 * STAGES + 10 + t); }
-    __device__ __forceinline__ uint32_t turn(int t) const { return base + 16 + 8 * (2 * STAGES + 12 + t); }
+    // S and P of one slot: per buffer, so that no barrier can run two phases ahead of its waiter
+    // (a buffer is refilled only after the P it held has been consumed)
+    __device__ __forceinline__ uint32_t s_full(uint32_t b) const { return base + 16 + 8 * (2 * STAGES + b); }
+    __device__ __forceinline__ uint32_t p_ready(uint32_t b) const { return base + 16 + 8 * (2 * STAGES + 3 + b); }
+    __device__ __forceinline__ uint32_t o_done(int t) const { return base + 16 + 8 * (2 * STAGES + 6 + t); }
+    __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (2 * STAGES + 8 + t); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (2 * STAGES + 10); }
+    __device__ __forceinline__ uint32_t q_rot() const { return base + 16 + 8 * (2 * STAGES + 11); }
+    __device__ __forceinline__ uint32_t pv_done(int t) const { return base + 16 + 8 * (2 * STAGES + 12 + t); }
+    __device__ __forceinline__ uint32_t turn(int t) const { return base + 16 + 8 * (2 * STAGES + 14 + t); }
 };
-static_assert(16 + 8 * (2 * STAGES + 14) == NUM_BARS * 8, "barrier block size");
+static_assert(16 + 8 * (2 * STAGES + 16) == NUM_BARS * 8, "barrier block size");
 
 // Key tile processed at step j of a CTA's u_local-th unit.  All CTAs work on units of the same
 // head at the same time and sweep its key tiles; consecutive rounds sweep in opposite
@@ -154,71 +159,7 @@ __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&s)[128]) {
     }
 }
 
-// The max-first step of the online softmax for one query row and one key tile (logits s[128],
-// masked columns already -inf): the row maximum decides whether the reference max m moves (by
-// more than 2^kRescaleThreshold).  When it moves, l (and O in TMEM, when o_live) is rescaled; P
-// is (re)computed and stored whenever the reference moved or store_always is set, and tsum is
-// then this tile's sum of p.  The tile's previous PV must have completed.
-__device__ __forceinline__ void exact_tile(const float (&s)[128], uint32_t tP, uint32_t tO, float sl2,
-                                           bool o_live, bool store_always, float& m, float& l, float& tsum) {
-    // row maximum: eight independent 16-column chains, then a small tree
-    float mx8[8];
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-        float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
-#pragma unroll
-        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
-        mx8[g] = fmaxf(a, s[16 * g + 15]);
-    }
-    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]), max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-    const float m_cand = mx * sl2;
-    const bool need = m_cand > m + kRescaleThreshold;
-    const bool rescale = __any_sync(0xffffffffu, need);
-    float alpha = 1.0f;
-    if (rescale) {
-        const float m_new = fmaxf(m, m_cand);
-        alpha = ex2_approx(m - m_new);                       // 0 when m = -inf
-        l *= alpha;
-        m = m_new;
-    }
-    if (rescale || store_always) {
-        const uint64_t sc2 = f2_pack(sl2, sl2);
-        const uint64_t nm2 = f2_pack(-m, -m);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
-                const float p0 = ex2_approx(x0);
-                const float p1 = ex2_approx(x1);
-                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(tP + 16 * c, pk);
-        }
-        float a0, a1;
-        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
-        tsum = a0 + a1;
-    }
-    // O *= alpha when the reference moved; the tile's next PV waits for p_ready, so it sees
-    // both updates
-    if (rescale && o_live) {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            tmem_ld32(tO + 32 * c, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tO + 32 * c, r);
-        }
-    }
-}
-
-template <bool kBias, bool kRope, bool kLazy>
+template <bool kBias, bool kRope>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcArgs p) {
@@ -239,9 +180,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(bars.kv_full(s), 1);
             mbar_init(bars.kv_empty(s), 2);
         }
+        for (uint32_t b = 0; b < NUM_SBUF; ++b) {
+            mbar_init(bars.s_full(b), 1);
+            mbar_init(bars.p_ready(b), 128);
+        }
         for (int t = 0; t < 2; ++t) {
-            mbar_init(bars.s_full(t), 1);
-            mbar_init(bars.p_ready(t), 128);
             mbar_init(bars.o_done(t), 1);
             mbar_init(bars.o_free(t), 128);
             mbar_init(bars.pv_done(t), 1);
@@ -338,39 +281,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
       } else if (warp <= 2) {
         // ------------------------------------------------------------------ MMA issuers
-        // Warp 1 issues the products of query tile 0, warp 2 those of tile 1.  They take turns
-        // (a token passed through the turn barriers), so the tensor pipe still receives the
-        // batches in the order tile 0, tile 1, tile 0, ... and the two tiles' softmax phases
-        // alternate; each issuer does its barrier bookkeeping while the other's batch runs
-        // (the pipe only queues a few instructions ahead).  The whole warp runs the loop so
-        // descriptors and TMEM addresses stay warp-uniform; one elected lane (always the
-        // lowest) issues every MMA, commit and token arrive.  A K/V stage is released when
-        // both issuers have committed it (the barrier counts two arrivals).  Descriptors
-        // advance by adding (byte offset >> 4) to their start-address field.
+        // Slots: the n-th (query tile, key tile) pair of a unit is slot n = 2j + t; slot n's S
+        // goes to buffer (global slot index) mod 3 and its P is written over it.  Batch G_n
+        // (issued by issuer n mod 2 once slot n's P is ready) holds PV(n), then QK(n + 3), whose
+        // buffer is the one PV(n) has just read: every softmax warp finds its next S computed.
+        // The issuers take turns (token through the turn barriers) so the batches reach the
+        // tensor pipe in slot order; issuer 0 opens each unit with the first three QKs.
         const int t = warp - 1;
-        const uint64_t dq = smem_desc_sw128(sbase + OFF_Q + t * TILE_BYTES, 16);
+        const uint64_t dQ = smem_desc_sw128(sbase + OFF_Q, 16);
         const uint64_t dK = smem_desc_sw128(sbase + OFF_K, 16);
         const uint64_t dV = smem_desc_sw128(sbase + OFF_V, TILE_BYTES);
         const uint64_t dQe = smem_desc_noswz(sbase + OFF_QEXT, 128, 256);
         const uint64_t dKe = smem_desc_noswz(sbase + OFF_KEXT, 128, 256);
         constexpr uint64_t kTileStep = TILE_BYTES >> 4;
         constexpr uint64_t kExtStep = EXT_BYTES >> 4;
-        const uint32_t ts = tmem + col_s(t), to = tmem + col_o(t), tp = tmem + col_p(t);
-        // turns taken: issuer 0 holds the token first (its first wait is on the preceding,
-        // already complete phase)
-        uint32_t kv_it = 0, g_it = 0, u_local = 0, turns = 0;
+        const uint32_t to = tmem + col_o(t);
+        uint32_t kv_base = 0, slot_base = 0, g = 0, u_local = 0, turns = 0;
         bool ok = true;
-        auto issue_qk = [&](int st) {
+        auto issue_qk = [&](uint32_t slot, int tq, int st) {
+            const uint32_t ts = tmem + col_buf(slot % NUM_SBUF);
+            const uint64_t dq = dQ + (uint64_t)tq * kTileStep;
             const uint64_t dk = dK + (uint64_t)st * kTileStep;
 #pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk)                  // 16 columns = 32 bytes
+            for (int kk = 0; kk < HD / 16; ++kk)
                 mma_ss(ts, dq + 2 * kk, dk + 2 * kk, IDESC_QK, kk > 0 ? 1u : 0u);
             if (kBias) mma_ss(ts, dQe, dKe + (uint64_t)st * kExtStep, IDESC_QK, 1u);
         };
-        auto issue_pv = [&](int st, uint32_t acc) {
+        auto issue_pv = [&](uint32_t slot, int st, uint32_t acc) {
+            const uint32_t tp = tmem + col_buf(slot % NUM_SBUF);
             const uint64_t dv = dV + (uint64_t)st * kTileStep;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)                  // 16 rows = 2048 bytes
+            for (int kk = 0; kk < BN / 16; ++kk)
                 mma_ts(to, tp + 8 * kk, dv + 128 * kk, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
         };
         auto take_turn = [&]() -> bool {
@@ -383,54 +324,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             __syncwarp();
         };
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-            // Q tiles loaded (and, with the rotary embedding, rotated by the softmax warps)
-            if (!warp_wait(kRope ? bars.q_rot() : bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
-            {
-                const int st = kv_it % STAGES;
-                if (!warp_wait(bars.kv_full(st), (kv_it / STAGES) & 1, abort_flag)) { ok = false; break; }
-                if (!take_turn()) { ok = false; break; }
-                tc_fence_after();
-                if (elect_one()) {
-                    issue_qk(st);
-                    mma_commit(bars.s_full(t));
-                }
-                __syncwarp();
-                pass_turn();
-            }
-            for (int j = 0; j < n_kv; ++j, ++kv_it, ++g_it) {
-                const int st = kv_it % STAGES;
-                const bool has_next = (j + 1 < n_kv);
-                const int stn = (kv_it + 1) % STAGES;
-                const uint32_t phn = ((kv_it + 1) / STAGES) & 1;
-                if (has_next && !warp_wait(bars.kv_full(stn), phn, abort_flag)) { ok = false; break; }
-                if (!warp_wait(bars.p_ready(t), g_it & 1, abort_flag)) { ok = false; break; }
-                if (j == 0 && !warp_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
-                if (!take_turn()) { ok = false; break; }
-                tc_fence_after();
-                if (elect_one()) {
-                    // the next S of this tile first (its softmax warps have read S_t), then this
-                    // tile's PV: the tensor pipe is in order, so S_t(j+1) is ready a PV earlier;
-                    // the softmax warps wait for pv_done before they touch P_t or O_t
-                    if (has_next) {
-                        issue_qk(stn);
-                        mma_commit(bars.s_full(t));
-                    } else {
-                        // every QK of the unit has been issued: the Q tiles are free once they
-                        // complete, so the next unit's Q loads during the last softmax and PV
-                        mma_commit(bars.q_empty());
+            const int n_slots = 2 * n_kv;
+            bool q_released = false;
+            for (int n = t; n < n_slots; n += 2) {
+                const int j = n >> 1;
+                const int st = (int)((kv_base + j) % STAGES);
+                const int m = n + 3;
+                const bool has_qk = m < n_slots;
+                const uint32_t kvm = kv_base + (uint32_t)(m >> 1);
+                if (n == 0) {
+                    // the unit's first three S: slots 0, 1 (key tile 0) and 2 (key tile 1)
+                    if (!warp_wait(kRope ? bars.q_rot() : bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
+                    if (!warp_wait(bars.kv_full(kv_base % STAGES), (kv_base / STAGES) & 1, abort_flag)) { ok = false; break; }
+                    if (n_kv > 1 && !warp_wait(bars.kv_full((kv_base + 1) % STAGES), ((kv_base + 1) / STAGES) & 1, abort_flag)) { ok = false; break; }
+                    if (!take_turn()) { ok = false; break; }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_qk(slot_base, 0, (int)(kv_base % STAGES));
+                        mma_commit(bars.s_full(slot_base % NUM_SBUF));
+                        issue_qk(slot_base + 1, 1, (int)(kv_base % STAGES));
+                        mma_commit(bars.s_full((slot_base + 1) % NUM_SBUF));
+                        if (n_kv > 1) {
+                            issue_qk(slot_base + 2, 0, (int)((kv_base + 1) % STAGES));
+                            mma_commit(bars.s_full((slot_base + 2) % NUM_SBUF));
+                        }
                     }
-                    issue_pv(st, j > 0 ? 1u : 0u);
+                    __syncwarp();
+                    // issuer 0 keeps the turn: G_0 follows
+                }
+                if (has_qk && !warp_wait(bars.kv_full(kvm % STAGES), (kvm / STAGES) & 1, abort_flag)) { ok = false; break; }
+                const uint32_t sn = slot_base + (uint32_t)n;      // global slot: buffer sn % 3, fill sn / 3
+                if (!warp_wait(bars.p_ready(sn % NUM_SBUF), (sn / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
+                if (n < 2 && !warp_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (n != 0 && !take_turn()) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
+                    if (!has_qk && !q_released) mma_commit(bars.q_empty());   // every QK of this issuer issued
+                    issue_pv(slot_base + n, st, j > 0 ? 1u : 0u);
+                    if (has_qk) {
+                        issue_qk(slot_base + m, m & 1, (int)(kvm % STAGES));
+                        mma_commit(bars.s_full((slot_base + m) % NUM_SBUF));
+                    }
                 }
                 __syncwarp();
+                if (!has_qk) q_released = true;
                 pass_turn();
                 if (elect_one()) {
                     mma_commit(bars.pv_done(t));
-                    mma_commit(bars.kv_empty(st));                  // QK_j and PV_j of this tile
-                    if (!has_next) mma_commit(bars.o_done(t));
+                    mma_commit(bars.kv_empty(st));                  // this issuer's last use of the stage
+                    if (n >= n_slots - 2) mma_commit(bars.o_done(t));
                 }
                 __syncwarp();
+                ++g;
             }
             if (!ok) break;
+            kv_base += (uint32_t)n_kv;
+            slot_base += (uint32_t)n_slots;
         }
         // every MMA issued so far completes before TMEM is released
         if (elect_one()) mma_commit(bars.drain());
@@ -444,11 +393,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const int sub = warp & 3;                       // TMEM lanes [32*sub, 32*sub+32)
         const int r_in_tile = sub * 32 + lane;
         const uint32_t lane_bits = (uint32_t)(sub * 32) << 16;
-        const uint32_t tS = tmem + lane_bits + col_s(t);
         const uint32_t tO = tmem + lane_bits + col_o(t);
-        const uint32_t tP = tmem + lane_bits + col_p(t);
         const float sl2 = p.scale_log2;
-        uint32_t g_it = 0, u_local = 0;
+        uint32_t g_it = 0, u_local = 0, slot_base = 0;
         bool ok = true;
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
             const int seg = (int)(u / p.n_pairs);
@@ -493,193 +440,89 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         (xr.s_mean == -INFINITY ? 0.f : exp2f(xr.s_mean - m));
             }
 
-            // Long key ranges: exponentials against the current reference first (kLazy).  Short
-            // ones (a frame's dozen key tiles) keep the max-first step, which costs no extra pass
-            // over a unit's first key tile.
-            if constexpr (kLazy) {
-                // A row without the extra components has no reference max yet: the unit's first key
-                // tile sets it (to that tile's row maximum, as a max-first softmax would), so that
-                // the loop below can exponentiate against it right away.
-                if (__any_sync(0xffffffffu, m == -INFINITY)) {
-                    if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    float s[128];
-                    ld_row128(tS, s);
-                    tmem_wait_ld();
-                    if (key_tile(0, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
+            for (int j = 0; j < n_kv; ++j, ++g_it) {
+                // this slot's S, and then its P, live in buffer (global slot) mod 3
+                const uint32_t sn = slot_base + 2u * (uint32_t)j + (uint32_t)t;    // global slot
+                const uint32_t tS = tmem + lane_bits + col_buf(sn % NUM_SBUF);
+                if (!warp_wait(bars.s_full(sn % NUM_SBUF), (sn / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                float s[128];
+                ld_row128(tS, s);
+                tmem_wait_ld();
+                if (key_tile(j, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c)
-                            if (c >= last_valid) s[c] = -INFINITY;
-                    }
-                    float mx8[8];
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
-#pragma unroll
-                        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
-                        mx8[g] = fmaxf(a, s[16 * g + 15]);
-                    }
-                    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
-                                           max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-                    if (m == -INFINITY) m = mx * sl2;
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= last_valid) s[c] = -INFINITY;
                 }
-
-                for (int j = 0; j < n_kv; ++j, ++g_it) {
-                    if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    float s[128];
-                    ld_row128(tS, s);
-                    tmem_wait_ld();
-                    const bool ragged = key_tile(j, n_kv, u_local) == n_kv - 1 && last_valid < BN;   // warp-uniform
-                    if (ragged) {
+                // row maximum: eight independent 16-column chains, then a small tree
+                float mx8[8];
 #pragma unroll
-                        for (int c = 0; c < 128; ++c)
-                            if (c >= last_valid) s[c] = -INFINITY;
-                    }
-                    // p = 2^(s * scale_log2 - m) against the row's current reference max m, two
-                    // columns per packed FMA; P goes back to TMEM as bf16 pairs one 32-column chunk
-                    // at a time.  P_t and O_t are free once this tile's previous PV has completed;
-                    // that wait comes after the first chunk's exponentials (the PV was issued right
-                    // behind the QK that produced this S).  A row whose reference is not set yet
-                    // (m = -inf: the first key tile without the extra components) takes the exact
-                    // path at once.
-                    float tsum = 0.f;
-                    {
-                        const uint64_t sc2 = f2_pack(sl2, sl2);
-                        const uint64_t nm2 = f2_pack(-m, -m);
-                        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                for (int gg = 0; gg < 8; ++gg) {
+                    float a = max3f(s[16 * gg], s[16 * gg + 1], s[16 * gg + 2]);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                float x0, x1;
-                                f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
-                                const float p0 = ex2_approx(x0);
-                                const float p1 = ex2_approx(x1);
-                                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                                pk[i] = pack_bf16x2(p0, p1);
-                            }
-                            if (c == 0 && j > 0) {
-                                if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
-                                tc_fence_after();
-                            }
-                            tmem_st16(tP + 16 * c, pk);
-                        }
-                        if (!ok) break;
-                        float a0, a1;
-                        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
-                        tsum = a0 + a1;
-                        // The reference max moves (and O is rescaled) only when a row's logits exceed
-                        // it by more than 2^kRescaleThreshold.  A row whose tile sum is at most
-                        // kSumTrigger = 2^7 has every p <= 2^7: its logits stay at least 1 below that
-                        // bound, a margin far above the rounding of the two computations, so the P
-                        // just stored is final.  Otherwise (rare: many large p) the decision is taken
-                        // exactly as a max-first softmax takes it, and P is recomputed when the
-                        // reference moves.
-                        if (__any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
-                            // the logits again from TMEM (S_t(j) stays intact until p_ready)
-                            float s2[128];
-                            ld_row128(tS, s2);
-                            tmem_wait_ld();
-                            if (ragged) {
-#pragma unroll
-                                for (int c = 0; c < 128; ++c)
-                                    if (c >= last_valid) s2[c] = -INFINITY;
-                            }
-                            tmem_wait_st();                              // the P stores above are done
-                            exact_tile(s2, tP, tO, sl2, j > 0, false, m, l, tsum);
-                        }
-                    }
-                    l += tsum;
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(bars.p_ready(t));
+                    for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * gg + c], s[16 * gg + c + 1]);
+                    mx8[gg] = fmaxf(a, s[16 * gg + 15]);
                 }
-                if (!ok) break;
-            } else {
-                for (int j = 0; j < n_kv; ++j, ++g_it) {
-                    if (!warp_wait(bars.s_full(t), g_it & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    float s[128];
-                    ld_row128(tS, s);
-                    tmem_wait_ld();
-                    if (key_tile(j, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
-#pragma unroll
-                        for (int c = 0; c < 128; ++c)
-                            if (c >= last_valid) s[c] = -INFINITY;
-                    }
-                    // row maximum: eight independent 16-column chains, then a small tree
-                    float mx8[8];
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        float a = max3f(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
-#pragma unroll
-                        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * g + c], s[16 * g + c + 1]);
-                        mx8[g] = fmaxf(a, s[16 * g + 15]);
-                    }
-                    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
-                                           max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-                    const float m_cand = mx * sl2;
-                    const bool need = m_cand > m + kRescaleThreshold;
-                    const bool rescale = __any_sync(0xffffffffu, need);
-                    float alpha = 1.0f;
-                    if (rescale) {
-                        const float m_new = fmaxf(m, m_cand);
-                        alpha = ex2_approx(m - m_new);               // 0 when m = -inf
-                        l *= alpha;
-                        m = m_new;
-                    }
-                    // P_t and O_t are free once this tile's previous PV has completed (it was issued
-                    // after the QK that produced this S, so it is usually done already)
-                    if (j > 0) {
-                        if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                    }
-                    // p = 2^(s * scale_log2 - m), two columns per packed FMA; P goes back to TMEM
-                    // as bf16 pairs one 32-column chunk at a time
-                    const uint64_t sc2 = f2_pack(sl2, sl2);
-                    const uint64_t nm2 = f2_pack(-m, -m);
-                    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float x0, x1;
-                            f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
-                            const float p0 = ex2_approx(x0);
-                            const float p1 = ex2_approx(x1);
-                            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                            pk[i] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st16(tP + 16 * c, pk);
-                    }
-                    {
-                        float a0, a1;
-                        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
-                        l += a0 + a1;
-                    }
-                    // O *= alpha when the reference max moved (the logits are dead by now; the
-                    // previous PV has completed); this tile's next PV waits for p_ready, so it sees
-                    // both updates
-                    if (rescale && j > 0) {
-                        uint32_t r[32];
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            tmem_ld32(tO + 32 * c, r);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            tmem_st32(tO + 32 * c, r);
-                        }
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(bars.p_ready(t));
+                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                const float m_cand = mx * sl2;
+                const bool need = m_cand > m + kRescaleThreshold;
+                const bool rescale = __any_sync(0xffffffffu, need);
+                float alpha = 1.0f;
+                if (rescale) {
+                    const float m_new = fmaxf(m, m_cand);
+                    alpha = ex2_approx(m - m_new);               // 0 when m = -inf
+                    l *= alpha;
+                    m = m_new;
                 }
-                if (!ok) break;
+                // p = 2^(s * scale_log2 - m), two columns per packed FMA; P goes over the first
+                // 64 columns of this slot's S as bf16 pairs, one 32-column chunk at a time (the
+                // whole row of S is in registers already)
+                const uint64_t sc2 = f2_pack(sl2, sl2);
+                const uint64_t nm2 = f2_pack(-m, -m);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + 16 * c, pk);
+                }
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                    l += a0 + a1;
+                }
+                // O *= alpha when the reference moved, once this tile's previous PV has
+                // completed (the logits are dead by now); this slot's PV waits for p_ready, so it
+                // sees the update
+                if (rescale && j > 0) {
+                    if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t r[32];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld32(tO + 32 * c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tO + 32 * c, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bars.p_ready(sn % NUM_SBUF));
             }
+            if (!ok) break;
+            slot_base += 2u * (uint32_t)n_kv;
+
             // epilogue: O from TMEM, extra components, normalisation, store
             if (!warp_wait(bars.o_done(t), u_local & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();

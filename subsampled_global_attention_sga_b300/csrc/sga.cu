@@ -25,7 +25,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool init = false;
     int sm_count = 0;
-    bool tc_ready[2][2][2] = {};                               // attn_tc_kernel<bias, rope, lazy> ready
+    bool tc_ready[2][2] = {};                                  // attn_tc_kernel<bias, rope> ready
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -125,29 +125,29 @@ struct AttnProblem {
 // The tensor-core kernel instantiation for a bias setting, checked once per device: its
 // setmaxnreg split assumes exactly LAUNCH_REGS registers per thread at launch (any other count
 // would leave setmaxnreg.inc unsatisfiable), and it needs the large dynamic shared memory.
-template <bool kBias, bool kRope, bool kLazy>
+template <bool kBias, bool kRope>
 sga_status prepare_tc(DeviceInfo* di) {
     namespace T = sga::tc;
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (di->tc_ready[kBias][kRope][kLazy]) return SGA_OK;
+    if (di->tc_ready[kBias][kRope]) return SGA_OK;
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias, kRope, kLazy>) != cudaSuccess) return SGA_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias, kRope>) != cudaSuccess) return SGA_ERR_CUDA;
     if (fa.numRegs != (int)T::LAUNCH_REGS) return SGA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias, kRope, kLazy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias, kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_BYTES) != cudaSuccess)
         return SGA_ERR_CUDA;
-    di->tc_ready[kBias][kRope][kLazy] = true;
+    di->tc_ready[kBias][kRope] = true;
     return SGA_OK;
 }
 
 // Launch one instantiation of the tensor-core kernel.
-template <bool kBias, bool kRope, bool kLazy>
+template <bool kBias, bool kRope>
 sga_status launch_tc(DeviceInfo* di, long long grid, const CUtensorMap& mq, const CUtensorMap& mk,
                      const CUtensorMap& mv, const sga::tc::TcArgs& a, cudaStream_t stream) {
     namespace T = sga::tc;
-    sga_status st = prepare_tc<kBias, kRope, kLazy>(di);
+    sga_status st = prepare_tc<kBias, kRope>(di);
     if (st != SGA_OK) return st;
-    T::attn_tc_kernel<kBias, kRope, kLazy><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+    T::attn_tc_kernel<kBias, kRope><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
     return launch_status();
 }
 
@@ -186,17 +186,9 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.inv_scale = 1.0f / pb.scale;
         a.drop_kv = pb.drop_kv;
         const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
-        // the exponentials-first softmax pays off over long key ranges; short ones (frame-local
-        // attention: 11 key tiles per frame) keep the max-first step
-        const bool lazy = a.n_kv_tiles >= T::kLazyMinKeyTiles;
-        if (pb.bias)
-            return lazy ? launch_tc<true, false, true>(di, grid, mq, mk, mv, a, stream)
-                        : launch_tc<true, false, false>(di, grid, mq, mk, mv, a, stream);
-        if (pb.rope)
-            return lazy ? launch_tc<false, true, true>(di, grid, mq, mk, mv, a, stream)
-                        : launch_tc<false, true, false>(di, grid, mq, mk, mv, a, stream);
-        return lazy ? launch_tc<false, false, true>(di, grid, mq, mk, mv, a, stream)
-                    : launch_tc<false, false, false>(di, grid, mq, mk, mv, a, stream);
+        if (pb.bias) return launch_tc<true, false>(di, grid, mq, mk, mv, a, stream);
+        if (pb.rope) return launch_tc<false, true>(di, grid, mq, mk, mv, a, stream);
+        return launch_tc<false, false>(di, grid, mq, mk, mv, a, stream);
     }
     if (kern != SGA_KERNEL_SIMT) return SGA_ERR_INVALID_ARG;
     sga::SimtArgs a;
