@@ -31,7 +31,8 @@
 // accumulator already contains q.k + bias/scale and the softmax is unchanged.
 // A row's reference max is only moved (and O rescaled in TMEM) when its logits exceed it by
 // more than 2^8; the final normalisation uses the same reference, so the result is exact either
-// way.
+// way.  The exponentials are taken against the current reference first; a tile sum above 2^7
+// sends the tile to the max-first decision, so the row maximum is off the per-tile path.
 #pragma once
 
 #include "extras.cuh"
@@ -50,6 +51,7 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return 64u * (uint32_t)t; 
 __host__ __device__ constexpr uint32_t col_buf(uint32_t b) { return 128u + 128u * b; }     // S (then P) buffer b
 constexpr uint32_t NUM_SBUF = 3;
 constexpr float kRescaleThreshold = 8.0f;      // base-2: rescale when the max grows by > 2^8
+constexpr float kSumTrigger = 128.0f;          // a tile sum above this takes the max-first decision
 
 // Register split (setmaxnreg): the kernel is launched with LAUNCH_REGS per thread; warpgroup 0
 // (TMA producer, two MMA issuers, one idle warp) gives registers back, the two softmax warpgroups
@@ -440,6 +442,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         (xr.s_mean == -INFINITY ? 0.f : exp2f(xr.s_mean - m));
             }
 
+            // A row without the extra components has no reference max yet: the unit's first key
+            // tile sets it to that tile's row maximum (as a max-first softmax would), so the loop
+            // can exponentiate against it at once.  This reads S before any P is written over it.
+            if (__any_sync(0xffffffffu, m == -INFINITY)) {
+                const uint32_t sn0 = slot_base + (uint32_t)t;
+                const uint32_t tS0 = tmem + lane_bits + col_buf(sn0 % NUM_SBUF);
+                if (!warp_wait(bars.s_full(sn0 % NUM_SBUF), (sn0 / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                float s[128];
+                ld_row128(tS0, s);
+                tmem_wait_ld();
+                if (key_tile(0, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= last_valid) s[c] = -INFINITY;
+                }
+                float mx8[8];
+#pragma unroll
+                for (int gg = 0; gg < 8; ++gg) {
+                    float a = max3f(s[16 * gg], s[16 * gg + 1], s[16 * gg + 2]);
+#pragma unroll
+                    for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * gg + c], s[16 * gg + c + 1]);
+                    mx8[gg] = fmaxf(a, s[16 * gg + 15]);
+                }
+                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                if (m == -INFINITY) m = mx * sl2;
+            }
+
             for (int j = 0; j < n_kv; ++j, ++g_it) {
                 // this slot's S, and then its P, live in buffer (global slot) mod 3
                 const uint32_t sn = slot_base + 2u * (uint32_t)j + (uint32_t)t;    // global slot
@@ -454,32 +485,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     for (int c = 0; c < 128; ++c)
                         if (c >= last_valid) s[c] = -INFINITY;
                 }
-                // row maximum: eight independent 16-column chains, then a small tree
-                float mx8[8];
-#pragma unroll
-                for (int gg = 0; gg < 8; ++gg) {
-                    float a = max3f(s[16 * gg], s[16 * gg + 1], s[16 * gg + 2]);
-#pragma unroll
-                    for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * gg + c], s[16 * gg + c + 1]);
-                    mx8[gg] = fmaxf(a, s[16 * gg + 15]);
-                }
-                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
-                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-                const float m_cand = mx * sl2;
-                const bool need = m_cand > m + kRescaleThreshold;
-                const bool rescale = __any_sync(0xffffffffu, need);
-                float alpha = 1.0f;
-                if (rescale) {
-                    const float m_new = fmaxf(m, m_cand);
-                    alpha = ex2_approx(m - m_new);               // 0 when m = -inf
-                    l *= alpha;
-                    m = m_new;
-                }
-                // p = 2^(s * scale_log2 - m), two columns per packed FMA; P goes over the first
-                // 64 columns of this slot's S as bf16 pairs, one 32-column chunk at a time (the
-                // whole row of S is in registers already)
+                // p = 2^(s * scale_log2 - m) against the row's current reference max m (the whole
+                // row of S is in registers, so P can go over it at once); the tile sum decides
+                // whether that was final
                 const uint64_t sc2 = f2_pack(sl2, sl2);
-                const uint64_t nm2 = f2_pack(-m, -m);
+                uint64_t nm2 = f2_pack(-m, -m);
                 uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -495,27 +505,71 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     }
                     tmem_st16(tS + 16 * c, pk);
                 }
+                float tsum;
                 {
                     float a0, a1;
                     f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
-                    l += a0 + a1;
+                    tsum = a0 + a1;
                 }
-                // O *= alpha when the reference moved, once this tile's previous PV has
-                // completed (the logits are dead by now); this slot's PV waits for p_ready, so it
-                // sees the update
-                if (rescale && j > 0) {
-                    if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    uint32_t r[32];
+                // The reference moves (and O is rescaled) only when a row's logits exceed it by
+                // more than 2^kRescaleThreshold.  A tile sum of at most 2^7 puts every p at or
+                // below 2^7, so every logit stays at least 1 below that bound: the P just stored
+                // is final.  Otherwise (rare) the decision is taken on the row maximum as a
+                // max-first softmax takes it, and P is recomputed when the reference moves.
+                if (__any_sync(0xffffffffu, !(tsum <= kSumTrigger))) {
+                    float mx8[8];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        tmem_ld32(tO + 32 * c, r);
-                        tmem_wait_ld();
+                    for (int gg = 0; gg < 8; ++gg) {
+                        float a = max3f(s[16 * gg], s[16 * gg + 1], s[16 * gg + 2]);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tO + 32 * c, r);
+                        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * gg + c], s[16 * gg + c + 1]);
+                        mx8[gg] = fmaxf(a, s[16 * gg + 15]);
+                    }
+                    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                           max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                    const float m_cand = mx * sl2;
+                    const bool need = m_cand > m + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float m_new = fmaxf(m, m_cand);
+                        const float alpha = ex2_approx(m - m_new);
+                        l *= alpha;
+                        m = m_new;
+                        nm2 = f2_pack(-m, -m);
+                        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+                        tmem_wait_st();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                float x0, x1;
+                                f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sc2, nm2), x0, x1);
+                                const float p0 = ex2_approx(x0);
+                                const float p1 = ex2_approx(x1);
+                                acc2[i & 3] = f2_add(acc2[i & 3], f2_pack(p0, p1));
+                                pk[i] = pack_bf16x2(p0, p1);
+                            }
+                            tmem_st16(tS + 16 * c, pk);
+                        }
+                        float a0, a1;
+                        f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), a0, a1);
+                        tsum = a0 + a1;
+                        if (j > 0) {
+                            if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
+                            tc_fence_after();
+                            uint32_t r[32];
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                tmem_ld32(tO + 32 * c, r);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                                tmem_st32(tO + 32 * c, r);
+                            }
+                        }
                     }
                 }
+                l += tsum;
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bars.p_ready(sn % NUM_SBUF));
