@@ -10,13 +10,16 @@
 //
 // Work unit: two 128-row query tiles of one segment (a (batch, head) pair, or one frame of it)
 // against all key tiles of that segment.  A unit is a sequence of slots n = 2j + t (query tile t,
-// key tile j).  Roles (384 threads):
-//   warp 0      TMA producer: the two Q tiles, then a STAGES-deep ring of K and V tiles (one
-//               barrier pair per stage)
+// key tile j); a CTA numbers the slots of its units on from one unit to the next.  Roles (384
+// threads):
+//   warp 0      TMA producer: the two Q tiles of a unit (into one of two Q buffers, so the next
+//               unit's are in place before this one ends), then a STAGES-deep ring of K and V
+//               tiles (one barrier pair per stage)
 //   warps 1, 2  MMA issuers (one elected lane each), taking turns:
 //                 S(n)  = Q_t K_j^T  (M=128, N=128, K=64; A, B from shared memory)
 //                 O_t  += P(n) V_j   (M=128, N=64,  K=128; P from TMEM, V from shared memory)
-//               batch G_n = PV(n), then QK(n + 3); issuer n mod 2 issues it once P(n) is ready
+//               batch G_n = PV(n), then QK(n + 3) (possibly of the next unit); issuer n mod 2
+//               issues it once P(n) is ready
 //   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
 //   warps 8-11  softmax + epilogue of query tile 1
 // TMEM columns: O_0 [0,64) O_1 [64,128), and three S buffers [128,256) [256,384) [384,512).  The
@@ -65,7 +68,7 @@ static_assert(LAUNCH_REGS * NUM_THREADS <= 65536, "register file");
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+constexpr int OFF_K = OFF_Q + 4 * TILE_BYTES;          // Q: two buffers of two tiles
 constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
 // bias blocks: 128 rows x 16 bf16 columns in the no-swizzle K-major core-matrix layout
 // (8 rows x 16 bytes per core matrix; LBO = 128 B between the two K halves, SBO = 256 B
@@ -74,9 +77,9 @@ constexpr int EXT_BYTES = 128 * 16 * 2;
 constexpr int OFF_QEXT = OFF_V + STAGES * TILE_BYTES;
 constexpr int OFF_KEXT = OFF_QEXT + EXT_BYTES;
 constexpr int OFF_BAR = OFF_KEXT + STAGES * EXT_BYTES;
-// barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[3], p_ready[3], o_done[2],
-//           o_free[2], drain, q_rot, pv_done[2], turn[2]
-constexpr int NUM_BARS = 2 + 2 * STAGES + 6 + 4 + 2 + 2 + 2;
+// barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[3], p_ready[3], o_done[2],
+//           o_free[2], drain, q_rot[2], pv_done[2], turn[2]
+constexpr int NUM_BARS = 4 + 2 * STAGES + 6 + 4 + 1 + 2 + 2 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
 
@@ -109,22 +112,23 @@ __host__ __device__ constexpr uint32_t ext_off(int r, int c) {
 // mbarrier addresses (computed, so that no dynamically indexed array lands in local memory)
 struct Bars {
     uint32_t base;
-    __device__ __forceinline__ uint32_t q_full() const { return base; }
-    __device__ __forceinline__ uint32_t q_empty() const { return base + 8; }
-    __device__ __forceinline__ uint32_t kv_full(int s) const { return base + 16 + 8 * s; }
-    __device__ __forceinline__ uint32_t kv_empty(int s) const { return base + 16 + 8 * (STAGES + s); }
+    // Q buffer b holds the two query tiles of the CTA's units with u_local mod 2 == b
+    __device__ __forceinline__ uint32_t q_full(uint32_t b) const { return base + 8 * b; }
+    __device__ __forceinline__ uint32_t q_empty(uint32_t b) const { return base + 16 + 8 * b; }
+    __device__ __forceinline__ uint32_t kv_full(int s) const { return base + 32 + 8 * s; }
+    __device__ __forceinline__ uint32_t kv_empty(int s) const { return base + 32 + 8 * (STAGES + s); }
     // S and P of one slot: per buffer, so that no barrier can run two phases ahead of its waiter
     // (a buffer is refilled only after the P it held has been consumed)
-    __device__ __forceinline__ uint32_t s_full(uint32_t b) const { return base + 16 + 8 * (2 * STAGES + b); }
-    __device__ __forceinline__ uint32_t p_ready(uint32_t b) const { return base + 16 + 8 * (2 * STAGES + 3 + b); }
-    __device__ __forceinline__ uint32_t o_done(int t) const { return base + 16 + 8 * (2 * STAGES + 6 + t); }
-    __device__ __forceinline__ uint32_t o_free(int t) const { return base + 16 + 8 * (2 * STAGES + 8 + t); }
-    __device__ __forceinline__ uint32_t drain() const { return base + 16 + 8 * (2 * STAGES + 10); }
-    __device__ __forceinline__ uint32_t q_rot() const { return base + 16 + 8 * (2 * STAGES + 11); }
-    __device__ __forceinline__ uint32_t pv_done(int t) const { return base + 16 + 8 * (2 * STAGES + 12 + t); }
-    __device__ __forceinline__ uint32_t turn(int t) const { return base + 16 + 8 * (2 * STAGES + 14 + t); }
+    __device__ __forceinline__ uint32_t s_full(uint32_t b) const { return base + 32 + 8 * (2 * STAGES + b); }
+    __device__ __forceinline__ uint32_t p_ready(uint32_t b) const { return base + 32 + 8 * (2 * STAGES + 3 + b); }
+    __device__ __forceinline__ uint32_t o_done(int t) const { return base + 32 + 8 * (2 * STAGES + 6 + t); }
+    __device__ __forceinline__ uint32_t o_free(int t) const { return base + 32 + 8 * (2 * STAGES + 8 + t); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 32 + 8 * (2 * STAGES + 10); }
+    __device__ __forceinline__ uint32_t q_rot(uint32_t b) const { return base + 32 + 8 * (2 * STAGES + 11 + b); }
+    __device__ __forceinline__ uint32_t pv_done(int t) const { return base + 32 + 8 * (2 * STAGES + 13 + t); }
+    __device__ __forceinline__ uint32_t turn(int t) const { return base + 32 + 8 * (2 * STAGES + 15 + t); }
 };
-static_assert(16 + 8 * (2 * STAGES + 16) == NUM_BARS * 8, "barrier block size");
+static_assert(32 + 8 * (2 * STAGES + 17) == NUM_BARS * 8, "barrier block size");
 
 // Key tile processed at step j of a CTA's u_local-th unit.  All CTAs work on units of the same
 // head at the same time and sweep its key tiles; consecutive rounds sweep in opposite
@@ -176,8 +180,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(bars.q_full(), 1);
-        mbar_init(bars.q_empty(), 2);                   // one commit per MMA issuer
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(bars.q_full(b), 1);
+            mbar_init(bars.q_empty(b), 2);              // the QKs of the unit's last two slots
+            mbar_init(bars.q_rot(b), 256);
+        }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bars.kv_full(s), 1);
             mbar_init(bars.kv_empty(s), 2);
@@ -193,7 +200,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(bars.turn(t), 1);
         }
         mbar_init(bars.drain(), 2);
-        mbar_init(bars.q_rot(), 256);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmQ);
@@ -233,11 +239,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
             const int seg = (int)(u / p.n_pairs);
             const int row0 = (int)(u % p.n_pairs) * 2 * BM;
-            if (!warp_wait(bars.q_empty(), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
+            const uint32_t qb = u_local & 1;
+            if (!warp_wait(bars.q_empty(qb), ((u_local >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
             if (elect_one()) {
-                mbar_arrive_expect_tx(bars.q_full(), 2 * TILE_BYTES);
-                tma_load_3d(sbase + OFF_Q, &tmQ, bars.q_full(), 0, row0, seg);
-                tma_load_3d(sbase + OFF_Q + TILE_BYTES, &tmQ, bars.q_full(), 0, row0 + BM, seg);
+                const uint32_t dst = sbase + OFF_Q + qb * 2 * TILE_BYTES;
+                mbar_arrive_expect_tx(bars.q_full(qb), 2 * TILE_BYTES);
+                tma_load_3d(dst, &tmQ, bars.q_full(qb), 0, row0, seg);
+                tma_load_3d(dst + TILE_BYTES, &tmQ, bars.q_full(qb), 0, row0 + BM, seg);
             }
             __syncwarp();
             ++q_issued;
@@ -279,16 +287,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             // let the copies already issued land before the CTA leaves
             for (uint32_t i = (kv_issued > STAGES ? kv_issued - STAGES : 0); i < kv_issued; ++i)
                 if ((long long)i != p.drop_kv) drain_wait(bars.kv_full(i % STAGES), (i / STAGES) & 1);
-            if (q_issued > 0) drain_wait(bars.q_full(), (q_issued - 1) & 1);
+            for (uint32_t i = (q_issued > 2 ? q_issued - 2 : 0); i < q_issued; ++i)
+                drain_wait(bars.q_full(i & 1), (i >> 1) & 1);
         }
       } else if (warp <= 2) {
         // ------------------------------------------------------------------ MMA issuers
-        // Slots: the n-th (query tile, key tile) pair of a unit is slot n = 2j + t; slot n's S
-        // goes to buffer (global slot index) mod 3 and its P is written over it.  Batch G_n
-        // (issued by issuer n mod 2 once slot n's P is ready) holds PV(n), then QK(n + 3), whose
-        // buffer is the one PV(n) has just read: every softmax warp finds its next S computed.
-        // The issuers take turns (token through the turn barriers) so the batches reach the
-        // tensor pipe in slot order; issuer 0 opens each unit with the first three QKs.
+        // Slots: the n-th (query tile, key tile) pair of a unit is slot n = 2j + t; the CTA's
+        // slots are numbered on across its units (global slot s = u_local * 2 n_kv + n, key ring
+        // entry s / 2).  Slot s's S goes to buffer s mod 3 and its P is written over it.  Batch G_s
+        // (issued by issuer s mod 2 once P(s) is ready) holds PV(s), then QK(s + 3), whose buffer
+        // is the one PV(s) has just read; QK(s + 3) may belong to the next unit (its Q tiles sit
+        // in the other Q buffer), so the tensor pipe runs on across unit boundaries and every
+        // softmax warp finds its next S computed.  The issuers take turns (token through the turn
+        // barriers) so the batches reach the tensor pipe in slot order; issuer 0 opens with the
+        // first three QKs.
         const int t = warp - 1;
         const uint64_t dQ = smem_desc_sw128(sbase + OFF_Q, 16);
         const uint64_t dK = smem_desc_sw128(sbase + OFF_K, 16);
@@ -298,19 +310,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         constexpr uint64_t kTileStep = TILE_BYTES >> 4;
         constexpr uint64_t kExtStep = EXT_BYTES >> 4;
         const uint32_t to = tmem + col_o(t);
-        uint32_t kv_base = 0, slot_base = 0, g = 0, u_local = 0, turns = 0;
+        const uint32_t n_slots = 2u * (uint32_t)n_kv;
+        const uint32_t my_units = (uint32_t)((p.n_units - 1 - blockIdx.x) / gridDim.x + 1);   // grid <= n_units
+        const uint32_t total = my_units * n_slots;
+        uint32_t turns = 0;
         bool ok = true;
-        auto issue_qk = [&](uint32_t slot, int tq, int st) {
-            const uint32_t ts = tmem + col_buf(slot % NUM_SBUF);
-            const uint64_t dq = dQ + (uint64_t)tq * kTileStep;
+        // waits (whole warp) for what QK of slot (unit ul, n) reads: its key tile and the unit's Q
+        // (each issuer waits on the Q barrier itself: slots 0-2 of a unit alternate issuers)
+        auto qk_ready = [&](uint32_t ul, uint32_t n) -> bool {
+            const uint32_t e = ul * (uint32_t)n_kv + (n >> 1);
+            if (!warp_wait(bars.kv_full((int)(e % STAGES)), (e / STAGES) & 1, abort_flag)) return false;
+            if (n < 3 && !warp_wait(kRope ? bars.q_rot(ul & 1) : bars.q_full(ul & 1), (ul >> 1) & 1, abort_flag))
+                return false;
+            return true;
+        };
+        auto issue_qk = [&](uint32_t s, uint32_t ul, uint32_t n) {
+            const uint32_t e = ul * (uint32_t)n_kv + (n >> 1);
+            const int st = (int)(e % STAGES);
+            const uint32_t ts = tmem + col_buf(s % NUM_SBUF);
+            const uint64_t dq = dQ + (uint64_t)(2 * (ul & 1) + (n & 1)) * kTileStep;
             const uint64_t dk = dK + (uint64_t)st * kTileStep;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
                 mma_ss(ts, dq + 2 * kk, dk + 2 * kk, IDESC_QK, kk > 0 ? 1u : 0u);
             if (kBias) mma_ss(ts, dQe, dKe + (uint64_t)st * kExtStep, IDESC_QK, 1u);
+            mma_commit(bars.s_full(s % NUM_SBUF));
+            if (n + 2 >= n_slots) mma_commit(bars.q_empty(ul & 1));   // the unit's last two QKs
         };
-        auto issue_pv = [&](uint32_t slot, int st, uint32_t acc) {
-            const uint32_t tp = tmem + col_buf(slot % NUM_SBUF);
+        auto issue_pv = [&](uint32_t s, int st, uint32_t acc) {
+            const uint32_t tp = tmem + col_buf(s % NUM_SBUF);
             const uint64_t dv = dV + (uint64_t)st * kTileStep;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
@@ -325,63 +353,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             if (elect_one()) mbar_arrive(bars.turn(t ^ 1));
             __syncwarp();
         };
-        for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-            const int n_slots = 2 * n_kv;
-            bool q_released = false;
-            for (int n = t; n < n_slots; n += 2) {
-                const int j = n >> 1;
-                const int st = (int)((kv_base + j) % STAGES);
-                const int m = n + 3;
-                const bool has_qk = m < n_slots;
-                const uint32_t kvm = kv_base + (uint32_t)(m >> 1);
-                if (n == 0) {
-                    // the unit's first three S: slots 0, 1 (key tile 0) and 2 (key tile 1)
-                    if (!warp_wait(kRope ? bars.q_rot() : bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
-                    if (!warp_wait(bars.kv_full(kv_base % STAGES), (kv_base / STAGES) & 1, abort_flag)) { ok = false; break; }
-                    if (n_kv > 1 && !warp_wait(bars.kv_full((kv_base + 1) % STAGES), ((kv_base + 1) / STAGES) & 1, abort_flag)) { ok = false; break; }
-                    if (!take_turn()) { ok = false; break; }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        issue_qk(slot_base, 0, (int)(kv_base % STAGES));
-                        mma_commit(bars.s_full(slot_base % NUM_SBUF));
-                        issue_qk(slot_base + 1, 1, (int)(kv_base % STAGES));
-                        mma_commit(bars.s_full((slot_base + 1) % NUM_SBUF));
-                        if (n_kv > 1) {
-                            issue_qk(slot_base + 2, 0, (int)((kv_base + 1) % STAGES));
-                            mma_commit(bars.s_full((slot_base + 2) % NUM_SBUF));
-                        }
-                    }
-                    __syncwarp();
-                    // issuer 0 keeps the turn: G_0 follows
-                }
-                if (has_qk && !warp_wait(bars.kv_full(kvm % STAGES), (kvm / STAGES) & 1, abort_flag)) { ok = false; break; }
-                const uint32_t sn = slot_base + (uint32_t)n;      // global slot: buffer sn % 3, fill sn / 3
-                if (!warp_wait(bars.p_ready(sn % NUM_SBUF), (sn / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
-                if (n < 2 && !warp_wait(bars.o_free(t), (u_local & 1) ^ 1, abort_flag)) { ok = false; break; }
-                if (n != 0 && !take_turn()) { ok = false; break; }
+        if (t == 0) {
+            // the first three S: slots 0, 1 (key tile 0) and 2 (key tile 1, or the next unit)
+            uint32_t ul = 0, n = 0;
+            for (uint32_t s = 0; s < 3 && s < total && ok; ++s) {
+                if (!qk_ready(ul, n)) { ok = false; break; }
                 tc_fence_after();
-                if (elect_one()) {
-                    if (!has_qk && !q_released) mma_commit(bars.q_empty());   // every QK of this issuer issued
-                    issue_pv(slot_base + n, st, j > 0 ? 1u : 0u);
-                    if (has_qk) {
-                        issue_qk(slot_base + m, m & 1, (int)(kvm % STAGES));
-                        mma_commit(bars.s_full((slot_base + m) % NUM_SBUF));
-                    }
-                }
+                if (elect_one()) issue_qk(s, ul, n);
                 __syncwarp();
-                if (!has_qk) q_released = true;
-                pass_turn();
-                if (elect_one()) {
-                    mma_commit(bars.pv_done(t));
-                    mma_commit(bars.kv_empty(st));                  // this issuer's last use of the stage
-                    if (n >= n_slots - 2) mma_commit(bars.o_done(t));
-                }
-                __syncwarp();
-                ++g;
+                if (++n == n_slots) { n = 0; ++ul; }
             }
-            if (!ok) break;
-            kv_base += (uint32_t)n_kv;
-            slot_base += (uint32_t)n_slots;
+        }
+        // batch G_s: slot s = (unit ul, n); QK(s + 3) = (unit ulm, nm).  Everything the batch
+        // waits for is waited for before the turn is taken, so the turn is held only to issue;
+        // the one exception is a RoPE unit's rotated Q (see below).
+        uint32_t ul = 0, n = (uint32_t)t;
+        uint32_t ulm = 0, nm = (uint32_t)t + 3;
+        while (nm >= n_slots) { nm -= n_slots; ++ulm; }
+        for (uint32_t s = (uint32_t)t; s < total && ok; s += 2) {
+            const uint32_t j = n >> 1;
+            const int st = (int)((s >> 1) % STAGES);
+            const bool has_qk = s + 3 < total;
+            // with RoPE the next unit's Q is rotated by the softmax warps once they are through
+            // this unit's tiles, and one of them may still wait for PV(s): that QK waits for the
+            // rotation after PV(s) has been issued
+            const bool late_q = kRope && has_qk && nm < 3;
+            if (has_qk) {
+                const uint32_t e = ulm * (uint32_t)n_kv + (nm >> 1);
+                if (!warp_wait(bars.kv_full((int)(e % STAGES)), (e / STAGES) & 1, abort_flag)) { ok = false; break; }
+                if (!kRope && nm < 3 && !warp_wait(bars.q_full(ulm & 1), (ulm >> 1) & 1, abort_flag)) { ok = false; break; }
+            }
+            if (!warp_wait(bars.p_ready(s % NUM_SBUF), (s / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
+            if (n < 2 && !warp_wait(bars.o_free(t), (ul & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (!take_turn()) { ok = false; break; }
+            tc_fence_after();
+            if (elect_one()) {
+                issue_pv(s, st, j > 0 ? 1u : 0u);
+                if (n + 2 >= n_slots) mma_commit(bars.o_done(t));
+                if (has_qk && !late_q) issue_qk(s + 3, ulm, nm);
+            }
+            __syncwarp();
+            if (late_q) {
+                if (!warp_wait(bars.q_rot(ulm & 1), (ulm >> 1) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) issue_qk(s + 3, ulm, nm);
+                __syncwarp();
+            }
+            pass_turn();
+            if (elect_one()) {
+                mma_commit(bars.pv_done(t));
+                mma_commit(bars.kv_empty(st));                  // this issuer's last use of the stage
+            }
+            __syncwarp();
+            n += 2;
+            if (n >= n_slots) { n -= n_slots; ++ul; }
+            nm += 2;
+            while (nm >= n_slots) { nm -= n_slots; ++ulm; }
         }
         // every MMA issued so far completes before TMEM is released
         if (elect_one()) mma_commit(bars.drain());
@@ -397,6 +424,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const uint32_t lane_bits = (uint32_t)(sub * 32) << 16;
         const uint32_t tO = tmem + lane_bits + col_o(t);
         const float sl2 = p.scale_log2;
+        // RoPE: rotate this thread's row of query tile t of unit uu (the CTA's ul-th) in its Q
+        // buffer (128-byte swizzle: the 16-byte chunk c of row r sits at chunk c ^ (r mod 8)), then
+        // release it to the MMA.  The first unit's rows are rotated up front, every later unit's
+        // as soon as this warpgroup is through the tiles of the unit before it.
+        auto rotate_q = [&](long long uu, uint32_t ul) -> bool {
+            if (!warp_wait(bars.q_full(ul & 1), (ul >> 1) & 1, abort_flag)) return false;
+            const int rrow = (int)(uu % p.n_pairs) * 2 * BM + t * BM + r_in_tile;
+            if (rrow < p.seg_rows) {
+                uint8_t* qrow = base + OFF_Q + (2 * (ul & 1) + t) * TILE_BYTES + r_in_tile * 128;
+                float x[64];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + ((c ^ (r_in_tile & 7)) * 16));
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) { x[8 * c + 2 * i] = bf16_lo(ww[i]); x[8 * c + 2 * i + 1] = bf16_hi(ww[i]); }
+                }
+                rope_row64(p.ex.rope, rrow, x);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(qrow + ((c ^ (r_in_tile & 7)) * 16)) =
+                        make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                                   pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            mbar_arrive(bars.q_rot(ul & 1));
+            return true;
+        };
         uint32_t g_it = 0, u_local = 0, slot_base = 0;
         bool ok = true;
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
@@ -404,30 +459,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const int row = (int)(u % p.n_pairs) * 2 * BM + t * BM + r_in_tile;
             const bool valid = row < p.seg_rows;
 
-            if constexpr (kRope) {
-                // rotate this thread's row of the Q tile in shared memory (128-byte swizzle: the
-                // 16-byte chunk c of row r sits at chunk c ^ (r mod 8)), then release it to the MMA
-                if (!warp_wait(bars.q_full(), u_local & 1, abort_flag)) { ok = false; break; }
-                if (valid) {
-                    uint8_t* qrow = base + OFF_Q + t * TILE_BYTES + r_in_tile * 128;
-                    float x[64];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(qrow + ((c ^ (r_in_tile & 7)) * 16));
-                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) { x[8 * c + 2 * i] = bf16_lo(ww[i]); x[8 * c + 2 * i + 1] = bf16_hi(ww[i]); }
-                    }
-                    rope_row64(p.ex.rope, row, x);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(qrow + ((c ^ (r_in_tile & 7)) * 16)) =
-                            make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
-                                       pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                mbar_arrive(bars.q_rot());
-            }
+            if (kRope && u_local == 0 && !rotate_q(u, 0)) { ok = false; break; }
 
             float m = -INFINITY, l = 0.f;
             ExtraRow xr{};
@@ -576,6 +608,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
             if (!ok) break;
             slot_base += 2u * (uint32_t)n_kv;
+            if (kRope && u + gridDim.x < p.n_units && !rotate_q(u + gridDim.x, u_local + 1)) { ok = false; break; }
 
             // epilogue: O from TMEM, extra components, normalisation, store
             if (!warp_wait(bars.o_done(t), u_local & 1, abort_flag)) { ok = false; break; }
