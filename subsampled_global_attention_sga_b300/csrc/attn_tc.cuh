@@ -9,9 +9,10 @@
 // and mean components share the softmax); "RegimeVGGT ...", Key design 2 (ln g logit bias).
 //
 // Work unit: two 128-row query tiles of one segment (a (batch, head) pair, or one frame of it)
-// against all key tiles of that segment.  A unit is a sequence of slots n = 2j + t (query tile t,
-// key tile j); a CTA numbers the slots of its units on from one unit to the next.  Roles (384
-// threads):
+// against all key tiles of that segment; a segment with an odd tile count leaves its last tile to
+// a mixed unit with the next segment's (each tile against its own segment's keys).  A unit is a
+// sequence of slots n = 2j + t (query tile t, key tile j); a CTA numbers the slots of its units
+// on from one unit to the next.  Roles (384 threads):
 //   warp 0      TMA producer: the two Q tiles of a unit (into one of two Q buffers, so the next
 //               unit's are in place before this one ends), then a STAGES-deep ring of K and V
 //               tiles (one barrier pair per stage)
@@ -90,9 +91,11 @@ struct TcArgs {
     int n_seg;              // segments
     int seg_rows;           // query rows per segment
     int kv_rows;            // keys per segment
-    int n_pairs;            // work units per segment (pairs of 128-row query tiles)
+    int n_pairs;            // full pairs of 128-row query tiles per segment (q_tiles / 2)
     int n_kv_tiles;         // ceil(kv_rows / 128)
-    long long n_units;      // n_seg * n_pairs
+    long long n_units;      // n_seg * n_pairs, + ceil(n_seg / 2) mixed units when q_tiles is odd
+    int group;              // with mixed units: units per pair of segments (2 n_pairs + 1); else 0
+    int last_row0;          // first row of a segment's last query tile ((q_tiles - 1) * 128)
     float scale_log2;       // scale * log2(e)
     const __nv_bfloat16* Q; // [n_seg, seg_rows, 64] (rows read for the extra components)
     __nv_bfloat16* O;       // [n_seg, seg_rows, 64]
@@ -107,6 +110,53 @@ struct TcArgs {
 // byte offset of element (row r, column c) in a bias block
 __host__ __device__ constexpr uint32_t ext_off(int r, int c) {
     return (uint32_t)((r >> 3) * 256 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+
+// The query tiles of work unit u.  A full unit holds two consecutive tiles of one segment.  When
+// a segment has an odd number of tiles its last one is left over, and the left-over tiles of
+// segments 2g and 2g + 1 form a mixed unit: each tile of it attends to the keys of its own
+// segment, so no unit computes a tile that lies wholly past the end of its segment.  Units come
+// in groups of 2 n_pairs + 1: the full units of segment 2g, those of segment 2g + 1, then their
+// mixed unit, so that a mixed unit runs while its segments' keys are still in L2.  (With an odd
+// segment count the last group has one segment, and its mixed unit repeats that segment as its
+// second tile, which is then not stored.)
+struct UnitTiles {
+    int seg0, seg1;         // segment of query tile 0, 1
+    int row0, row1;         // first row of query tile 0, 1 within its segment
+    bool mixed;             // tiles of two segments: ring entries (K_0 j, K_1 j), (V_0 j, V_1 j)
+    bool dup1;              // tile 1 repeats tile 0 (odd segment count): not stored
+};
+__device__ __forceinline__ UnitTiles unit_tiles(const TcArgs& p, long long u) {
+    UnitTiles x;
+    int seg, pair = -1;
+    if (p.group == 0) {
+        seg = (int)(u / p.n_pairs);
+        pair = (int)(u % p.n_pairs);
+    } else {
+        const int g = (int)(u / p.group), r = (int)(u % p.group);
+        const bool last_single = 2 * g + 1 >= p.n_seg;          // the odd segment count's last group
+        seg = 2 * g;
+        if (r < p.n_pairs) pair = r;
+        else if (!last_single && r < 2 * p.n_pairs) { seg = 2 * g + 1; pair = r - p.n_pairs; }
+    }
+    x.mixed = pair < 0;
+    if (!x.mixed) {
+        x.seg0 = x.seg1 = seg;
+        x.row0 = pair * 2 * BM;
+        x.row1 = x.row0 + BM;
+        x.dup1 = false;
+    } else {
+        x.seg0 = seg;
+        x.dup1 = seg + 1 >= p.n_seg;
+        x.seg1 = x.dup1 ? seg : seg + 1;
+        x.row0 = x.row1 = p.last_row0;
+    }
+    return x;
+}
+__device__ __forceinline__ bool unit_mixed(const TcArgs& p, long long u) {
+    if (p.group == 0) return false;
+    const int g = (int)(u / p.group), r = (int)(u % p.group);
+    return r == (2 * g + 1 >= p.n_seg ? p.n_pairs : 2 * p.n_pairs);
 }
 
 // mbarrier addresses (computed, so that no dynamically indexed array lands in local memory)
@@ -237,21 +287,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         uint32_t kv_it = 0, kv_issued = 0, q_issued = 0, u_local = 0;
         bool ok = true;
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-            const int seg = (int)(u / p.n_pairs);
-            const int row0 = (int)(u % p.n_pairs) * 2 * BM;
+            const UnitTiles ut = unit_tiles(p, u);
             const uint32_t qb = u_local & 1;
             if (!warp_wait(bars.q_empty(qb), ((u_local >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
             if (elect_one()) {
                 const uint32_t dst = sbase + OFF_Q + qb * 2 * TILE_BYTES;
                 mbar_arrive_expect_tx(bars.q_full(qb), 2 * TILE_BYTES);
-                tma_load_3d(dst, &tmQ, bars.q_full(qb), 0, row0, seg);
-                tma_load_3d(dst + TILE_BYTES, &tmQ, bars.q_full(qb), 0, row0 + BM, seg);
+                tma_load_3d(dst, &tmQ, bars.q_full(qb), 0, ut.row0, ut.seg0);
+                tma_load_3d(dst + TILE_BYTES, &tmQ, bars.q_full(qb), 0, ut.row1, ut.seg1);
             }
             __syncwarp();
             ++q_issued;
-            for (int j = 0; j < n_kv; ++j, ++kv_it) {
+            // ring entries: (K j, V j) of the segment (full unit); in a mixed unit (K j of
+            // segment 0, K j of segment 1), then (V j of segment 0, V j of segment 1), so that a
+            // K entry is released as soon as its two QKs are done (the bias variant has no
+            // mixed units)
+            const int n_ent = ut.mixed ? 2 * n_kv : n_kv;
+            for (int i = 0; i < n_ent; ++i, ++kv_it) {
                 const int st = kv_it % STAGES;
                 const uint32_t ph = (kv_it / STAGES) & 1;
+                const int j = ut.mixed ? (i >> 1) : i;
+                const int seg = ut.seg0;
                 const int jt = key_tile(j, n_kv, u_local);
                 if (!warp_wait(bars.kv_empty(st), ph ^ 1, abort_flag)) { ok = false; break; }
                 if (kBias) {
@@ -274,13 +330,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 // tile drop_kv, so that barrier never completes
                 if ((long long)kv_it != p.drop_kv) {
                     if (elect_one()) {
+                        const CUtensorMap* m0 = (ut.mixed && (i & 1)) ? &tmV : &tmK;
+                        const CUtensorMap* m1 = ut.mixed ? m0 : &tmV;
                         mbar_arrive_expect_tx(bars.kv_full(st), 2 * TILE_BYTES);
-                        tma_load_3d(sbase + OFF_K + st * TILE_BYTES, &tmK, bars.kv_full(st), 0, jt * BN, seg);
-                        tma_load_3d(sbase + OFF_V + st * TILE_BYTES, &tmV, bars.kv_full(st), 0, jt * BN, seg);
+                        tma_load_3d(sbase + OFF_K + st * TILE_BYTES, m0, bars.kv_full(st), 0, jt * BN, seg);
+                        tma_load_3d(sbase + OFF_V + st * TILE_BYTES, m1, bars.kv_full(st), 0, jt * BN, ut.seg1);
                     }
                     __syncwarp();
                 }
-                kv_issued = kv_it + 1;               // key tiles [0, kv_issued) are issued (but drop_kv)
+                kv_issued = kv_it + 1;               // entries [0, kv_issued) are issued (but drop_kv)
             }
         }
         if (!ok) {
@@ -293,14 +351,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       } else if (warp <= 2) {
         // ------------------------------------------------------------------ MMA issuers
         // Slots: the n-th (query tile, key tile) pair of a unit is slot n = 2j + t; the CTA's
-        // slots are numbered on across its units (global slot s = u_local * 2 n_kv + n, key ring
-        // entry s / 2).  Slot s's S goes to buffer s mod 3 and its P is written over it.  Batch G_s
-        // (issued by issuer s mod 2 once P(s) is ready) holds PV(s), then QK(s + 3), whose buffer
-        // is the one PV(s) has just read; QK(s + 3) may belong to the next unit (its Q tiles sit
-        // in the other Q buffer), so the tensor pipe runs on across unit boundaries and every
-        // softmax warp finds its next S computed.  The issuers take turns (token through the turn
-        // barriers) so the batches reach the tensor pipe in slot order; issuer 0 opens with the
-        // first three QKs.
+        // slots are numbered on across its units (global slot s = u_local * 2 n_kv + n).  Slot s's
+        // S goes to buffer s mod 3 and its P is written over it.  Batch G_s (issued by issuer
+        // s mod 2 once P(s) is ready) holds PV(s), then QK(s + 3), whose buffer is the one PV(s)
+        // has just read; QK(s + 3) may belong to the next unit (its Q tiles sit in the other Q
+        // buffer), so the tensor pipe runs on across unit boundaries and every softmax warp finds
+        // its next S computed.  The issuers take turns (token through the turn barriers) so the
+        // batches reach the tensor pipe in slot order; issuer 0 opens with the first three QKs.
         const int t = warp - 1;
         const uint64_t dQ = smem_desc_sw128(sbase + OFF_Q, 16);
         const uint64_t dK = smem_desc_sw128(sbase + OFF_K, 16);
@@ -309,37 +366,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const uint64_t dKe = smem_desc_noswz(sbase + OFF_KEXT, 128, 256);
         constexpr uint64_t kTileStep = TILE_BYTES >> 4;
         constexpr uint64_t kExtStep = EXT_BYTES >> 4;
+        // in a mixed unit, tile 1's K sits in the V half of the stage and tile 0's V in the K half
+        constexpr uint64_t kHalfStep = (uint64_t)(STAGES * TILE_BYTES) >> 4;
         const uint32_t to = tmem + col_o(t);
         const uint32_t n_slots = 2u * (uint32_t)n_kv;
         const uint32_t my_units = (uint32_t)((p.n_units - 1 - blockIdx.x) / gridDim.x + 1);   // grid <= n_units
         const uint32_t total = my_units * n_slots;
+        // A position in the CTA's slot sequence: unit ul (the CTA's ul-th), slot n in it, and the
+        // unit's first key ring entry (a full unit takes n_kv entries, a mixed one 2 n_kv).
+        struct Cursor { uint32_t ul, n, ebase; bool mixed; };
+        auto next_unit = [&](Cursor& c) {
+            c.n -= n_slots;
+            c.ebase += (c.mixed ? 2u : 1u) * (uint32_t)n_kv;
+            ++c.ul;
+            c.mixed = unit_mixed(p, blockIdx.x + (long long)c.ul * gridDim.x);
+        };
+        auto cursor_at = [&](uint32_t n0) -> Cursor {
+            Cursor c{0u, n0, 0u, unit_mixed(p, blockIdx.x)};
+            while (c.n >= n_slots) next_unit(c);
+            return c;
+        };
+        // ring entry read by QK (kv = 0) or PV (kv = 1) of slot c
+        auto entry = [&](const Cursor& c, uint32_t kv) -> uint32_t {
+            return c.ebase + (c.mixed ? (c.n & ~1u) + kv : c.n >> 1);
+        };
         uint32_t turns = 0;
         bool ok = true;
-        // waits (whole warp) for what QK of slot (unit ul, n) reads: its key tile and the unit's Q
-        // (each issuer waits on the Q barrier itself: slots 0-2 of a unit alternate issuers)
-        auto qk_ready = [&](uint32_t ul, uint32_t n) -> bool {
-            const uint32_t e = ul * (uint32_t)n_kv + (n >> 1);
-            if (!warp_wait(bars.kv_full((int)(e % STAGES)), (e / STAGES) & 1, abort_flag)) return false;
-            if (n < 3 && !warp_wait(kRope ? bars.q_rot(ul & 1) : bars.q_full(ul & 1), (ul >> 1) & 1, abort_flag))
-                return false;
-            return true;
-        };
-        auto issue_qk = [&](uint32_t s, uint32_t ul, uint32_t n) {
-            const uint32_t e = ul * (uint32_t)n_kv + (n >> 1);
-            const int st = (int)(e % STAGES);
+        auto issue_qk = [&](uint32_t s, const Cursor& c) {
+            const int st = (int)(entry(c, 0) % STAGES);
             const uint32_t ts = tmem + col_buf(s % NUM_SBUF);
-            const uint64_t dq = dQ + (uint64_t)(2 * (ul & 1) + (n & 1)) * kTileStep;
-            const uint64_t dk = dK + (uint64_t)st * kTileStep;
+            const uint64_t dq = dQ + (uint64_t)(2 * (c.ul & 1) + (c.n & 1)) * kTileStep;
+            const uint64_t dk = dK + (uint64_t)st * kTileStep + ((c.mixed && (c.n & 1)) ? kHalfStep : 0ull);
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
                 mma_ss(ts, dq + 2 * kk, dk + 2 * kk, IDESC_QK, kk > 0 ? 1u : 0u);
             if (kBias) mma_ss(ts, dQe, dKe + (uint64_t)st * kExtStep, IDESC_QK, 1u);
             mma_commit(bars.s_full(s % NUM_SBUF));
-            if (n + 2 >= n_slots) mma_commit(bars.q_empty(ul & 1));   // the unit's last two QKs
+            if (c.n + 2 >= n_slots) mma_commit(bars.q_empty(c.ul & 1));   // the unit's last two QKs
         };
-        auto issue_pv = [&](uint32_t s, int st, uint32_t acc) {
+        auto issue_pv = [&](uint32_t s, int st, bool v_low, uint32_t acc) {
             const uint32_t tp = tmem + col_buf(s % NUM_SBUF);
-            const uint64_t dv = dV + (uint64_t)st * kTileStep;
+            const uint64_t dv = dV + (uint64_t)st * kTileStep - (v_low ? kHalfStep : 0ull);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
                 mma_ts(to, tp + 8 * kk, dv + 128 * kk, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
@@ -354,61 +421,73 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             __syncwarp();
         };
         if (t == 0) {
-            // the first three S: slots 0, 1 (key tile 0) and 2 (key tile 1, or the next unit)
-            uint32_t ul = 0, n = 0;
+            // the first three S: slots 0, 1 (key tile 0) and 2 (key tile 1, or the next unit).
+            // Each issuer waits on a unit's Q barrier itself (slots 0-2 alternate issuers).
+            Cursor c = cursor_at(0);
             for (uint32_t s = 0; s < 3 && s < total && ok; ++s) {
-                if (!qk_ready(ul, n)) { ok = false; break; }
+                const uint32_t e = entry(c, 0);
+                if (!warp_wait(bars.kv_full((int)(e % STAGES)), (e / STAGES) & 1, abort_flag) ||
+                    !warp_wait(kRope ? bars.q_rot(c.ul & 1) : bars.q_full(c.ul & 1), (c.ul >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                if (elect_one()) issue_qk(s, ul, n);
+                if (elect_one()) {
+                    issue_qk(s, c);
+                    if (c.mixed) mma_commit(bars.kv_empty((int)(e % STAGES)));   // a mixed unit's K entry
+                }
                 __syncwarp();
-                if (++n == n_slots) { n = 0; ++ul; }
+                if (++c.n == n_slots) next_unit(c);
             }
         }
-        // batch G_s: slot s = (unit ul, n); QK(s + 3) = (unit ulm, nm).  Everything the batch
-        // waits for is waited for before the turn is taken, so the turn is held only to issue;
-        // the one exception is a RoPE unit's rotated Q (see below).
-        uint32_t ul = 0, n = (uint32_t)t;
-        uint32_t ulm = 0, nm = (uint32_t)t + 3;
-        while (nm >= n_slots) { nm -= n_slots; ++ulm; }
+        // batch G_s: PV of slot cp, QK of slot cq (three slots on).  Everything the batch waits
+        // for is waited for before the turn is taken, so the turn is held only to issue; the one
+        // exception is a RoPE unit's rotated Q (see below).
+        Cursor cp = cursor_at((uint32_t)t);
+        Cursor cq = cursor_at((uint32_t)t + 3);
         for (uint32_t s = (uint32_t)t; s < total && ok; s += 2) {
-            const uint32_t j = n >> 1;
-            const int st = (int)((s >> 1) % STAGES);
+            const uint32_t j = cp.n >> 1;
+            const int st = (int)(entry(cp, 1) % STAGES);
             const bool has_qk = s + 3 < total;
             // with RoPE the next unit's Q is rotated by the softmax warps once they are through
             // this unit's tiles, and one of them may still wait for PV(s): that QK waits for the
             // rotation after PV(s) has been issued
-            const bool late_q = kRope && has_qk && nm < 3;
+            const bool late_q = kRope && has_qk && cq.n < 3;
+            const uint32_t eq = entry(cq, 0);
             if (has_qk) {
-                const uint32_t e = ulm * (uint32_t)n_kv + (nm >> 1);
-                if (!warp_wait(bars.kv_full((int)(e % STAGES)), (e / STAGES) & 1, abort_flag)) { ok = false; break; }
-                if (!kRope && nm < 3 && !warp_wait(bars.q_full(ulm & 1), (ulm >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.kv_full((int)(eq % STAGES)), (eq / STAGES) & 1, abort_flag)) { ok = false; break; }
+                if (!kRope && cq.n < 3 && !warp_wait(bars.q_full(cq.ul & 1), (cq.ul >> 1) & 1, abort_flag)) { ok = false; break; }
             }
+            // a mixed unit's V has a ring entry of its own (a full unit's V came with its K)
+            if (cp.mixed && !warp_wait(bars.kv_full(st), (entry(cp, 1) / STAGES) & 1, abort_flag)) { ok = false; break; }
             if (!warp_wait(bars.p_ready(s % NUM_SBUF), (s / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
-            if (n < 2 && !warp_wait(bars.o_free(t), (ul & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (cp.n < 2 && !warp_wait(bars.o_free(t), (cp.ul & 1) ^ 1, abort_flag)) { ok = false; break; }
             if (!take_turn()) { ok = false; break; }
             tc_fence_after();
             if (elect_one()) {
-                issue_pv(s, st, j > 0 ? 1u : 0u);
-                if (n + 2 >= n_slots) mma_commit(bars.o_done(t));
-                if (has_qk && !late_q) issue_qk(s + 3, ulm, nm);
+                issue_pv(s, st, cp.mixed && (cp.n & 1) == 0, j > 0 ? 1u : 0u);
+                if (cp.n + 2 >= n_slots) mma_commit(bars.o_done(t));
+                if (has_qk && !late_q) issue_qk(s + 3, cq);
             }
             __syncwarp();
             if (late_q) {
-                if (!warp_wait(bars.q_rot(ulm & 1), (ulm >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.q_rot(cq.ul & 1), (cq.ul >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                if (elect_one()) issue_qk(s + 3, ulm, nm);
+                if (elect_one()) issue_qk(s + 3, cq);
                 __syncwarp();
             }
             pass_turn();
             if (elect_one()) {
                 mma_commit(bars.pv_done(t));
                 mma_commit(bars.kv_empty(st));                  // this issuer's last use of the stage
+                // a mixed unit's K entry is released by its two QKs
+                if (has_qk && cq.mixed) mma_commit(bars.kv_empty((int)(eq % STAGES)));
             }
             __syncwarp();
-            n += 2;
-            if (n >= n_slots) { n -= n_slots; ++ul; }
-            nm += 2;
-            while (nm >= n_slots) { nm -= n_slots; ++ulm; }
+            cp.n += 2;
+            if (cp.n >= n_slots) next_unit(cp);
+            cq.n += 2;
+            if (cq.n >= n_slots) next_unit(cq);
         }
         // every MMA issued so far completes before TMEM is released
         if (elect_one()) mma_commit(bars.drain());
@@ -430,7 +509,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         // as soon as this warpgroup is through the tiles of the unit before it.
         auto rotate_q = [&](long long uu, uint32_t ul) -> bool {
             if (!warp_wait(bars.q_full(ul & 1), (ul >> 1) & 1, abort_flag)) return false;
-            const int rrow = (int)(uu % p.n_pairs) * 2 * BM + t * BM + r_in_tile;
+            const UnitTiles un = unit_tiles(p, uu);
+            const int rrow = (t ? un.row1 : un.row0) + r_in_tile;
             if (rrow < p.seg_rows) {
                 uint8_t* qrow = base + OFF_Q + (2 * (ul & 1) + t) * TILE_BYTES + r_in_tile * 128;
                 float x[64];
@@ -455,9 +535,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         uint32_t g_it = 0, u_local = 0, slot_base = 0;
         bool ok = true;
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
-            const int seg = (int)(u / p.n_pairs);
-            const int row = (int)(u % p.n_pairs) * 2 * BM + t * BM + r_in_tile;
-            const bool valid = row < p.seg_rows;
+            const UnitTiles ut = unit_tiles(p, u);
+            const int seg = t ? ut.seg1 : ut.seg0;
+            const int row = (t ? ut.row1 : ut.row0) + r_in_tile;
+            const bool valid = row < p.seg_rows && !(t == 1 && ut.dup1);
 
             if (kRope && u_local == 0 && !rotate_q(u, 0)) { ok = false; break; }
 

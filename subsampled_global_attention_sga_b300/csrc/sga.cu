@@ -174,9 +174,14 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.seg_rows = (int)pb.seg_rows;
         a.kv_rows = (int)pb.kv_rows;
         const long long q_tiles = (pb.seg_rows + T::BM - 1) / T::BM;
-        a.n_pairs = (int)((q_tiles + 1) / 2);
+        // a segment's left-over query tile (odd tile count) goes into a mixed unit with the next
+        // segment's; the bias variant keeps it in a unit of its own (its second tile unused)
+        const bool mixed = (q_tiles & 1) && !pb.bias;
+        a.n_pairs = (int)(mixed ? q_tiles / 2 : (q_tiles + 1) / 2);
         a.n_kv_tiles = (int)((pb.kv_rows + T::BN - 1) / T::BN);
-        a.n_units = (long long)a.n_seg * a.n_pairs;
+        a.n_units = (long long)a.n_seg * a.n_pairs + (mixed ? (a.n_seg + 1) / 2 : 0);
+        a.group = mixed ? 2 * a.n_pairs + 1 : 0;
+        a.last_row0 = (int)((q_tiles - 1) * T::BM);
         a.scale_log2 = scale_log2;
         a.Q = reinterpret_cast<const __nv_bfloat16*>(pb.Q);
         a.O = reinterpret_cast<__nv_bfloat16*>(pb.O);
