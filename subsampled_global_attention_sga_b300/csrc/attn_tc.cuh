@@ -82,7 +82,11 @@ constexpr int OFF_BAR = OFF_KEXT + STAGES * EXT_BYTES;
 //           o_free[2], drain, q_rot[2], pv_done[2], turn[2]
 constexpr int NUM_BARS = 4 + 2 * STAGES + 6 + 4 + 1 + 2 + 2 + 2;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+// a softmax thread's row state while its unit waits for the epilogue: 8 words per thread, stored
+// word-major ([word][thread]) so that a warp's accesses fall in distinct banks
+constexpr int OFF_PEND = OFF_MISC + 16;
+constexpr int PEND_WORDS = 8;
+constexpr int SMEM_BYTES = OFF_PEND + PEND_WORDS * 256 * 4 + 1024;   // + alignment slack
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, true);
@@ -532,15 +536,58 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_arrive(bars.q_rot(ul & 1));
             return true;
         };
+        // A unit's epilogue runs once this warpgroup has stored the next unit's first P: by then
+        // the unit's last PV is long complete.  Its row state waits in shared memory.
+        float* pend = reinterpret_cast<float*>(base + OFF_PEND) + (threadIdx.x - 128);
+        auto epilogue = [&](uint32_t ul) -> bool {
+            if (!warp_wait(bars.o_done(t), ul & 1, abort_flag)) return false;
+            tc_fence_after();
+            float o[64];
+            {
+                uint32_t r[32];
+                tmem_ld32(tO, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+                tmem_ld32(tO + 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[32 + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(bars.o_free(t));
+            const int seg = __float_as_int(pend[6 * 256]);
+            const int row = __float_as_int(pend[7 * 256]);
+            if (seg >= 0 && SGA_CHECK_INDEX((long long)seg * p.seg_rows + row, (long long)p.n_seg * p.seg_rows, 10)) {
+                const float m = pend[0], l = pend[256];
+                if (p.ex.on) {
+                    const ExtraRow xr{pend[2 * 256], pend[3 * 256], __float_as_int(pend[4 * 256]), pend[5 * 256]};
+                    extra_values<__nv_bfloat16, 64>(p.ex, seg, row, xr, m, 0, o);
+                }
+                const float inv_l = 1.0f / l;
+                const long long grow = (long long)seg * p.seg_rows + row;
+                uint4* dst = reinterpret_cast<uint4*>(p.O + grow * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16x2(o[8 * c + 0] * inv_l, o[8 * c + 1] * inv_l);
+                    w.y = pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l);
+                    w.z = pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l);
+                    w.w = pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l);
+                    dst[c] = w;
+                }
+                if (p.lse) p.lse[grow] = (m + log2f(l)) * 0.69314718055994531f;
+            }
+            return true;
+        };
         uint32_t g_it = 0, u_local = 0, slot_base = 0;
         bool ok = true;
+        if (kRope && !rotate_q(blockIdx.x, 0)) ok = false;
         for (long long u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++u_local) {
             const UnitTiles ut = unit_tiles(p, u);
             const int seg = t ? ut.seg1 : ut.seg0;
             const int row = (t ? ut.row1 : ut.row0) + r_in_tile;
             const bool valid = row < p.seg_rows && !(t == 1 && ut.dup1);
-
-            if (kRope && u_local == 0 && !rotate_q(u, 0)) { ok = false; break; }
 
             float m = -INFINITY, l = 0.f;
             ExtraRow xr{};
@@ -554,41 +601,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     l = (xr.s_diag == -INFINITY ? 0.f : exp2f(xr.s_diag - m)) +
                         (xr.s_mean == -INFINITY ? 0.f : exp2f(xr.s_mean - m));
             }
-
             // A row without the extra components has no reference max yet: the unit's first key
-            // tile sets it to that tile's row maximum (as a max-first softmax would), so the loop
-            // can exponentiate against it at once.  This reads S before any P is written over it.
-            if (__any_sync(0xffffffffu, m == -INFINITY)) {
-                const uint32_t sn0 = slot_base + (uint32_t)t;
-                const uint32_t tS0 = tmem + lane_bits + col_buf(sn0 % NUM_SBUF);
-                if (!warp_wait(bars.s_full(sn0 % NUM_SBUF), (sn0 / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                float s[128];
-                ld_row128(tS0, s);
-                tmem_wait_ld();
-                if (key_tile(0, n_kv, u_local) == n_kv - 1 && last_valid < BN) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (c >= last_valid) s[c] = -INFINITY;
-                }
-                float mx8[8];
-#pragma unroll
-                for (int gg = 0; gg < 8; ++gg) {
-                    float a = max3f(s[16 * gg], s[16 * gg + 1], s[16 * gg + 2]);
-#pragma unroll
-                    for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * gg + c], s[16 * gg + c + 1]);
-                    mx8[gg] = fmaxf(a, s[16 * gg + 15]);
-                }
-                const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
-                                       max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-                if (m == -INFINITY) m = mx * sl2;
-            }
+            // tile sets it to that tile's row maximum (as a max-first softmax would).
+            const bool need_init = __any_sync(0xffffffffu, m == -INFINITY);
 
-            for (int j = 0; j < n_kv; ++j, ++g_it) {
+            // one key tile of this unit (the first one also sets the reference max where there is
+            // none yet, and runs the previous unit's epilogue)
+            auto tile = [&](int j, bool first) -> bool {
                 // this slot's S, and then its P, live in buffer (global slot) mod 3
                 const uint32_t sn = slot_base + 2u * (uint32_t)j + (uint32_t)t;    // global slot
                 const uint32_t tS = tmem + lane_bits + col_buf(sn % NUM_SBUF);
-                if (!warp_wait(bars.s_full(sn % NUM_SBUF), (sn / NUM_SBUF) & 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(bars.s_full(sn % NUM_SBUF), (sn / NUM_SBUF) & 1, abort_flag)) return false;
                 tc_fence_after();
                 float s[128];
                 ld_row128(tS, s);
@@ -597,6 +620,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (c >= last_valid) s[c] = -INFINITY;
+                }
+                if (first && need_init) {
+                    float mx8[8];
+#pragma unroll
+                    for (int gg = 0; gg < 8; ++gg) {
+                        float a = max3f(s[16 * gg], s[16 * gg + 1], s[16 * gg + 2]);
+#pragma unroll
+                        for (int c = 3; c < 15; c += 2) a = max3f(a, s[16 * gg + c], s[16 * gg + c + 1]);
+                        mx8[gg] = fmaxf(a, s[16 * gg + 15]);
+                    }
+                    const float mx = fmaxf(max3f(mx8[0], mx8[1], mx8[2]),
+                                           max3f(max3f(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                    if (m == -INFINITY) m = mx * sl2;
                 }
                 // p = 2^(s * scale_log2 - m) against the row's current reference max m (the whole
                 // row of S is in registers, so P can go over it at once); the tile sum decides
@@ -668,7 +704,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), a0, a1);
                         tsum = a0 + a1;
                         if (j > 0) {
-                            if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) { ok = false; break; }
+                            if (!warp_wait(bars.pv_done(t), (g_it - 1) & 1, abort_flag)) return false;
                             tc_fence_after();
                             uint32_t r[32];
 #pragma unroll
@@ -686,45 +722,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bars.p_ready(sn % NUM_SBUF));
-            }
+                // the previous unit's epilogue, now that this unit's first P is out
+                if (first && u_local > 0 && !epilogue(u_local - 1)) return false;
+                return true;
+            };
+            if (!tile(0, true)) { ok = false; break; }
+            ++g_it;
+            for (int j = 1; j < n_kv; ++j, ++g_it)
+                if (!tile(j, false)) { ok = false; break; }
             if (!ok) break;
             slot_base += 2u * (uint32_t)n_kv;
             if (kRope && u + gridDim.x < p.n_units && !rotate_q(u + gridDim.x, u_local + 1)) { ok = false; break; }
-
-            // epilogue: O from TMEM, extra components, normalisation, store
-            if (!warp_wait(bars.o_done(t), u_local & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            float o[64];
-            {
-                uint32_t r[32];
-                tmem_ld32(tO, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
-                tmem_ld32(tO + 32, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[32 + i] = __uint_as_float(r[i]);
-            }
-            tc_fence_before();
-            mbar_arrive(bars.o_free(t));
-            if (valid && SGA_CHECK_INDEX((long long)seg * p.seg_rows + row, (long long)p.n_seg * p.seg_rows, 10)) {
-                if (p.ex.on) extra_values<__nv_bfloat16, 64>(p.ex, seg, row, xr, m, 0, o);
-                const float inv_l = 1.0f / l;
-                const long long grow = (long long)seg * p.seg_rows + row;
-                uint4* dst = reinterpret_cast<uint4*>(p.O + grow * 64);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 w;
-                    w.x = pack_bf16x2(o[8 * c + 0] * inv_l, o[8 * c + 1] * inv_l);
-                    w.y = pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l);
-                    w.z = pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l);
-                    w.w = pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l);
-                    dst[c] = w;
-                }
-                if (p.lse) p.lse[grow] = (m + log2f(l)) * 0.69314718055994531f;
-            }
+            pend[0] = m;
+            pend[256] = l;
+            pend[2 * 256] = xr.s_diag;
+            pend[3 * 256] = xr.s_mean;
+            pend[4 * 256] = __int_as_float(xr.loo);
+            pend[5 * 256] = xr.inv_c;
+            pend[6 * 256] = __int_as_float(valid ? seg : -1);
+            pend[7 * 256] = __int_as_float(row);
         }
+        if (ok && u_local > 0) epilogue(u_local - 1);
     }
 
     // ---------------------------------------------------------------------- teardown
