@@ -357,7 +357,7 @@ sga_status sga_selftest_timeout(void* stream);
  * check every indexed store of the compaction, attention, merge and unmerge kernels, and the
  * index reads that steer them, against the buffer's bound; a failed check skips the access,
  * sets the device status word to SGA_ERR_DEBUG_CHECK and records the first failure.  This call
- * copies that record to the host and clears it: `site` (the check that failed: 1-2 compaction,
+ * copies that record to the host and clears it: `site` (the check that failed: 1-3 compaction,
  * 10-12 attention, 20-23 merging), the offending `index`, its `bound`, and `count`, the number of
  * failed checks.  Any output pointer may be NULL.  Synchronous.  A normal build returns
  * SGA_ERR_UNSUPPORTED. */

@@ -10,7 +10,8 @@
 // whose dims rotate together); several rows per lane are in flight.  Kept rows go to the slot the
 // plan assigned; dropped rows are accumulated in fp32 registers.  The per-block partial sums go
 // to a scratch buffer and a second kernel adds them in a fixed order, so the result does not
-// depend on scheduling.
+// depend on scheduling.  (bf16 with the rotation runs the TMA-fed kernel of compact_rope.cuh;
+// this kernel's rotating instance serves fp32.)
 #pragma once
 
 #include "rope.cuh"
@@ -18,6 +19,9 @@
 namespace sga {
 
 constexpr int kCompactThreads = 256;
+// (cos, sin) table rows in shared memory padded from 16 to 18 entries (144 bytes): the rows of
+// the 8 tokens a warp rotates at once start 4 banks apart, and a row stays 16-byte aligned
+constexpr int kRopeTabStride = 18;
 constexpr int kCompactUnroll = 4;
 
 struct CompactArgs {
@@ -98,10 +102,21 @@ __global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel
     if constexpr (kRope) {
         // rotated keys: the (cos, sin) table in shared memory
         extern __shared__ float2 rope_s[];
-        for (int i = threadIdx.x; i < a.rope.P * 16; i += kCompactThreads) rope_s[i] = a.rope.tab[i];
+        for (int i = threadIdx.x; i < a.rope.P * 16; i += kCompactThreads)
+            rope_s[(i >> 4) * kRopeTabStride + (i & 15)] = a.rope.tab[i];
         __syncthreads();
         using VT = Vec16<T>;
         const int d0 = va * kElemsPerVec;                         // first dim of vector va
+        // token position within its frame, per row in flight, stepped along with the rows (no
+        // division per row); the grid row of a patch from a float quotient that is exact for the
+        // frame sizes the plan allows (q < 2^21)
+        constexpr int kStep = kRowsPerPass * kUnroll;
+        const int L = a.rope.L, ns = a.rope.n_special, gw = a.rope.grid_w, off = a.rope.pos_offset;
+        const int step_mod = kStep % L;
+        const float inv_gw = 1.0f / (float)gw;
+        int pu[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) pu[u] = (int)((r_begin + (long long)u * kRowsPerPass + rsub) % L);
         for (long long r0 = r_begin; r0 < r_end; r0 += (long long)kRowsPerPass * kUnroll) {
             uint4 ka[kUnroll], kb[kUnroll], wa[kUnroll], wb[kUnroll];
             int sl[kUnroll];
@@ -120,10 +135,14 @@ __global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 if (sl[u] == -2) continue;
-                const long long t = r0 + (long long)u * kRowsPerPass + rsub;
-                int pr, pc;
-                rope_pos(a.rope, t, pr, pc);
-                const float2* tb = rope_s + ((d0 & 32) ? pc : pr) * 16 + (d0 & 15);
+                int pr = 0, pc = 0;
+                if (pu[u] >= ns) {
+                    const int q = pu[u] - ns;
+                    const int qr = (int)(((float)q + 0.5f) * inv_gw);
+                    pr = qr + off;
+                    pc = q - qr * gw + off;
+                }
+                const float2* tb = rope_s + ((d0 & 32) ? pc : pr) * kRopeTabStride + (d0 & 15);
                 float x0[kElemsPerVec], x1[kElemsPerVec];
                 VT::unpack(ka[u], x0);
                 VT::unpack(kb[u], x1);
@@ -155,6 +174,11 @@ __global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel
                         vs[kElemsPerVec + e] += v1[e];
                     }
                 }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                pu[u] += step_mod;
+                if (pu[u] >= L) pu[u] -= L;
             }
         }
     } else {

@@ -12,6 +12,7 @@
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
 #include "compact.cuh"
+#include "compact_rope.cuh"
 #include "compact_noalloc.cuh"
 #include "merge.cuh"
 #include "rope.cuh"
@@ -20,12 +21,16 @@ namespace {
 
 constexpr uint32_t kPlanMagic = 0x53474150u;   // "SGAP"
 constexpr int kCompactRowsPerChunk = 2048;
+// bf16 with the rotation: work items of the persistent TMA-fed kernel (2 CTAs per SM), short
+// enough that the items spread evenly over the CTAs (a multiple of its 64-row stage)
+constexpr int kCompactRowsPerChunkRope = 1024;
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     bool init = false;
     int sm_count = 0;
     bool tc_ready[2][2] = {};                                  // attn_tc_kernel<bias, rope> ready
+    size_t cr_smem = 0;                                        // compact_rope_kernel: smem enabled
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -37,8 +42,9 @@ struct sga_plan_s {
     sga_config cfg;
     int device;
     long long L, T, S, D;
+    int rows_per_chunk;     // compaction rows per block (work item of the RoPE kernel)
     int n_chunks;
-    int32_t* d_slot;        // [T]
+    int32_t* d_slot;        // [T], padded with -1 to a multiple of 64 entries (whole 256-byte copies)
     int32_t* d_kv_index;    // [S]
     int32_t* d_frame_off;   // [N+1]
     float* d_partials;      // [B*H, n_chunks, 128]
@@ -85,13 +91,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 3-D map over a contiguous [n_seg, rows, 64] bf16 tensor, box = 128 rows x 64 columns,
 // 128-byte swizzle (rows are exactly 128 bytes), zero fill outside [0, rows).
-sga_status make_map(CUtensorMap* map, const void* ptr, long long rows, long long n_seg) {
+sga_status make_map(CUtensorMap* map, const void* ptr, long long rows, long long n_seg, int box_rows = 128) {
     auto fn = encode_fn();
     if (!fn) return SGA_ERR_CUDA;
     if (rows <= 0 || n_seg <= 0 || rows > 0x7FFFFFFFLL || n_seg > 0x7FFFFFFFLL) return SGA_ERR_UNSUPPORTED;
     cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)n_seg};
     cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -375,7 +381,8 @@ sga_status upload_plan(const sga_config& c, const std::vector<int32_t>& slot, co
     plan->T = T;
     plan->S = (long long)kv.size();
     plan->D = T - plan->S;
-    plan->n_chunks = (int)((T + kCompactRowsPerChunk - 1) / kCompactRowsPerChunk);
+    plan->rows_per_chunk = (c.rope && c.dtype == SGA_BF16) ? kCompactRowsPerChunkRope : kCompactRowsPerChunk;
+    plan->n_chunks = (int)((T + plan->rows_per_chunk - 1) / plan->rows_per_chunk);
     plan->h_kv_index = kv;
     plan->h_frame_off = off;
     plan->d_slot = nullptr;
@@ -404,7 +411,9 @@ sga_status upload_plan(const sga_config& c, const std::vector<int32_t>& slot, co
     }
     bool okc = true;
     const size_t part_bytes = (size_t)c.B * c.H * plan->n_chunks * 128 * sizeof(float);
-    okc = okc && cudaMalloc(&plan->d_slot, sizeof(int32_t) * (size_t)T) == cudaSuccess;
+    const size_t slot_n = (size_t)((T + 63) / 64) * 64;
+    okc = okc && cudaMalloc(&plan->d_slot, sizeof(int32_t) * slot_n) == cudaSuccess;
+    okc = okc && cudaMemset(plan->d_slot, 0xFF, sizeof(int32_t) * slot_n) == cudaSuccess;
     okc = okc && cudaMalloc(&plan->d_kv_index, sizeof(int32_t) * (size_t)(plan->S > 0 ? plan->S : 1)) == cudaSuccess;
     okc = okc && cudaMalloc(&plan->d_frame_off, sizeof(int32_t) * (size_t)(c.N + 1)) == cudaSuccess;
     okc = okc && cudaMalloc(&plan->d_partials, part_bytes) == cudaSuccess;
@@ -603,7 +612,7 @@ sga_status sga_compact(sga_plan_t plan, const void* K, const void* V, void* K_S,
     sga::CompactArgs a;
     a.T = plan->T;
     a.S = plan->S;
-    a.rows_per_chunk = kCompactRowsPerChunk;
+    a.rows_per_chunk = plan->rows_per_chunk;
     a.n_chunks = plan->n_chunks;
     a.slot = plan->d_slot;
     a.K = K;
@@ -614,14 +623,47 @@ sga_status sga_compact(sga_plan_t plan, const void* K, const void* V, void* K_S,
     a.rope = rope_args(plan);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     dim3 grid((unsigned)plan->n_chunks, (unsigned)BH);
-    const size_t rope_smem = c.rope ? sizeof(float2) * (size_t)plan->rope_P * 16 : 0;
-    if (rope_smem > 48 * 1024) return SGA_ERR_UNSUPPORTED;
+    const size_t rope_smem = c.rope ? sizeof(float2) * (size_t)plan->rope_P * sga::kRopeTabStride : 0;
     if (c.dtype == SGA_BF16) {
-        if (c.rope)
-            sga::compact_kernel<__nv_bfloat16, true><<<grid, sga::kCompactThreads, rope_smem, s>>>(a);
-        else
+        if (c.rope) {
+            // persistent TMA-fed kernel: the rotation needs the loads decoupled from the compute
+            namespace R = sga::cr;
+            int dev;
+            DeviceInfo* di;
+            if (current_device(&dev) != SGA_OK) return SGA_ERR_CUDA;
+            if ((st = device_info(dev, &di)) != SGA_OK) return st;
+            const size_t smem = R::smem_bytes(plan->rope_P);
+            if (smem > 227 * 1024) return SGA_ERR_UNSUPPORTED;
+            {
+                std::lock_guard<std::mutex> lk(g_dev_mu);
+                if (di->cr_smem < smem) {
+                    if (cudaFuncSetAttribute(R::compact_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem) != cudaSuccess)
+                        return SGA_ERR_CUDA;
+                    di->cr_smem = smem;
+                }
+            }
+            CUtensorMap mk, mv;
+            if ((st = make_map(&mk, K, plan->T, BH, R::kStageRows)) != SGA_OK) return st;
+            if ((st = make_map(&mv, V, plan->T, BH, R::kStageRows)) != SGA_OK) return st;
+            R::Args ra;
+            ra.T = plan->T;
+            ra.S = plan->S;
+            ra.rows_per_chunk = plan->rows_per_chunk;
+            ra.n_chunks = plan->n_chunks;
+            ra.n_items = (long long)BH * plan->n_chunks;
+            ra.KS = reinterpret_cast<__nv_bfloat16*>(K_S);
+            ra.VS = reinterpret_cast<__nv_bfloat16*>(V_S);
+            ra.partials = plan->d_partials;
+            ra.rope = a.rope;
+            ra.slot = plan->d_slot;
+            const long long cap = 2LL * di->sm_count;
+            const long long g = ra.n_items < cap ? ra.n_items : cap;
+            R::compact_rope_kernel<<<(unsigned)g, R::kThreads, smem, s>>>(mk, mv, ra);
+        } else
             sga::compact_kernel<__nv_bfloat16, false><<<grid, sga::kCompactThreads, 0, s>>>(a);
     } else {
+        if (rope_smem > 48 * 1024) return SGA_ERR_UNSUPPORTED;
         if (c.rope)
             sga::compact_kernel<float, true><<<grid, sga::kCompactThreads, rope_smem, s>>>(a);
         else

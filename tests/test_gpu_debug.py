@@ -96,6 +96,17 @@ op = oracle.plan(cfg.N, cfg.grid_h, cfg.grid_w, cfg.n_special, 3, 3, True, True)
 idx = torch.as_tensor(op.kv_index.astype(np.int64), device=dev)
 assert torch.equal(outs[0], k2[:, :, idx]) and torch.equal(outs[1], v2[:, :, idx])
 
+# the compaction with the rotary embedding (bf16: the TMA-fed kernel)
+rc = sga.SGAConfig(B=1, H=2, N=5, grid_h=11, grid_w=9, sigma=4, phase_shift=True, rope=True, rope_base=100.0,
+                   rope_pos_offset=1)
+_, k3, v3 = correlated_qkv(1, 2, rc.N, rc.L, 64, seed=90, dtype=torch.bfloat16, device=dev)
+K3, V3, _, _ = sga.Plan(rc, dev).compact(k3, v3)
+torch.cuda.synchronize(dev)
+opr = oracle.plan(rc.N, rc.grid_h, rc.grid_w, rc.n_special, 2, 2, True, True)
+for h in range(2):
+    kr = oracle.rope2d(host(k3[0, h]), rc.L, rc.n_special, rc.grid_w, rc.rope_base, rc.rope_pos_offset)
+    assert np.abs(host(K3[0, h]) - kr[opr.kv_index]).max() <= 8e-3 * max(1.0, np.abs(kr).max())
+
 assert sga.device_status(dev) == 0
 w = [ctypes.c_int64(-1) for _ in range(4)]
 assert sga.lib().sga_debug_report(*[ctypes.byref(x) for x in w]) == 0
