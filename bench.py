@@ -275,7 +275,8 @@ class Job:
                            ("attention", lambda: plan.forward(q, k, v, *bufs, out=out))]
             self.flops = layer_flops(cfg, plan.S)
             self.dominant = ("attention", "tensor", self.flops, "sga::tc::attn_tc_kernel<false>")
-            self.secondary = ("compaction", "hbm", compaction_bytes(cfg, plan.S), "sga::compact_kernel")
+            ck = "sga::cr::compact_rope_kernel" if (cfg.rope and cfg.dtype == "bf16") else "sga::compact_kernel"
+            self.secondary = ("compaction", "hbm", compaction_bytes(cfg, plan.S), ck)
             self.dtype = cfg.dtype
             self.config = {"B_per_rank": cfg.B, "H": cfg.H, "N": cfg.N, "L": cfg.L, "T": cfg.T, "S": plan.S,
                            "sigma": cfg.sigma, "flops_per_layer": self.flops}

@@ -312,7 +312,53 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         const long long mi = base + (rank[k] >= 0 ? rank[k] : rank[best[k - ws]]);
         if (SGA_CHECK_INDEX(tok(k), g.T, 20) && SGA_CHECK_INDEX(mi, g.M, 21)) map[tok(k)] = (int32_t)mi;
     }
-    // 7. group means of the kept entries (a destination plus the sources merged into it, summed
+    // 7. each destination's merged sources, in ascending entry order: counted, offsets scanned
+    //    and listed by one warp, 32 sources at a time (the lanes of one destination find each
+    //    other with a match), so the group sums below run over the members alone and in the
+    //    same order as before.  The lists reuse the similarity array (ws + n_src = nb entries).
+    int* cnt = reinterpret_cast<int*>(sim);                  // [ws]: count, then running position
+    int* list = cnt + ws;                                   // [n_src] members, destination-major
+    if (tid < 32) {
+        const int lane = tid;
+        for (int d = lane; d < ws; d += 32) cnt[d] = 0;
+        __syncwarp();
+        for (int c0 = 0; c0 < n_src; c0 += 32) {
+            const int a2 = c0 + lane;
+            const bool mg = a2 < n_src && rank[ws + a2] < 0;
+            const int d = mg ? best[a2] : -1;
+            const uint32_t m = __match_any_sync(0xffffffffu, d);
+            if (mg && lane == __ffs(m) - 1) cnt[d] += __popc(m);
+            __syncwarp();
+        }
+        // exclusive scan of the counts: cnt[d] becomes the first list position of d
+        int run = 0;
+        for (int d0 = 0; d0 < ws; d0 += 32) {
+            const int d = d0 + lane;
+            const int v = d < ws ? cnt[d] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (d < ws) cnt[d] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        __syncwarp();
+        for (int c0 = 0; c0 < n_src; c0 += 32) {
+            const int a2 = c0 + lane;
+            const bool mg = a2 < n_src && rank[ws + a2] < 0;
+            const int d = mg ? best[a2] : -1;
+            const uint32_t m = __match_any_sync(0xffffffffu, d);
+            if (mg) list[cnt[d] + __popc(m & ((1u << lane) - 1u))] = a2;
+            __syncwarp();
+            if (mg && lane == __ffs(m) - 1) cnt[d] += __popc(m);
+            __syncwarp();
+        }
+        // now cnt[d] is one past the last member of d; its first is cnt[d - 1] (0 for d = 0)
+    }
+    __syncthreads();
+    // 8. group means of the kept entries (a destination plus the sources merged into it, summed
     //    in entry order), 16 dimensions per work item, and ln of the group size
     for (int it = tid; it < nb * 4; it += kMergeThreads) {
         const int k = it >> 2, e0 = (it & 3) * 16;
@@ -323,12 +369,12 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) { sx[e] = xs[k * kXS + e0 + e]; sy[e] = 0.f; }
         if (Y) load16<T>(y_smem ? ys + k * 64 + e0 : Y + tok(k) * 64 + e0, sy);
-        int cnt = 1;
+        int cntk = 1;
         if (k < ws) {
-            for (int a2 = 0; a2 < n_src; ++a2) {
-                if (rank[ws + a2] >= 0 || best[a2] != k) continue;
-                ++cnt;
-                const int ks = ws + a2;
+            const int m_end = cnt[k], m_beg = k > 0 ? cnt[k - 1] : 0;
+            cntk += m_end - m_beg;
+            for (int q = m_beg; q < m_end; ++q) {
+                const int ks = ws + list[q];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) sx[e] += xs[ks * kXS + e0 + e];
                 if (Y) {
@@ -339,12 +385,12 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
                 }
             }
         }
-        const float inv = 1.0f / (float)cnt;
+        const float inv = 1.0f / (float)cntk;
 #pragma unroll
         for (int e = 0; e < 16; ++e) { sx[e] *= inv; sy[e] *= inv; }
         store16<T>(Xm + mi * 64 + e0, sx);
         if (Ym) store16<T>(Ym + mi * 64 + e0, sy);
-        if (lg && e0 == 0) lg[mi] = logf((float)cnt);
+        if (lg && e0 == 0) lg[mi] = logf((float)cntk);
     }
 }
 
