@@ -219,7 +219,8 @@ __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&s)[128]) {
     }
 }
 
-template <bool kBias, bool kRope>
+// kDefer: run a unit's epilogue after the next unit's first P (for short units; see below)
+template <bool kBias, bool kRope, bool kDefer>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const TcArgs p) {
@@ -536,8 +537,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_arrive(bars.q_rot(ul & 1));
             return true;
         };
-        // A unit's epilogue runs once this warpgroup has stored the next unit's first P: by then
-        // the unit's last PV is long complete.  Its row state waits in shared memory.
+        // With kDefer a unit's epilogue runs once this warpgroup has stored the next unit's first
+        // P: by then the unit's last PV is long complete.  That matters for short units
+        // (frame-local attention, 11 key tiles); for units of whole sequences the host launches
+        // the form that runs it straight after the unit, which needs fewer registers.  Either
+        // way the row state waits in shared memory.
         float* pend = reinterpret_cast<float*>(base + OFF_PEND) + (threadIdx.x - 128);
         auto epilogue = [&](uint32_t ul) -> bool {
             if (!warp_wait(bars.o_done(t), ul & 1, abort_flag)) return false;
@@ -723,7 +727,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 tc_fence_before();
                 mbar_arrive(bars.p_ready(sn % NUM_SBUF));
                 // the previous unit's epilogue, now that this unit's first P is out
-                if (first && u_local > 0 && !epilogue(u_local - 1)) return false;
+                if (kDefer && first && u_local > 0 && !epilogue(u_local - 1)) return false;
                 return true;
             };
             if (!tile(0, true)) { ok = false; break; }
@@ -741,8 +745,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             pend[5 * 256] = xr.inv_c;
             pend[6 * 256] = __int_as_float(valid ? seg : -1);
             pend[7 * 256] = __int_as_float(row);
+            if (!kDefer && !epilogue(u_local)) { ok = false; break; }
         }
-        if (ok && u_local > 0) epilogue(u_local - 1);
+        if (kDefer && ok && u_local > 0) epilogue(u_local - 1);
     }
 
     // ---------------------------------------------------------------------- teardown

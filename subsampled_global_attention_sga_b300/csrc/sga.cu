@@ -29,7 +29,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool init = false;
     int sm_count = 0;
-    bool tc_ready[2][2] = {};                                  // attn_tc_kernel<bias, rope> ready
+    bool tc_ready[2][2][2] = {};                               // attn_tc_kernel<bias, rope, defer> ready
     size_t cr_smem = 0;                                        // compact_rope_kernel: smem enabled
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -131,29 +131,29 @@ struct AttnProblem {
 // The tensor-core kernel instantiation for a bias setting, checked once per device: its
 // setmaxnreg split assumes exactly LAUNCH_REGS registers per thread at launch (any other count
 // would leave setmaxnreg.inc unsatisfiable), and it needs the large dynamic shared memory.
-template <bool kBias, bool kRope>
+template <bool kBias, bool kRope, bool kDefer>
 sga_status prepare_tc(DeviceInfo* di) {
     namespace T = sga::tc;
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (di->tc_ready[kBias][kRope]) return SGA_OK;
+    if (di->tc_ready[kBias][kRope][kDefer]) return SGA_OK;
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias, kRope>) != cudaSuccess) return SGA_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, T::attn_tc_kernel<kBias, kRope, kDefer>) != cudaSuccess) return SGA_ERR_CUDA;
     if (fa.numRegs != (int)T::LAUNCH_REGS) return SGA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias, kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(T::attn_tc_kernel<kBias, kRope, kDefer>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_BYTES) != cudaSuccess)
         return SGA_ERR_CUDA;
-    di->tc_ready[kBias][kRope] = true;
+    di->tc_ready[kBias][kRope][kDefer] = true;
     return SGA_OK;
 }
 
 // Launch one instantiation of the tensor-core kernel.
-template <bool kBias, bool kRope>
+template <bool kBias, bool kRope, bool kDefer>
 sga_status launch_tc(DeviceInfo* di, long long grid, const CUtensorMap& mq, const CUtensorMap& mk,
                      const CUtensorMap& mv, const sga::tc::TcArgs& a, cudaStream_t stream) {
     namespace T = sga::tc;
-    sga_status st = prepare_tc<kBias, kRope>(di);
+    sga_status st = prepare_tc<kBias, kRope, kDefer>(di);
     if (st != SGA_OK) return st;
-    T::attn_tc_kernel<kBias, kRope><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+    T::attn_tc_kernel<kBias, kRope, kDefer><<<(unsigned)grid, T::NUM_THREADS, T::SMEM_BYTES, stream>>>(mq, mk, mv, a);
     return launch_status();
 }
 
@@ -197,9 +197,17 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.inv_scale = 1.0f / pb.scale;
         a.drop_kv = pb.drop_kv;
         const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
-        if (pb.bias) return launch_tc<true, false>(di, grid, mq, mk, mv, a, stream);
-        if (pb.rope) return launch_tc<false, true>(di, grid, mq, mk, mv, a, stream);
-        return launch_tc<false, false>(di, grid, mq, mk, mv, a, stream);
+        // short units (up to 32 key tiles: frame-local attention, small layers) defer each unit's
+        // epilogue past the next unit's first P; units of whole sequences do not need to
+        const bool defer = a.n_kv_tiles <= 32;
+        if (pb.bias)
+            return defer ? launch_tc<true, false, true>(di, grid, mq, mk, mv, a, stream)
+                         : launch_tc<true, false, false>(di, grid, mq, mk, mv, a, stream);
+        if (pb.rope)
+            return defer ? launch_tc<false, true, true>(di, grid, mq, mk, mv, a, stream)
+                         : launch_tc<false, true, false>(di, grid, mq, mk, mv, a, stream);
+        return defer ? launch_tc<false, false, true>(di, grid, mq, mk, mv, a, stream)
+                     : launch_tc<false, false, false>(di, grid, mq, mk, mv, a, stream);
     }
     if (kern != SGA_KERNEL_SIMT) return SGA_ERR_INVALID_ARG;
     sga::SimtArgs a;
