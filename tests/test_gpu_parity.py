@@ -180,6 +180,25 @@ def test_dense_and_frame_variants(dev, kernel):
         _compare(_host(of)[0, h], ref, "bf16", "frame")
 
 
+@pytest.mark.parametrize("T", [32 * 128, 32 * 128 + 77])
+def test_dense_at_the_epilogue_form_boundary(dev, T):
+    """Units of up to 32 key tiles run each unit's epilogue after the next unit's first P, longer
+    ones straight after the unit (two template instances of the kernel, chosen by the host):
+    4096 keys are the last size of the first form, 4173 (33 tiles, the last one ragged) the
+    first of the second; both against the oracle on every row, several units per CTA."""
+    H = 2
+    q, k, v = correlated_qkv(1, H, 1, T, 64, seed=21, dtype=torch.bfloat16, device=dev)
+    g = guarded(q.shape, q.dtype, dev)
+    od = sga.dense_forward(q, k, v, out=g.t)
+    torch.cuda.synchronize(dev)
+    g.check("dense")
+    qf, kf, vf = _host(q), _host(k), _host(v)
+    rows = np.arange(T)
+    for h in range(H):
+        ref, _ = oracle.attention_rows(qf[0, h], kf[0, h], vf[0, h], rows)
+        _compare(_host(od)[0, h], ref, "bf16", f"dense T={T} h{h}")
+
+
 def test_dense_frame_f32(dev):
     N, L, H = 2, 70, 2
     q, k, v = correlated_qkv(1, H, N, L, 64, seed=6, dtype=torch.float32, device=dev)
