@@ -107,6 +107,7 @@ struct TcArgs {
     ExtraArgs ex;           // ex.on only for SGA (segment = batch*head)
     const float* bias;      // [n_seg, kv_rows] natural-log per-key bias (size-aware variant)
     float inv_scale;        // 1 / scale
+    int store32;            // 1: O is 32-byte aligned, rows are stored as four 32-byte sectors
     long long drop_kv;      // failure-detection self-test: the producer never loads this key
                             // tile (global ring index), so its wait expires; -1 in normal use
 };
@@ -207,6 +208,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     const bool ok = mbar_wait(bar, parity, abort_flag);
     return __all_sync(0xffffffffu, ok);
+}
+
+// 32-byte global store (sm_100+), address 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(p), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7) : "memory");
 }
 
 __device__ __forceinline__ void ld_row128(uint32_t taddr, float (&s)[128]) {
@@ -570,15 +578,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 const float inv_l = 1.0f / l;
                 const long long grow = (long long)seg * p.seg_rows + row;
-                uint4* dst = reinterpret_cast<uint4*>(p.O + grow * 64);
+                uint32_t w[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 w;
-                    w.x = pack_bf16x2(o[8 * c + 0] * inv_l, o[8 * c + 1] * inv_l);
-                    w.y = pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l);
-                    w.z = pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l);
-                    w.w = pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l);
-                    dst[c] = w;
+                for (int c = 0; c < 32; ++c) w[c] = pack_bf16x2(o[2 * c] * inv_l, o[2 * c + 1] * inv_l);
+                if (p.store32) {
+                    // whole 32-byte sectors: a warp's store writes 32 full sectors, not 32 halves
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        st_global_v8(p.O + grow * 64 + 16 * c, w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3],
+                                     w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(p.O + grow * 64);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
                 }
                 if (p.lse) p.lse[grow] = (m + log2f(l)) * 0.69314718055994531f;
             }

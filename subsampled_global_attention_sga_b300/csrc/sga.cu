@@ -196,6 +196,8 @@ sga_status run_attention(const AttnProblem& pb, cudaStream_t stream) {
         a.bias = pb.bias;
         a.inv_scale = 1.0f / pb.scale;
         a.drop_kv = pb.drop_kv;
+        // outputs are only required to be 16-byte aligned; whole-sector stores need 32
+        a.store32 = (reinterpret_cast<uintptr_t>(pb.O) & 31) == 0 ? 1 : 0;
         const long long grid = a.n_units < di->sm_count ? a.n_units : di->sm_count;
         // short units (up to 32 key tiles: frame-local attention, small layers) defer each unit's
         // epilogue past the next unit's first P; units of whole sequences do not need to

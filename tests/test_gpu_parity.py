@@ -199,6 +199,26 @@ def test_dense_at_the_epilogue_form_boundary(dev, T):
         _compare(_host(od)[0, h], ref, "bf16", f"dense T={T} h{h}")
 
 
+def test_output_only_16_byte_aligned(dev):
+    """The epilogue writes each row as four 32-byte sectors when O is 32-byte aligned; the entry
+    points only require 16, and an output at an odd multiple of 16 bytes takes the 16-byte
+    stores.  Both must give the oracle's rows and leave the neighbours untouched."""
+    N, L, H = 2, 300, 2
+    q, k, v = correlated_qkv(1, H, N, L, 64, seed=22, dtype=torch.bfloat16, device=dev)
+    n = q.numel()
+    buf = torch.full((n + 2 * 4096 + 8,), float("nan"), dtype=torch.bfloat16, device=dev)
+    out = buf[4096 + 8:4096 + 8 + n].view(q.shape)          # 8 bf16 = 16 bytes past a 32-byte boundary
+    assert out.data_ptr() % 32 == 16
+    sga.dense_forward(q, k, v, out=out)
+    torch.cuda.synchronize(dev)
+    assert torch.isnan(buf[:4096 + 8]).all() and torch.isnan(buf[4096 + 8 + n:]).all()
+    qf, kf, vf = _host(q), _host(k), _host(v)
+    rows = np.arange(N * L)
+    for h in range(H):
+        ref, _ = oracle.attention_rows(qf[0, h], kf[0, h], vf[0, h], rows)
+        _compare(_host(out)[0, h], ref, "bf16", "dense, 16-byte aligned output")
+
+
 def test_dense_frame_f32(dev):
     N, L, H = 2, 70, 2
     q, k, v = correlated_qkv(1, H, N, L, 64, seed=6, dtype=torch.float32, device=dev)
