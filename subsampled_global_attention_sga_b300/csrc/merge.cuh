@@ -71,9 +71,41 @@ struct MergeArgs {
 //   ranks, and the per-warp totals of the rank scan.
 constexpr int kXS = 68;                // row stride of the fp32 X rows in shared memory
 __host__ __device__ constexpr int merge_partials(int nb_max) { return nb_max > kMergeThreads ? nb_max : kMergeThreads; }
-__host__ __device__ constexpr int merge_smem_bytes(int nb_max, int elem_bytes, bool y_smem) {
+__host__ __device__ constexpr int merge_smem_bytes(int nb_max, int elem_bytes, bool y_smem, bool x_f32 = true) {
     return (y_smem ? nb_max * 64 * elem_bytes : 0) +
-           4 * (nb_max * kXS + nb_max + 2 * merge_partials(nb_max) + nb_max + kMergeThreads / 32);
+           4 * ((x_f32 ? nb_max * kXS : 0) + nb_max + 2 * merge_partials(nb_max) + nb_max + kMergeThreads / 32);
+}
+
+// The tensor-core matching (bf16 keys, at most 128 sources and 128 destinations per block): one
+// tcgen05.mma computes every (source, destination) dot product at once, A = the block's source
+// rows (128 x 64), B = its destination rows (Npad x 64), both in shared memory with the
+// 128-byte swizzle, D in Tensor Memory.  Its fp32 sums come in the tensor core's order, so
+// they only shortlist: a destination whose approximate cosine is within kMatchWindow of the
+// best one gets the exact fixed-order fma chain, and the first maximum of the exact cosines
+// decides, as before.  The window: the products of bf16 values are exact; an fp32 sum of 64 of
+// them in any order is within 64 ulp-steps, under 2^-17 of sum |x_i b_i|, which Cauchy-Schwarz
+// bounds by the product of the norms; so the approximate and exact cosines differ by less than
+// 2^-16 (plus the divisions' rounding), and every destination whose exact cosine could reach
+// the maximum lies within 2^-15 of the best approximate one.  kMatchWindow = 2^-10 leaves a
+// factor 32 for the tensor core's accumulation order and rounding.
+constexpr float kMatchWindow = 9.765625e-4f;          // 2^-10
+constexpr int kTcMaxSrc = 128;                          // sources per block (one M = 128 tile)
+constexpr int kTcMaxDst = 128;                          // destinations per block (N <= 128)
+__host__ __device__ constexpr int merge_tc_npad(int ws_max) { return ((ws_max + 15) / 16) * 16; }
+// shared memory added by the tensor-core path: the A and B tiles (1024-byte aligned), the
+// mbarrier and the TMEM address
+__host__ __device__ constexpr int merge_tc_extra_bytes(int ws_max) {
+    return 2048 + kTcMaxSrc * 128 + merge_tc_npad(ws_max) * 128;    // + alignment slack
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
 }
 
 // 16 consecutive elements of a row (generic address: shared or global) to fp32
@@ -115,8 +147,9 @@ __device__ __forceinline__ void store16(T* dst, const float (&x)[16]) {
 }
 
 // grid: (n_windows + 1, n_chunks, BH); blockIdx.x == n_windows handles the chunk's specials.
-template <typename T>
-__global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
+template <typename T, bool kTC>
+__global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(MergeArgs a) {
+    static_assert(!kTC || sizeof(T) == 2, "the tensor-core matching takes bf16 keys");
     constexpr int VPR = 64 * (int)sizeof(T) / 16;       // 16-byte vectors per row
     constexpr int EPV = 16 / (int)sizeof(T);            // elements per vector
     const MergeGeom& g = a.g;
@@ -164,12 +197,39 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     T* ys = reinterpret_cast<T*>(smem);                                     // [nb][64] when staged
     float* xs = reinterpret_cast<float*>(smem + (a.y_smem ? nb_max * 64 * (int)sizeof(T) : 0));  // [nb][kXS]
-    float* nrm = xs + nb_max * kXS;                                         // [nb]
+    float* nrm = xs + (kTC ? 0 : nb_max * kXS);                             // [nb]
     float* sim = nrm + nb_max;                                              // partials, then [n_src]
     int* best = reinterpret_cast<int*>(sim + merge_partials(nb_max));      // partials, then [n_src]
     int* rank = best + merge_partials(nb_max);                              // [nb]: merged index in block, or -1
     int* wtot = rank + nb_max;                                              // [8] warp totals of the scan
+    // tensor-core path: mbarrier, TMEM address, then the A (sources) and B (destinations) tiles
+    uint8_t* tc_misc = reinterpret_cast<uint8_t*>(wtot + kMergeThreads / 32);
+    tc_misc = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_misc) + 7) & ~uintptr_t(7));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tc_misc + 8);
+    uint8_t* tileA = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_misc + 16) + 1023) & ~uintptr_t(1023));
+    uint8_t* tileB = tileA + kTcMaxSrc * 128;
+    const int npad = merge_tc_npad(ws);
+    const uint32_t tmem_cols = npad <= 32 ? 32u : npad <= 64 ? 64u : 128u;
+    if constexpr (kTC) {
+        if (tid < 32) {
+            tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+            tmem_relinquish();
+        }
+        if (tid == 0) {
+            mbar_init(smem_u32(tc_misc), 1);
+            mbar_fence_init();
+        }
+    }
 
+    // tensor-core path: entry k's row lives only in its bf16 tile (B: destinations, A:
+    // sources); 8 dims of 16-byte chunk c, exactly as fp32
+    auto xchunk = [&](int k, int c, float (&x)[8]) {
+        const int row = k < ws ? k : k - ws;
+        const uint8_t* tile = k < ws ? tileB : tileA;
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4));
+        x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+        x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+    };
     auto tok = [&](int i) -> long long {                        // token of block entry i
         return (long long)(f0 + i / ws) * g.L + g.n_special + (long long)w * g.n_s + i % ws;
     };
@@ -179,7 +239,8 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         const long long t = tok(k);
         const uint4 wv = __ldg(reinterpret_cast<const uint4*>(X + t * 64) + v);
         float4* dst = reinterpret_cast<float4*>(xs + k * kXS + v * EPV);
-        if constexpr (sizeof(T) == 2) {
+        if constexpr (kTC) {
+        } else if constexpr (sizeof(T) == 2) {
             dst[0] = make_float4(bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y));
             dst[1] = make_float4(bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w));
         } else {
@@ -187,19 +248,38 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
                                  __uint_as_float(wv.w));
         }
         if (y_smem) reinterpret_cast<uint4*>(ys + k * 64)[v] = __ldg(reinterpret_cast<const uint4*>(Y + t * 64) + v);
+        if constexpr (kTC) {
+            // the raw bf16 row into its tile, 16-byte chunk v of row r at chunk v ^ (r mod 8)
+            const int row = k < ws ? k : k - ws;
+            uint8_t* tile = k < ws ? tileB : tileA;
+            *reinterpret_cast<uint4*>(tile + row * 128 + ((v ^ (row & 7)) << 4)) = wv;
+        }
     }
+    if constexpr (kTC) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     // 2. norms: sqrt_rn of the fma chain of squares, dimensions in order
     for (int k = tid; k < nb; k += kMergeThreads) {
-        const float4* row = reinterpret_cast<const float4*>(xs + k * kXS);
         float s = 0.f;
+        if constexpr (kTC) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const float4 x = row[q];
-            s = __fmaf_rn(x.x, x.x, s);
-            s = __fmaf_rn(x.y, x.y, s);
-            s = __fmaf_rn(x.z, x.z, s);
-            s = __fmaf_rn(x.w, x.w, s);
+            for (int c = 0; c < 8; ++c) {
+                float x[8];
+                xchunk(k, c, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s = __fmaf_rn(x[e], x[e], s);
+            }
+        } else {
+            const float4* row = reinterpret_cast<const float4*>(xs + k * kXS);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 x = row[q];
+                s = __fmaf_rn(x.x, x.x, s);
+                s = __fmaf_rn(x.y, x.y, s);
+                s = __fmaf_rn(x.z, x.z, s);
+                s = __fmaf_rn(x.w, x.w, s);
+            }
         }
         nrm[k] = __fsqrt_rn(s);
     }
@@ -209,6 +289,89 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
     //    The destinations are split into G contiguous groups so that all threads work; each
     //    (source, group) item keeps four dot products in flight, and the groups' first maxima are
     //    combined in ascending order, which gives the first maximum over all destinations.
+    if constexpr (kTC) {
+        const uint32_t tmem = *tmem_slot;
+        const uint32_t bar = smem_u32(tc_misc);
+        if (tid == 0 && n_src > 0) {
+            const uint64_t dA = smem_desc_sw128(smem_u32(tileA), 16);
+            const uint64_t dB = smem_desc_sw128(smem_u32(tileB), 16);
+            const uint32_t idesc = idesc_bf16_f32(128, npad, false);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem, dA + 2 * kk, dB + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+            mma_commit(bar);
+        }
+        if (tid < 128 && n_src > 0) {
+            // one thread per source (TMEM lane); the wait is bounded
+            const long long t0 = clock64();
+            while (!mbar_try_wait(bar, 0)) {
+                if (clock64() - t0 > kTimeoutCycles) {
+                    atomicExch(&g_status, (int)SGA_ERR_TIMEOUT);
+                    break;
+                }
+            }
+            tc_fence_after();
+            const int a2 = tid;
+            const bool live = a2 < n_src;
+            const uint32_t taddr = tmem + ((uint32_t)(tid & ~31) << 16);
+            const float nk = live ? nrm[ws + a2] : 0.f;
+            // pass 1: the best approximate cosine
+            float amax = -INFINITY;
+            for (int c0 = 0; c0 < npad; c0 += 16) {
+                uint32_t r16[16];
+                tmem_ld16(taddr + c0, r16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int d = c0 + i;
+                    if (live && d < ws) {
+                        const float den = __fmul_rn(nk, nrm[d]);
+                        const float ac = den == 0.f ? 0.f : __fdividef(__uint_as_float(r16[i]), den);
+                        amax = fmaxf(amax, ac);
+                    }
+                }
+            }
+            // pass 2: the exact cosine of every destination within the window, in ascending
+            // order; the first maximum decides
+            float bs = -INFINITY;
+            int bd = -1;
+            for (int c0 = 0; c0 < npad; c0 += 16) {
+                uint32_t r16[16];
+                tmem_ld16(taddr + c0, r16);
+                tmem_wait_ld();
+                uint32_t cand = 0;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int d = c0 + i;
+                    if (live && d < ws) {
+                        const float den = __fmul_rn(nk, nrm[d]);
+                        const float ac = den == 0.f ? 0.f : __fdividef(__uint_as_float(r16[i]), den);
+                        if (ac >= amax - kMatchWindow) cand |= 1u << i;
+                    }
+                }
+                for (; cand; cand &= cand - 1) {
+                    const int d = c0 + __ffs(cand) - 1;
+                    const float den = __fmul_rn(nk, nrm[d]);
+                    float dot = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float u[8], w[8];
+                        xchunk(ws + a2, c, u);
+                        xchunk(d, c, w);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) dot = __fmaf_rn(u[e], w[e], dot);
+                    }
+                    const float cs = den == 0.f ? 0.f : __fdiv_rn(dot, den);
+                    if (cs > bs) { bs = cs; bd = d; }
+                }
+            }
+            if (live) {
+                sim[a2] = bs;
+                best[a2] = bd;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    } else {
     const int G = n_src > 0 ? max(1, min(4, kMergeThreads / n_src)) : 1;
     for (int it = tid; it < n_src * G; it += kMergeThreads) {
         const int a2 = it % n_src, grp = it / n_src;
@@ -268,6 +431,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
             best[a2] = bd;
         }
         __syncthreads();
+    }
     }
     // 4. merged sources: the r largest similarities (ties: lower token index = lower entry index,
     //    since entries are in token order)
@@ -367,7 +531,19 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         if (!SGA_CHECK_INDEX(mi, g.M, 21)) continue;
         float sx[16], sy[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) { sx[e] = xs[k * kXS + e0 + e]; sy[e] = 0.f; }
+        for (int e = 0; e < 16; ++e) sy[e] = 0.f;
+        if constexpr (kTC) {
+            float x8[8];
+            xchunk(k, e0 >> 3, x8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sx[e] = x8[e];
+            xchunk(k, (e0 >> 3) + 1, x8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sx[8 + e] = x8[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sx[e] = xs[k * kXS + e0 + e];
+        }
         if (Y) load16<T>(y_smem ? ys + k * 64 + e0 : Y + tok(k) * 64 + e0, sy);
         int cntk = 1;
         if (k < ws) {
@@ -375,8 +551,18 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
             cntk += m_end - m_beg;
             for (int q = m_beg; q < m_end; ++q) {
                 const int ks = ws + list[q];
+                if constexpr (kTC) {
+                    float x8[8];
+                    xchunk(ks, e0 >> 3, x8);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) sx[e] += xs[ks * kXS + e0 + e];
+                    for (int e = 0; e < 8; ++e) sx[e] += x8[e];
+                    xchunk(ks, (e0 >> 3) + 1, x8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sx[8 + e] += x8[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sx[e] += xs[ks * kXS + e0 + e];
+                }
                 if (Y) {
                     float ty[16];
                     load16<T>(y_smem ? ys + ks * 64 + e0 : Y + tok(ks) * 64 + e0, ty);
@@ -391,6 +577,14 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(MergeArgs a) {
         store16<T>(Xm + mi * 64 + e0, sx);
         if (Ym) store16<T>(Ym + mi * 64 + e0, sy);
         if (lg && e0 == 0) lg[mi] = logf((float)cntk);
+    }
+    if constexpr (kTC) {
+        tc_fence_before();
+        __syncthreads();
+        if (tid < 32) {
+            tc_fence_after();
+            tmem_dealloc(*tmem_slot, tmem_cols);
+        }
     }
 }
 

@@ -832,7 +832,7 @@ sga_status merge_geom(const sga_merge_config* c, sga::MergeGeom* g) {
     return SGA_OK;
 }
 
-bool g_merge_smem_set[kMaxDevices][2];
+bool g_merge_smem_set[kMaxDevices][3];
 
 }  // namespace
 
@@ -865,19 +865,27 @@ sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, 
     int optin = 0;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return SGA_ERR_CUDA;
+    // bf16 blocks of at most 128 sources and 128 destinations match on the tensor cores (their
+    // rows then live in shared memory as bf16 tiles only); other blocks on the CUDA cores
+    const bool tc = di == 0 && (g.n_t - 1) * g.n_s <= sga::kTcMaxSrc && g.n_s <= sga::kTcMaxDst;
+    const int ki = tc ? 2 : di;
+    const int extra = tc ? sga::merge_tc_extra_bytes(g.n_s) : 0;
     // the values are staged in shared memory beside the keys when both fit
-    const bool y_smem = Y != nullptr && sga::merge_smem_bytes(nb_max, elem, true) <= optin;
-    const int smem = sga::merge_smem_bytes(nb_max, elem, y_smem);
+    const bool y_smem = Y != nullptr && sga::merge_smem_bytes(nb_max, elem, true, !tc) + extra <= optin;
+    const int smem = sga::merge_smem_bytes(nb_max, elem, y_smem, !tc) + extra;
     if (smem > optin) return SGA_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
-        if (!g_merge_smem_set[dev][di]) {
-            const cudaError_t e = di == 0 ? cudaFuncSetAttribute(sga::merge_kernel<__nv_bfloat16>,
-                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin)
-                                          : cudaFuncSetAttribute(sga::merge_kernel<float>,
-                                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (!g_merge_smem_set[dev][ki]) {
+            const cudaError_t e =
+                ki == 2 ? cudaFuncSetAttribute(sga::merge_kernel<__nv_bfloat16, true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, optin)
+                : ki == 0 ? cudaFuncSetAttribute(sga::merge_kernel<__nv_bfloat16, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin)
+                          : cudaFuncSetAttribute(sga::merge_kernel<float, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
             if (e != cudaSuccess) return SGA_ERR_CUDA;
-            g_merge_smem_set[dev][di] = true;
+            g_merge_smem_set[dev][ki] = true;
         }
     }
     sga::MergeArgs a;
@@ -892,10 +900,12 @@ sga_status sga_merge(const sga_merge_config* cfg, const void* X, const void* Y, 
     a.y_smem = y_smem ? 1 : 0;
     dim3 grid((unsigned)g.n_windows + 1, (unsigned)g.n_chunks, (unsigned)(cfg->B * cfg->H));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (di == 0)
-        sga::merge_kernel<__nv_bfloat16><<<grid, sga::kMergeThreads, smem, s>>>(a);
+    if (tc)
+        sga::merge_kernel<__nv_bfloat16, true><<<grid, sga::kMergeThreads, smem, s>>>(a);
+    else if (di == 0)
+        sga::merge_kernel<__nv_bfloat16, false><<<grid, sga::kMergeThreads, smem, s>>>(a);
     else
-        sga::merge_kernel<float><<<grid, sga::kMergeThreads, smem, s>>>(a);
+        sga::merge_kernel<float, false><<<grid, sga::kMergeThreads, smem, s>>>(a);
     return launch_status();
 }
 
