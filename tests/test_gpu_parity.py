@@ -582,6 +582,22 @@ def test_rope_sga_full(dev, kernel, sigma, phase, base, off):
         assert np.abs(lse[0, h].cpu().numpy() - rl).max() < 2e-3
 
 
+def test_rope_sga_odd_heads_and_tiles(dev):
+    """Three heads of 258 tokens: 3 query tiles per head, so the last tiles of heads 0 and 1 share
+    a mixed unit and head 2's sits in one that repeats it (odd segment count); the units are short,
+    so each epilogue runs after the next unit's first P.  Every row against the oracle."""
+    cfg = sga.SGAConfig(B=1, H=3, N=3, grid_h=9, grid_w=9, sigma=4, kernel="tc", rope=True, rope_base=100.0,
+                        rope_pos_offset=1)
+    assert cfg.T == 258
+    q, k, v = correlated_qkv(1, 3, cfg.N, cfg.L, 64, seed=95, dtype=torch.bfloat16, device=dev)
+    _, out, lse, _ = _run(cfg, q, k, v, dev, lse=True)
+    op = _oracle_plan(cfg)
+    for h in range(3):
+        ref, rl = oracle.sga_full(op, _rope_ref(q[0, h], cfg), _rope_ref(k[0, h], cfg), _host(v[0, h]))
+        _compare(_host(out[0, h]), ref, "bf16", f"rope odd h{h}")
+        assert np.abs(lse[0, h].cpu().numpy() - rl).max() < 2e-3
+
+
 def test_rope_sga_f32(dev):
     cfg = sga.SGAConfig(B=1, H=2, N=4, grid_h=9, grid_w=7, sigma=6, phase_shift=True, dtype="f32", rope=True)
     q, k, v = correlated_qkv(1, 2, cfg.N, cfg.L, 64, seed=92, dtype=torch.float32, device=dev)
@@ -696,6 +712,30 @@ def test_merge_matches_oracle(dev, dtype, tdt, n_t, n_s, r):
     for b in range(2):
         for h in range(2):
             _merge_check(mc, k, v, Km, Vm, lg, mp, b, h)
+
+
+def test_merge_ties_zero_rows_and_near_ties(dev):
+    """Inputs built to stress the tensor-core shortlist (approximate cosines, exact decision):
+    two identical destinations with a source equal to both (an exact tie: the lower index wins),
+    an all-zero source (every cosine is 0: the first destination wins), and a destination one
+    bf16 step away from another with a source equal to the first.  The partition must equal the
+    oracle's bit for bit."""
+    mc = sga.MergeConfig(B=1, H=1, N=4, grid_h=6, grid_w=7, n_t=4, n_s=7, r_permille=500)
+    L = mc.n_special + mc.grid_h * mc.grid_w
+    _, k, v = correlated_qkv(1, 1, mc.N, L, 64, seed=131, dtype=torch.bfloat16, device=dev)
+    tok = lambda f, p: f * L + mc.n_special + p              # frame f, patch p
+    x = k[0, 0]
+    x[tok(0, 1)] = x[tok(0, 0)]                             # window 0: duplicate destinations
+    x[tok(1, 3)] = x[tok(0, 0)]                             #   and a source equal to both
+    x[tok(2, 9)] = 0                                        # window 1: an all-zero source
+    x[tok(0, 15)] = x[tok(0, 14)]                           # window 2: destinations one step apart
+    e = x[tok(0, 15), 5:6].clone()
+    x[tok(0, 15), 5:6] = (e.view(torch.int16) + 1).view(torch.bfloat16)   # one bf16 step
+    x[tok(3, 16)] = x[tok(0, 14)]                           #   and a source equal to the first
+    Km, Vm, lg, mp = _merge_guarded(mc, k, v)
+    torch.cuda.synchronize(dev)
+    assert sga.device_status(dev) == 0
+    _merge_check(mc, k, v, Km, Vm, lg, mp, 0, 0)
 
 
 @pytest.mark.parametrize("dtype,tdt", [("bf16", torch.bfloat16), ("f32", torch.float32)])
