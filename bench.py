@@ -95,6 +95,9 @@ TRAFFIC_GB = {
     # Q tiles released at the unit's last key tile, plus the self-test's skipped-tile hook (off
     # in this launch): 170.49 + 2.44 GB; same 1.38 s, the kernel is not bound by DRAM
     "58b57bb8c27c1a5d": {"headline": 172.93},
+    # slots numbered across units, mixed units, the epilogue forms, whole-sector output stores:
+    # 114.51 + 3.40 GB (1.15 s; L2 evict-last hints on the K/V tiles left it at 116.8 GB)
+    "094d1d58d00a412f": {"headline": 117.91},
 }
 
 
