@@ -91,11 +91,13 @@ __host__ __device__ constexpr int merge_smem_bytes(int nb_max, int elem_bytes, b
 constexpr float kMatchWindow = 9.765625e-4f;          // 2^-10
 constexpr int kTcMaxSrc = 128;                          // sources per block (one M = 128 tile)
 constexpr int kTcMaxDst = 128;                          // destinations per block (N <= 128)
+constexpr int kTcList = 8;                              // shortlist entries kept per source
 __host__ __device__ constexpr int merge_tc_npad(int ws_max) { return ((ws_max + 15) / 16) * 16; }
 // shared memory added by the tensor-core path: the A and B tiles (1024-byte aligned), the
-// mbarrier and the TMEM address
+// mbarrier and the TMEM address, the destinations' inverse norms and the sources' shortlists
 __host__ __device__ constexpr int merge_tc_extra_bytes(int ws_max) {
-    return 2048 + kTcMaxSrc * 128 + merge_tc_npad(ws_max) * 128;    // + alignment slack
+    return 2048 + kTcMaxSrc * 128 + merge_tc_npad(ws_max) * 128 +   // + alignment slack
+           4 * kTcMaxDst + kTcList * kTcMaxSrc;
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -208,6 +210,8 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tc_misc + 8);
     uint8_t* tileA = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_misc + 16) + 1023) & ~uintptr_t(1023));
     uint8_t* tileB = tileA + kTcMaxSrc * 128;
+    float* inv_nd = reinterpret_cast<float*>(tileB + merge_tc_npad(ws) * 128);   // [ws]: 1 / n_d, or 0
+    uint8_t* shortlist = reinterpret_cast<uint8_t*>(inv_nd + kTcMaxDst);        // [kTcList][128]
     const int npad = merge_tc_npad(ws);
     const uint32_t tmem_cols = npad <= 32 ? 32u : npad <= 64 ? 64u : 128u;
     if constexpr (kTC) {
@@ -282,6 +286,7 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
             }
         }
         nrm[k] = __fsqrt_rn(s);
+        if (kTC && k < ws) inv_nd[k] = s == 0.f ? 0.f : __frcp_rn(nrm[k]);
     }
     __syncthreads();
     // 3. every source (entries ws .. nb-1) finds its destination (entries 0 .. ws-1): the first
@@ -314,56 +319,57 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
             const bool live = a2 < n_src;
             const uint32_t taddr = tmem + ((uint32_t)(tid & ~31) << 16);
             const float nk = live ? nrm[ws + a2] : 0.f;
-            // pass 1: the best approximate cosine
+            // pass 1: the best approximate cosine, scaled by n_k (the TMEM sum times 1 / n_d)
             float amax = -INFINITY;
             for (int c0 = 0; c0 < npad; c0 += 16) {
                 uint32_t r16[16];
                 tmem_ld16(taddr + c0, r16);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int d = c0 + i;
-                    if (live && d < ws) {
-                        const float den = __fmul_rn(nk, nrm[d]);
-                        const float ac = den == 0.f ? 0.f : __fdividef(__uint_as_float(r16[i]), den);
-                        amax = fmaxf(amax, ac);
-                    }
-                }
+                for (int i = 0; i < 16; ++i)
+                    if (c0 + i < ws) amax = fmaxf(amax, __fmul_rn(__uint_as_float(r16[i]), inv_nd[c0 + i]));
             }
-            // pass 2: the exact cosine of every destination within the window, in ascending
-            // order; the first maximum decides
-            float bs = -INFINITY;
-            int bd = -1;
+            // pass 2: the destinations within the window, in ascending order, onto the source's
+            // shortlist; the exact chains run after it, with the warp's lanes together
+            const float thr = amax - kMatchWindow * nk;
+            int n_cand = 0;
             for (int c0 = 0; c0 < npad; c0 += 16) {
                 uint32_t r16[16];
                 tmem_ld16(taddr + c0, r16);
                 tmem_wait_ld();
-                uint32_t cand = 0;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int d = c0 + i;
-                    if (live && d < ws) {
-                        const float den = __fmul_rn(nk, nrm[d]);
-                        const float ac = den == 0.f ? 0.f : __fdividef(__uint_as_float(r16[i]), den);
-                        if (ac >= amax - kMatchWindow) cand |= 1u << i;
+                    if (d < ws && live && __fmul_rn(__uint_as_float(r16[i]), inv_nd[d]) >= thr) {
+                        if (n_cand < kTcList) shortlist[n_cand * kTcMaxSrc + a2] = (uint8_t)d;
+                        ++n_cand;
                     }
-                }
-                for (; cand; cand &= cand - 1) {
-                    const int d = c0 + __ffs(cand) - 1;
-                    const float den = __fmul_rn(nk, nrm[d]);
-                    float dot = 0.f;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        float u[8], w[8];
-                        xchunk(ws + a2, c, u);
-                        xchunk(d, c, w);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) dot = __fmaf_rn(u[e], w[e], dot);
-                    }
-                    const float cs = den == 0.f ? 0.f : __fdiv_rn(dot, den);
-                    if (cs > bs) { bs = cs; bd = d; }
                 }
             }
+            // the exact cosine of each candidate; the first maximum decides.  A shortlist that
+            // overflowed (near-equal destinations) goes on with every destination after its last
+            // entry: a superset of the candidates, and every destination that could reach the
+            // maximum is a candidate, so the first maximum is the same.
+            float bs = -INFINITY;
+            int bd = -1;
+            auto verify = [&](int d) {
+                const float den = __fmul_rn(nk, nrm[d]);
+                float dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float u[8], w[8];
+                    xchunk(ws + a2, c, u);
+                    xchunk(d, c, w);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) dot = __fmaf_rn(u[e], w[e], dot);
+                }
+                const float cs = den == 0.f ? 0.f : __fdiv_rn(dot, den);
+                if (cs > bs) { bs = cs; bd = d; }
+            };
+            const int n_list = min(n_cand, kTcList);
+            for (int k = 0; k < n_list; ++k) verify(shortlist[k * kTcMaxSrc + a2]);
+            if (n_cand > kTcList)
+                for (int d = shortlist[(kTcList - 1) * kTcMaxSrc + a2] + 1; d < ws; ++d) verify(d);
             if (live) {
                 sim[a2] = bs;
                 best[a2] = bd;
