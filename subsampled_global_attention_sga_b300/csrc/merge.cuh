@@ -67,13 +67,13 @@ struct MergeArgs {
 // Dynamic shared memory of one block, sized for nb_max entries:
 //   Y rows as stored (only when staged), X rows as fp32 with a padded stride of 68 floats (rows
 //   16-byte aligned: a warp's per-thread float4 row reads are conflict-free and a destination
-//   row is broadcast four values per load), norms, similarity / destination partials (at least one per thread), kept
-//   ranks, and the per-warp totals of the rank scan.
+//   row is broadcast four values per load), norms, similarity / destination partials (at least
+//   one per thread), and one bit per source that says whether it is merged.
 constexpr int kXS = 68;                // row stride of the fp32 X rows in shared memory
 __host__ __device__ constexpr int merge_partials(int nb_max) { return nb_max > kMergeThreads ? nb_max : kMergeThreads; }
 __host__ __device__ constexpr int merge_smem_bytes(int nb_max, int elem_bytes, bool y_smem, bool x_f32 = true) {
     return (y_smem ? nb_max * 64 * elem_bytes : 0) +
-           4 * ((x_f32 ? nb_max * kXS : 0) + nb_max + 2 * merge_partials(nb_max) + nb_max + kMergeThreads / 32);
+           4 * ((x_f32 ? nb_max * kXS : 0) + nb_max + 2 * merge_partials(nb_max) + (nb_max + 31) / 32);
 }
 
 // The tensor-core matching (bf16 keys, at most 128 sources and 128 destinations per block): one
@@ -109,6 +109,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+
+// 16 bytes from global to shared memory without passing through registers; the copies of a
+// thread complete in the order of their commit groups
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_global) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src_global) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory"); }
 
 // 16 consecutive elements of a row (generic address: shared or global) to fp32
 template <typename T>
@@ -202,10 +211,9 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
     float* nrm = xs + (kTC ? 0 : nb_max * kXS);                             // [nb]
     float* sim = nrm + nb_max;                                              // partials, then [n_src]
     int* best = reinterpret_cast<int*>(sim + merge_partials(nb_max));      // partials, then [n_src]
-    int* rank = best + merge_partials(nb_max);                              // [nb]: merged index in block, or -1
-    int* wtot = rank + nb_max;                                              // [8] warp totals of the scan
+    uint32_t* mflag = reinterpret_cast<uint32_t*>(best + merge_partials(nb_max));   // merged-source bits
     // tensor-core path: mbarrier, TMEM address, then the A (sources) and B (destinations) tiles
-    uint8_t* tc_misc = reinterpret_cast<uint8_t*>(wtot + kMergeThreads / 32);
+    uint8_t* tc_misc = reinterpret_cast<uint8_t*>(mflag + (nb_max + 31) / 32);
     tc_misc = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_misc) + 7) & ~uintptr_t(7));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tc_misc + 8);
     uint8_t* tileA = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_misc + 16) + 1023) & ~uintptr_t(1023));
@@ -234,29 +242,46 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
         x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
         x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
     };
-    auto tok = [&](int i) -> long long {                        // token of block entry i
-        return (long long)(f0 + i / ws) * g.L + g.n_special + (long long)w * g.n_s + i % ws;
+    // token of block entry i; its frame i / ws from a float product: i + 1/2 lies at least 1/2
+    // from every multiple of ws, and the product's error, under (i / ws + 1) 2^-22, stays below
+    // 1 / (2 ws) while nb < 2^20 (a block's rows fit in shared memory)
+    const float inv_ws = 1.0f / (float)ws;
+    auto tok = [&](int i) -> long long {
+        const int fi = (int)(((float)i + 0.5f) * inv_ws);
+        return (long long)(f0 + fi) * g.L + g.n_special + (long long)w * g.n_s + (i - fi * ws);
     };
-    // 1. the block's rows: X as fp32 (exact), Y as stored
-    for (int i = tid; i < nb * VPR; i += kMergeThreads) {
-        const int k = i / VPR, v = i % VPR;
-        const long long t = tok(k);
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(X + t * 64) + v);
-        float4* dst = reinterpret_cast<float4*>(xs + k * kXS + v * EPV);
-        if constexpr (kTC) {
-        } else if constexpr (sizeof(T) == 2) {
-            dst[0] = make_float4(bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y));
-            dst[1] = make_float4(bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w));
-        } else {
-            dst[0] = make_float4(__uint_as_float(wv.x), __uint_as_float(wv.y), __uint_as_float(wv.z),
-                                 __uint_as_float(wv.w));
-        }
-        if (y_smem) reinterpret_cast<uint4*>(ys + k * 64)[v] = __ldg(reinterpret_cast<const uint4*>(Y + t * 64) + v);
-        if constexpr (kTC) {
-            // the raw bf16 row into its tile, 16-byte chunk v of row r at chunk v ^ (r mod 8)
+    // 1. the block's rows: X as fp32 (exact), Y as stored.  The tensor-core path copies both
+    //    straight into shared memory, X (the bf16 tiles) and Y in two commit groups, so that the
+    //    values arrive while the keys are matched.
+    if constexpr (kTC) {
+        for (int i = tid; i < nb * VPR; i += kMergeThreads) {
+            const int k = i / VPR, v = i % VPR;
             const int row = k < ws ? k : k - ws;
             uint8_t* tile = k < ws ? tileB : tileA;
-            *reinterpret_cast<uint4*>(tile + row * 128 + ((v ^ (row & 7)) << 4)) = wv;
+            cp_async16(tile + row * 128 + ((v ^ (row & 7)) << 4), reinterpret_cast<const uint4*>(X + tok(k) * 64) + v);
+        }
+        cp_async_commit();
+        if (y_smem)
+            for (int i = tid; i < nb * VPR; i += kMergeThreads) {
+                const int k = i / VPR, v = i % VPR;
+                cp_async16(reinterpret_cast<uint4*>(ys + k * 64) + v, reinterpret_cast<const uint4*>(Y + tok(k) * 64) + v);
+            }
+        cp_async_commit();
+        cp_async_wait<1>();
+    } else {
+        for (int i = tid; i < nb * VPR; i += kMergeThreads) {
+            const int k = i / VPR, v = i % VPR;
+            const long long t = tok(k);
+            const uint4 wv = __ldg(reinterpret_cast<const uint4*>(X + t * 64) + v);
+            float4* dst = reinterpret_cast<float4*>(xs + k * kXS + v * EPV);
+            if constexpr (sizeof(T) == 2) {
+                dst[0] = make_float4(bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y));
+                dst[1] = make_float4(bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w));
+            } else {
+                dst[0] = make_float4(__uint_as_float(wv.x), __uint_as_float(wv.y), __uint_as_float(wv.z),
+                                     __uint_as_float(wv.w));
+            }
+            if (y_smem) reinterpret_cast<uint4*>(ys + k * 64)[v] = __ldg(reinterpret_cast<const uint4*>(Y + t * 64) + v);
         }
     }
     if constexpr (kTC) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -288,6 +313,7 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
         nrm[k] = __fsqrt_rn(s);
         if (kTC && k < ws) inv_nd[k] = s == 0.f ? 0.f : __frcp_rn(nrm[k]);
     }
+    if (kTC && tid >= ws && tid < npad) inv_nd[tid] = __int_as_float(0x7fffffff);
     __syncthreads();
     // 3. every source (entries ws .. nb-1) finds its destination (entries 0 .. ws-1): the first
     //    maximum of cos = dot / (n_a * n_b), each dot an fma chain over the dimensions in order.
@@ -326,8 +352,7 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
                 tmem_ld16(taddr + c0, r16);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (c0 + i < ws) amax = fmaxf(amax, __fmul_rn(__uint_as_float(r16[i]), inv_nd[c0 + i]));
+                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, __fmul_rn(__uint_as_float(r16[i]), inv_nd[c0 + i]));
             }
             // pass 2: the destinations within the window, in ascending order, onto the source's
             // shortlist; the exact chains run after it, with the warp's lanes together
@@ -337,13 +362,14 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
                 uint32_t r16[16];
                 tmem_ld16(taddr + c0, r16);
                 tmem_wait_ld();
+                uint32_t cand = 0;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int d = c0 + i;
-                    if (d < ws && live && __fmul_rn(__uint_as_float(r16[i]), inv_nd[d]) >= thr) {
-                        if (n_cand < kTcList) shortlist[n_cand * kTcMaxSrc + a2] = (uint8_t)d;
-                        ++n_cand;
-                    }
+                for (int i = 0; i < 16; ++i)
+                    cand |= __fmul_rn(__uint_as_float(r16[i]), inv_nd[c0 + i]) >= thr ? 1u << i : 0u;
+                if (!live) cand = 0;
+                for (; cand; cand &= cand - 1) {
+                    if (n_cand < kTcList) shortlist[n_cand * kTcMaxSrc + a2] = (uint8_t)(c0 + __ffs(cand) - 1);
+                    ++n_cand;
                 }
             }
             // the exact cosine of each candidate; the first maximum decides.  A shortlist that
@@ -352,24 +378,31 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
             // maximum is a candidate, so the first maximum is the same.
             float bs = -INFINITY;
             int bd = -1;
+            const uint8_t* row_a = tileA + a2 * 128;
             auto verify = [&](int d) {
                 const float den = __fmul_rn(nk, nrm[d]);
+                const uint8_t* row_d = tileB + d * 128;
                 float dot = 0.f;
-#pragma unroll
+#pragma unroll 2
                 for (int c = 0; c < 8; ++c) {
-                    float u[8], w[8];
-                    xchunk(ws + a2, c, u);
-                    xchunk(d, c, w);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) dot = __fmaf_rn(u[e], w[e], dot);
+                    const uint4 u = *reinterpret_cast<const uint4*>(row_a + ((c ^ (a2 & 7)) << 4));
+                    const uint4 v = *reinterpret_cast<const uint4*>(row_d + ((c ^ (d & 7)) << 4));
+                    dot = __fmaf_rn(bf16_lo(u.x), bf16_lo(v.x), dot);
+                    dot = __fmaf_rn(bf16_hi(u.x), bf16_hi(v.x), dot);
+                    dot = __fmaf_rn(bf16_lo(u.y), bf16_lo(v.y), dot);
+                    dot = __fmaf_rn(bf16_hi(u.y), bf16_hi(v.y), dot);
+                    dot = __fmaf_rn(bf16_lo(u.z), bf16_lo(v.z), dot);
+                    dot = __fmaf_rn(bf16_hi(u.z), bf16_hi(v.z), dot);
+                    dot = __fmaf_rn(bf16_lo(u.w), bf16_lo(v.w), dot);
+                    dot = __fmaf_rn(bf16_hi(u.w), bf16_hi(v.w), dot);
                 }
                 const float cs = den == 0.f ? 0.f : __fdiv_rn(dot, den);
                 if (cs > bs) { bs = cs; bd = d; }
             };
-            const int n_list = min(n_cand, kTcList);
-            for (int k = 0; k < n_list; ++k) verify(shortlist[k * kTcMaxSrc + a2]);
-            if (n_cand > kTcList)
-                for (int d = shortlist[(kTcList - 1) * kTcMaxSrc + a2] + 1; d < ws; ++d) verify(d);
+            const int d_last = n_cand > kTcList ? shortlist[(kTcList - 1) * kTcMaxSrc + a2] : ws - 1;
+            const int n_ver = n_cand > kTcList ? kTcList + (ws - 1 - d_last) : n_cand;
+            for (int k = 0; k < n_ver; ++k)
+                verify(k < kTcList ? shortlist[k * kTcMaxSrc + a2] : d_last + 1 + (k - kTcList));
             if (live) {
                 sim[a2] = bs;
                 best[a2] = bd;
@@ -440,101 +473,49 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
     }
     }
     // 4. merged sources: the r largest similarities (ties: lower token index = lower entry index,
-    //    since entries are in token order)
-    for (int k = tid; k < nb; k += kMergeThreads) {
+    //    since entries are in token order); one flag bit per source, a warp's 32 in one word
+    for (int a0 = 0; a0 < n_src; a0 += kMergeThreads) {
+        const int a2 = a0 + tid;
         bool merged = false;
-        if (k >= ws) {
-            const int a2 = k - ws;
+        if (a2 < n_src) {
             const float sa = sim[a2];
-            long long ahead = 0;
+            int ahead = 0;
             for (int b2 = 0; b2 < n_src; ++b2) {
                 const float sb = sim[b2];
                 ahead += (sb > sa || (sb == sa && b2 < a2)) ? 1 : 0;
             }
             merged = ahead < r;
         }
-        rank[k] = merged ? -1 : 0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, merged);
+        const int w0 = a0 + (tid & ~31);
+        if ((tid & 31) == 0 && w0 < n_src) mflag[w0 >> 5] = bal;
+    }
+    if constexpr (kTC) {
+        cp_async_wait<0>();                                  // this thread's value rows
+        if (tid < 32) {
+            tc_fence_after();
+            tmem_dealloc(*tmem_slot, tmem_cols);             // the TMEM reads ended before phase 4
+        }
     }
     __syncthreads();
-    // 5. kept entries get consecutive merged indices in entry (= token) order: a block-wide
-    //    exclusive scan of the kept flags, 256 entries per round
-    {
-        const int warp = tid >> 5, lane = tid & 31;
-        int carry = 0;
-        for (int b0 = 0; b0 < nb; b0 += kMergeThreads) {
-            const int k = b0 + tid;
-            const bool kept = k < nb && rank[k] >= 0;
-            const uint32_t bal = __ballot_sync(0xffffffffu, kept);
-            if (lane == 0) wtot[warp] = __popc(bal);
-            __syncthreads();
-            int before = carry, total = carry;
-            for (int q = 0; q < kMergeThreads / 32; ++q) {
-                before += q < warp ? wtot[q] : 0;
-                total += wtot[q];
-            }
-            if (kept) rank[k] = before + __popc(bal & ((1u << lane) - 1u));
-            carry = total;
-            __syncthreads();
-        }
-    }
-    // 6. map: every token to its merged row (a merged source to its destination's)
-    for (int k = tid; k < nb; k += kMergeThreads) {
-        const long long mi = base + (rank[k] >= 0 ? rank[k] : rank[best[k - ws]]);
-        if (SGA_CHECK_INDEX(tok(k), g.T, 20) && SGA_CHECK_INDEX(mi, g.M, 21)) map[tok(k)] = (int32_t)mi;
-    }
-    // 7. each destination's merged sources, in ascending entry order: counted, offsets scanned
-    //    and listed by one warp, 32 sources at a time (the lanes of one destination find each
-    //    other with a match), so the group sums below run over the members alone and in the
-    //    same order as before.  The lists reuse the similarity array (ws + n_src = nb entries).
-    int* cnt = reinterpret_cast<int*>(sim);                  // [ws]: count, then running position
-    int* list = cnt + ws;                                   // [n_src] members, destination-major
-    if (tid < 32) {
-        const int lane = tid;
-        for (int d = lane; d < ws; d += 32) cnt[d] = 0;
-        __syncwarp();
-        for (int c0 = 0; c0 < n_src; c0 += 32) {
-            const int a2 = c0 + lane;
-            const bool mg = a2 < n_src && rank[ws + a2] < 0;
-            const int d = mg ? best[a2] : -1;
-            const uint32_t m = __match_any_sync(0xffffffffu, d);
-            if (mg && lane == __ffs(m) - 1) cnt[d] += __popc(m);
-            __syncwarp();
-        }
-        // exclusive scan of the counts: cnt[d] becomes the first list position of d
-        int run = 0;
-        for (int d0 = 0; d0 < ws; d0 += 32) {
-            const int d = d0 + lane;
-            const int v = d < ws ? cnt[d] : 0;
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
-            }
-            if (d < ws) cnt[d] = run + incl - v;
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        __syncwarp();
-        for (int c0 = 0; c0 < n_src; c0 += 32) {
-            const int a2 = c0 + lane;
-            const bool mg = a2 < n_src && rank[ws + a2] < 0;
-            const int d = mg ? best[a2] : -1;
-            const uint32_t m = __match_any_sync(0xffffffffu, d);
-            if (mg) list[cnt[d] + __popc(m & ((1u << lane) - 1u))] = a2;
-            __syncwarp();
-            if (mg && lane == __ffs(m) - 1) cnt[d] += __popc(m);
-            __syncwarp();
-        }
-        // now cnt[d] is one past the last member of d; its first is cnt[d - 1] (0 for d = 0)
-    }
-    __syncthreads();
+    // 5. kept entries get consecutive merged indices in entry (= token) order: the destinations
+    //    (entries 0 .. ws-1, never merged) keep their entry index, a kept source loses one for
+    //    every merged source before it
+    auto is_merged = [&](int a2) -> bool { return (mflag[a2 >> 5] >> (a2 & 31)) & 1u; };
+    auto kept_index = [&](int k) -> int {
+        if (k < ws) return k;
+        const int a2 = k - ws;
+        int before = __popc(mflag[a2 >> 5] & ((1u << (a2 & 31)) - 1u));
+        for (int q = 0; q < (a2 >> 5); ++q) before += __popc(mflag[q]);
+        return k - before;
+    };
     // 8. group means of the kept entries (a destination plus the sources merged into it, summed
     //    in entry order), 16 dimensions per work item, and ln of the group size
-    for (int it = tid; it < nb * 4; it += kMergeThreads) {
-        const int k = it >> 2, e0 = (it & 3) * 16;
-        if (rank[k] < 0) continue;
-        const long long mi = base + rank[k];
-        if (!SGA_CHECK_INDEX(mi, g.M, 21)) continue;
+    int* cnt = reinterpret_cast<int*>(sim);                  // [ws]: count, then running position
+    int* list = cnt + ws;                                   // [n_src] members, destination-major
+    auto mean_item = [&](int k, int e0) {
+        const long long mi = base + kept_index(k);
+        if (!SGA_CHECK_INDEX(mi, g.M, 21)) return;
         float sx[16], sy[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) sy[e] = 0.f;
@@ -583,15 +564,66 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
         store16<T>(Xm + mi * 64 + e0, sx);
         if (Ym) store16<T>(Ym + mi * 64 + e0, sy);
         if (lg && e0 == 0) lg[mi] = logf((float)cntk);
-    }
-    if constexpr (kTC) {
-        tc_fence_before();
-        __syncthreads();
-        if (tid < 32) {
-            tc_fence_after();
-            tmem_dealloc(*tmem_slot, tmem_cols);
+    };
+    if (tid < 32) {
+        // 7. each destination's merged sources, in ascending entry order: counted, offsets
+        //    scanned and listed by one warp, 32 sources at a time (the lanes of one destination
+        //    find each other with a match), so the group sums run over the members alone and in
+        //    the same order as before.  The lists reuse the similarity array (ws + n_src = nb
+        //    entries).  The other warps meanwhile write the map and the kept sources' rows.
+        const int lane = tid;
+        for (int d = lane; d < ws; d += 32) cnt[d] = 0;
+        __syncwarp();
+        for (int c0 = 0; c0 < n_src; c0 += 32) {
+            const int a2 = c0 + lane;
+            const bool mg = a2 < n_src && is_merged(a2);
+            const int d = mg ? best[a2] : -1;
+            const uint32_t m = __match_any_sync(0xffffffffu, d);
+            if (mg && lane == __ffs(m) - 1) cnt[d] += __popc(m);
+            __syncwarp();
+        }
+        // exclusive scan of the counts: cnt[d] becomes the first list position of d
+        int run = 0;
+        for (int d0 = 0; d0 < ws; d0 += 32) {
+            const int d = d0 + lane;
+            const int v = d < ws ? cnt[d] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (d < ws) cnt[d] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        __syncwarp();
+        for (int c0 = 0; c0 < n_src; c0 += 32) {
+            const int a2 = c0 + lane;
+            const bool mg = a2 < n_src && is_merged(a2);
+            const int d = mg ? best[a2] : -1;
+            const uint32_t m = __match_any_sync(0xffffffffu, d);
+            if (mg) list[cnt[d] + __popc(m & ((1u << lane) - 1u))] = a2;
+            __syncwarp();
+            if (mg && lane == __ffs(m) - 1) cnt[d] += __popc(m);
+            __syncwarp();
+        }
+        // now cnt[d] is one past the last member of d; its first is cnt[d - 1] (0 for d = 0)
+    } else {
+        // 6. map: every token to its merged row (a merged source to its destination's, whose
+        //    merged index is its entry index)
+        for (int k = tid - 32; k < nb; k += kMergeThreads - 32) {
+            const long long mi = base + (k >= ws && is_merged(k - ws) ? best[k - ws] : kept_index(k));
+            if (SGA_CHECK_INDEX(tok(k), g.T, 20) && SGA_CHECK_INDEX(mi, g.M, 21)) map[tok(k)] = (int32_t)mi;
+        }
+        // 8a. the kept sources' rows (groups of one)
+        for (int it = tid - 32; it < n_src * 4; it += kMergeThreads - 32) {
+            const int k = ws + (it >> 2);
+            if (!is_merged(k - ws)) mean_item(k, (it & 3) * 16);
         }
     }
+    __syncthreads();
+    // 8b. the destinations' group means
+    for (int it = tid; it < ws * 4; it += kMergeThreads) mean_item(it >> 2, (it & 3) * 16);
 }
 
 
