@@ -110,6 +110,47 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
+// fp32 arithmetic on a bf16 operand taken straight from its half of a packed word: the
+// mixed-precision fma / add of sm_100 and later round once, as fmaf / fadd of the operand
+// widened to fp32 do (the widening is exact), so the results are the same bits
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %3;}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float add_bf16_lo(uint32_t a, float c) {
+    float d;
+    asm("{.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %1;\n\tadd.rn.f32.bf16 %0, al, %2;}" : "=f"(d) : "r"(a), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float add_bf16_hi(uint32_t a, float c) {
+    float d;
+    asm("{.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %1;\n\tadd.rn.f32.bf16 %0, ah, %2;}" : "=f"(d) : "r"(a), "f"(c));
+    return d;
+}
+// the dot product of two 8-element bf16 chunks, continuing the fma chain s in element order
+__device__ __forceinline__ float fma_chain8(const uint4& u, const uint4& v, float s) {
+    s = fma_bf16_lo(u.x, v.x, s); s = fma_bf16_hi(u.x, v.x, s);
+    s = fma_bf16_lo(u.y, v.y, s); s = fma_bf16_hi(u.y, v.y, s);
+    s = fma_bf16_lo(u.z, v.z, s); s = fma_bf16_hi(u.z, v.z, s);
+    s = fma_bf16_lo(u.w, v.w, s); s = fma_bf16_hi(u.w, v.w, s);
+    return s;
+}
+// x[0..7] += the 8 bf16 elements of a chunk
+__device__ __forceinline__ void add_chunk8(const uint4& u, float* x) {
+    x[0] = add_bf16_lo(u.x, x[0]); x[1] = add_bf16_hi(u.x, x[1]);
+    x[2] = add_bf16_lo(u.y, x[2]); x[3] = add_bf16_hi(u.y, x[3]);
+    x[4] = add_bf16_lo(u.z, x[4]); x[5] = add_bf16_hi(u.z, x[5]);
+    x[6] = add_bf16_lo(u.w, x[6]); x[7] = add_bf16_hi(u.w, x[7]);
+}
+
 // 16 bytes from global to shared memory without passing through registers; the copies of a
 // thread complete in the order of their commit groups
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_global) {
@@ -235,6 +276,11 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
 
     // tensor-core path: entry k's row lives only in its bf16 tile (B: destinations, A:
     // sources); 8 dims of 16-byte chunk c, exactly as fp32
+    auto tchunk = [&](int k, int c) -> uint4 {                  // the raw 16 bytes
+        const int row = k < ws ? k : k - ws;
+        const uint8_t* tile = k < ws ? tileB : tileA;
+        return *reinterpret_cast<const uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4));
+    };
     auto xchunk = [&](int k, int c, float (&x)[8]) {
         const int row = k < ws ? k : k - ws;
         const uint8_t* tile = k < ws ? tileB : tileA;
@@ -294,10 +340,8 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
         if constexpr (kTC) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                float x[8];
-                xchunk(k, c, x);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s = __fmaf_rn(x[e], x[e], s);
+                const uint4 u = tchunk(k, c);
+                s = fma_chain8(u, u, s);
             }
         } else {
             const float4* row = reinterpret_cast<const float4*>(xs + k * kXS);
@@ -387,14 +431,7 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
                 for (int c = 0; c < 8; ++c) {
                     const uint4 u = *reinterpret_cast<const uint4*>(row_a + ((c ^ (a2 & 7)) << 4));
                     const uint4 v = *reinterpret_cast<const uint4*>(row_d + ((c ^ (d & 7)) << 4));
-                    dot = __fmaf_rn(bf16_lo(u.x), bf16_lo(v.x), dot);
-                    dot = __fmaf_rn(bf16_hi(u.x), bf16_hi(v.x), dot);
-                    dot = __fmaf_rn(bf16_lo(u.y), bf16_lo(v.y), dot);
-                    dot = __fmaf_rn(bf16_hi(u.y), bf16_hi(v.y), dot);
-                    dot = __fmaf_rn(bf16_lo(u.z), bf16_lo(v.z), dot);
-                    dot = __fmaf_rn(bf16_hi(u.z), bf16_hi(v.z), dot);
-                    dot = __fmaf_rn(bf16_lo(u.w), bf16_lo(v.w), dot);
-                    dot = __fmaf_rn(bf16_hi(u.w), bf16_hi(v.w), dot);
+                    dot = fma_chain8(u, v, dot);
                 }
                 const float cs = den == 0.f ? 0.f : __fdiv_rn(dot, den);
                 if (cs > bs) { bs = cs; bd = d; }
@@ -539,13 +576,14 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
             for (int q = m_beg; q < m_end; ++q) {
                 const int ks = ws + list[q];
                 if constexpr (kTC) {
-                    float x8[8];
-                    xchunk(ks, e0 >> 3, x8);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) sx[e] += x8[e];
-                    xchunk(ks, (e0 >> 3) + 1, x8);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) sx[8 + e] += x8[e];
+                    add_chunk8(tchunk(ks, e0 >> 3), sx);
+                    add_chunk8(tchunk(ks, (e0 >> 3) + 1), sx + 8);
+                    if (Y) {
+                        const uint4* yr = reinterpret_cast<const uint4*>(y_smem ? ys + ks * 64 + e0 : Y + tok(ks) * 64 + e0);
+                        add_chunk8(yr[0], sy);
+                        add_chunk8(yr[1], sy + 8);
+                    }
+                    continue;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) sx[e] += xs[ks * kXS + e0 + e];
@@ -615,10 +653,27 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
             const long long mi = base + (k >= ws && is_merged(k - ws) ? best[k - ws] : kept_index(k));
             if (SGA_CHECK_INDEX(tok(k), g.T, 20) && SGA_CHECK_INDEX(mi, g.M, 21)) map[tok(k)] = (int32_t)mi;
         }
-        // 8a. the kept sources' rows (groups of one)
-        for (int it = tid - 32; it < n_src * 4; it += kMergeThreads - 32) {
-            const int k = ws + (it >> 2);
-            if (!is_merged(k - ws)) mean_item(k, (it & 3) * 16);
+        // 8a. the kept sources' rows (groups of one): the mean of one row is the row itself, so
+        //    the tensor-core path copies its 16-byte chunks (and ln 1 = 0)
+        if constexpr (kTC) {
+            for (int it = tid - 32; it < n_src * VPR; it += kMergeThreads - 32) {
+                const int a2 = it / VPR, v = it % VPR;
+                if (is_merged(a2)) continue;
+                const int k = ws + a2;
+                const long long mi = base + kept_index(k);
+                if (!SGA_CHECK_INDEX(mi, g.M, 21)) continue;
+                reinterpret_cast<uint4*>(Xm + mi * 64)[v] = tchunk(k, v);
+                if (Ym)
+                    reinterpret_cast<uint4*>(Ym + mi * 64)[v] =
+                        y_smem ? reinterpret_cast<const uint4*>(ys + k * 64)[v]
+                               : __ldg(reinterpret_cast<const uint4*>(Y + tok(k) * 64) + v);
+                if (lg && v == 0) lg[mi] = 0.f;
+            }
+        } else {
+            for (int it = tid - 32; it < n_src * 4; it += kMergeThreads - 32) {
+                const int k = ws + (it >> 2);
+                if (!is_merged(k - ws)) mean_item(k, (it & 3) * 16);
+            }
         }
     }
     __syncthreads();
