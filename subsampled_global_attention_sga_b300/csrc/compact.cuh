@@ -249,16 +249,28 @@ __global__ void __launch_bounds__(kCompactThreads, kRope ? 2 : 1) compact_kernel
     }
 }
 
-// k_sum/v_sum[bh][d] = sum over chunks (in order) of the partials.
-__global__ void __launch_bounds__(128) compact_finalize_kernel(const float* partials, int n_chunks,
-                                                               float* k_sum, float* v_sum) {
+// k_sum/v_sum[bh][d] = the partials in a fixed order: the chunks cut into kFinalizeRuns
+// consecutive runs, each summed in chunk order by its own thread, then the run sums in order.
+// (One chain over all the chunks made the sum a long series of dependent loads.)
+constexpr int kFinalizeRuns = 8;
+__global__ void __launch_bounds__(128 * kFinalizeRuns) compact_finalize_kernel(const float* partials, int n_chunks,
+                                                                               float* k_sum, float* v_sum) {
+    __shared__ float run_sum[kFinalizeRuns][128];
     const int bh = blockIdx.x;
-    const int j = threadIdx.x;
+    const int j = threadIdx.x & 127, run = threadIdx.x >> 7;
+    const int c0 = (int)((long long)run * n_chunks / kFinalizeRuns);
+    const int c1 = (int)((long long)(run + 1) * n_chunks / kFinalizeRuns);
     const float* p = partials + (long long)bh * n_chunks * 128 + j;
     float s = 0.f;
-    for (int c = 0; c < n_chunks; ++c) s += p[(long long)c * 128];
-    if (j < 64) k_sum[bh * 64 + j] = s;
-    else v_sum[bh * 64 + (j - 64)] = s;
+    for (int c = c0; c < c1; ++c) s += p[(long long)c * 128];
+    run_sum[run][j] = s;
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        float t = 0.f;
+        for (int r = 0; r < kFinalizeRuns; ++r) t += run_sum[r][j];
+        if (j < 64) k_sum[bh * 64 + j] = t;
+        else v_sum[bh * 64 + (j - 64)] = t;
+    }
 }
 
 }  // namespace sga

@@ -680,7 +680,8 @@ sga_status sga_compact(sga_plan_t plan, const void* K, const void* V, void* K_S,
             sga::compact_kernel<float, false><<<grid, sga::kCompactThreads, 0, s>>>(a);
     }
     if ((st = launch_status()) != SGA_OK) return st;
-    sga::compact_finalize_kernel<<<BH, 128, 0, s>>>(plan->d_partials, plan->n_chunks, k_sum, v_sum);
+    sga::compact_finalize_kernel<<<BH, 128 * sga::kFinalizeRuns, 0, s>>>(plan->d_partials, plan->n_chunks, k_sum,
+                                                                        v_sum);
     return launch_status();
 }
 
@@ -1396,6 +1397,7 @@ extern "C" sga_status sga_compact_noalloc(const sga_config* cfg, const void* K, 
     else
         sga::compact_noalloc_kernel<float><<<grid, sga::kCompactThreads, 0, s>>>(a);
     if ((st = launch_status()) != SGA_OK) return st;
-    sga::compact_finalize_kernel<<<(unsigned)BH, 128, 0, s>>>(scratch, (int)n_chunks, k_sum, v_sum);
+    sga::compact_finalize_kernel<<<(unsigned)BH, 128 * sga::kFinalizeRuns, 0, s>>>(scratch, (int)n_chunks, k_sum,
+                                                                                  v_sum);
     return launch_status();
 }
