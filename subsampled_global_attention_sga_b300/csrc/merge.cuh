@@ -361,9 +361,11 @@ __global__ void __launch_bounds__(kMergeThreads, kTC ? 4 : 3) merge_kernel(Merge
     __syncthreads();
     // 3. every source (entries ws .. nb-1) finds its destination (entries 0 .. ws-1): the first
     //    maximum of cos = dot / (n_a * n_b), each dot an fma chain over the dimensions in order.
-    //    The destinations are split into G contiguous groups so that all threads work; each
-    //    (source, group) item keeps four dot products in flight, and the groups' first maxima are
-    //    combined in ascending order, which gives the first maximum over all destinations.
+    //    The tensor-core path shortlists with one MMA and runs the chains on the shortlist only.
+    //    The CUDA-core path splits the destinations into G contiguous groups so that all threads
+    //    work; each (source, group) item keeps four dot products in flight, and the groups' first
+    //    maxima are combined in ascending order, which gives the first maximum over all
+    //    destinations.
     if constexpr (kTC) {
         const uint32_t tmem = *tmem_slot;
         const uint32_t bar = smem_u32(tc_misc);
